@@ -1,0 +1,305 @@
+/*
+ * Paged-attention decode oracle: a plain, slow CPU implementation in double
+ * precision. TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the
+ * CPU-baseline leg of the benchmark are its only users; the product path never
+ * links or calls it. It shares no code with the CUDA library.
+ *
+ * What it computes (the plain definition the split-KV kernels reach up to
+ * rounding):
+ *
+ *   For sequence b, query index i in [0, QL), query head h, KV head
+ *   g = h / (Hq / Hkv)  (GQA grouping, PR "Add paged-attention Tile kernel",
+ *   host wrapper: query_group_size = num_q_heads // num_kv_heads):
+ *     L = ctx_lens[b], query position p = L - QL + i (the context includes the
+ *     new tokens: PR "Merge gfx1250 PA decode partitions ...", the non-causal
+ *     commit note says one row's causal bound is the whole context);
+ *     visible tokens T = { t in [0, L) : (!causal || t <= p)
+ *                                        && (W == 0 || t > p - W) }
+ *       (a window of W tokens includes the query's own token, so W = 1 leaves
+ *        only t = p; PR "Extend packed D256 PA decode pipe ...", Validation,
+ *        windows 0/1/17/257/8193);
+ *     sparse decode instead uses T = { idx[b][j] : 0 <= idx < L }.
+ *     K/V row of token t: page = block_table[b][t / S], slot = t % S,
+ *       dequantised exactly (FP8 e4m3fn code times its per-tensor or per-token
+ *       scale; BF16 widened), PR "Add paged-attention Tile kernel" (scales are
+ *       a scalar or [num_blocks, num_kv_heads, block_size]).
+ *     x_t = sm_scale * sum_d q[d] * k[d]
+ *     with sink s_h: m = max(max_t x_t, s_h), den = sum_t e^(x_t-m) + e^(s_h-m)
+ *     without:        m = max_t x_t,          den = sum_t e^(x_t-m)
+ *     out = sum_t e^(x_t-m) v_t / den; out = 0 when T is empty.
+ *
+ * Reading of the pages where they are silent (also listed in the design
+ * notes): the sink is an extra logit in natural-log units, not multiplied by
+ * sm_scale, with no value row; an empty visible set gives zeros, sink or not.
+ *
+ * Partials and their merge (PR "Merge gfx1250 PA decode partitions ...",
+ * Partition merges): a partial over a token subset is (m, l, O) with
+ * m = max x_t, l = sum e^(x_t - m), O = sum e^(x_t - m) v_t; merging a list of
+ * partials in order gives M = max(m_j [, s]), L = sum l_j e^(m_j - M)
+ * [+ e^(s - M)], out = sum O_j e^(m_j - M) / L.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define PA_ORACLE_OK 0
+#define PA_ORACLE_BAD_ARG 1
+#define PA_ORACLE_BAD_PAGE 2
+#define PA_ORACLE_NO_MEM 3
+
+enum { ORACLE_KV_FP8 = 0, ORACLE_KV_BF16 = 1 };
+enum { ORACLE_SCALE_NONE = 0, ORACLE_SCALE_PER_TENSOR = 1, ORACLE_SCALE_PER_TOKEN = 2 };
+
+typedef struct {
+  int batch;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_dim;
+  int query_len;
+  int page_size;
+  int max_pages_per_seq;
+  int num_pages;
+  int kv_dtype;   /* ORACLE_KV_FP8 or ORACLE_KV_BF16 */
+  int scale_mode; /* ORACLE_SCALE_* (FP8 only) */
+  int causal;
+  int window; /* 0 = off */
+  int has_sinks;
+  int topk; /* 0 = dense decode; > 0 = sparse index-list decode (QL must be 1) */
+  double sm_scale;
+} pa_oracle_shape;
+
+/* OCP 8-bit floating point, E4M3 ("fn": no infinities, S.1111.111 is NaN):
+ * exponent bias 7, normal value (1 + m/8) * 2^(e-7), subnormal (m/8) * 2^-6. */
+double pa_oracle_e4m3_to_double(uint8_t code) {
+  int sign = (code >> 7) & 1;
+  int e = (code >> 3) & 0xF;
+  int m = code & 0x7;
+  double mag;
+  if (e == 0xF && m == 0x7) return NAN;
+  if (e == 0)
+    mag = ldexp((double)m / 8.0, -6);
+  else
+    mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sign ? -mag : mag;
+}
+
+/* BF16 is the upper half of an IEEE binary32: widening is exact. */
+double pa_oracle_bf16_to_double(uint16_t bits) {
+  uint32_t w = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &w, sizeof f);
+  return (double)f;
+}
+
+/* Round a double to BF16 (8 significant bits, exponent range of binary32),
+ * round-to-nearest, ties to even; returns the BF16 bit pattern. */
+uint16_t pa_oracle_round_bf16(double x) {
+  double r;
+  float f;
+  uint32_t w;
+  if (isnan(x)) return 0x7FC0;
+  if (x == 0.0) return signbit(x) ? 0x8000 : 0x0000;
+  if (isinf(x)) return x > 0 ? 0x7F80 : 0xFF80;
+  {
+    int e;
+    double a = fabs(x);
+    (void)frexp(a, &e); /* a = f * 2^e with f in [0.5, 1) */
+    /* quantum: 2^(e-8) for normals, 2^-133 below the binary32 normal range */
+    int qexp = e - 8;
+    if (qexp < -133) qexp = -133;
+    r = nearbyint(ldexp(a, -qexp)); /* default rounding mode: ties to even */
+    r = ldexp(r, qexp);
+    if (r > 3.3895313892515355e38) r = INFINITY; /* above the largest finite BF16 */
+    if (signbit(x)) r = -r;
+  }
+  f = (float)r; /* exact: r is representable in BF16, hence in binary32 */
+  memcpy(&w, &f, sizeof w);
+  return (uint16_t)(w >> 16);
+}
+
+static double kv_element(const pa_oracle_shape* sh, const void* cache, const float* scale,
+                         int page, int g, int slot, int d) {
+  size_t idx = (((size_t)page * sh->num_kv_heads + g) * sh->page_size + slot) * sh->head_dim + d;
+  if (sh->kv_dtype == ORACLE_KV_BF16) return pa_oracle_bf16_to_double(((const uint16_t*)cache)[idx]);
+  {
+    double v = pa_oracle_e4m3_to_double(((const uint8_t*)cache)[idx]);
+    if (sh->scale_mode == ORACLE_SCALE_PER_TENSOR)
+      v *= (double)scale[0];
+    else if (sh->scale_mode == ORACLE_SCALE_PER_TOKEN)
+      v *= (double)scale[((size_t)page * sh->num_kv_heads + g) * sh->page_size + slot];
+    return v;
+  }
+}
+
+/* Physical page holding logical token t of sequence b, or -1 if the table
+ * entry is out of the pool. */
+static int token_page(const pa_oracle_shape* sh, const int32_t* block_table, int b, int t) {
+  int page = block_table[(size_t)b * sh->max_pages_per_seq + t / sh->page_size];
+  if (page < 0 || page >= sh->num_pages) return -1;
+  return page;
+}
+
+/* Visible token list of query row (b, i): dense mask or sparse index list. */
+static int visible_tokens(const pa_oracle_shape* sh, const int32_t* ctx_lens, const int32_t* topk_idx,
+                          int b, int i, int32_t* tokens) {
+  int L = ctx_lens[b];
+  int n = 0;
+  if (sh->topk > 0) {
+    for (int j = 0; j < sh->topk; ++j) {
+      int t = topk_idx[(size_t)b * sh->topk + j];
+      if (t >= 0 && t < L) tokens[n++] = t;
+    }
+    return n;
+  }
+  {
+    int p = L - sh->query_len + i;
+    for (int t = 0; t < L; ++t) {
+      if (sh->causal && t > p) continue;
+      if (sh->window > 0 && t <= p - sh->window) continue;
+      tokens[n++] = t;
+    }
+  }
+  return n;
+}
+
+/* Partial (m, l, O[D]) of query row (b, i, h) over an explicit token list,
+ * natural-log units. Empty list: m = -inf, l = 0, O = 0. */
+int pa_oracle_row_partial(const pa_oracle_shape* sh, const uint16_t* q, const void* k_cache,
+                          const void* v_cache, const int32_t* block_table, const float* k_scale,
+                          const float* v_scale, int b, int i, int h, const int32_t* tokens,
+                          int ntok, double* m_out, double* l_out, double* o_out) {
+  int D = sh->head_dim;
+  int G = sh->num_q_heads / sh->num_kv_heads;
+  int g = h / G;
+  const uint16_t* qrow = q + (((size_t)b * sh->query_len + i) * sh->num_q_heads + h) * D;
+  double* x = (double*)malloc(sizeof(double) * (ntok > 0 ? ntok : 1));
+  double m = -INFINITY, l = 0.0;
+  if (!x) return PA_ORACLE_NO_MEM;
+  for (int d = 0; d < D; ++d) o_out[d] = 0.0;
+  for (int j = 0; j < ntok; ++j) {
+    int t = tokens[j];
+    int page = token_page(sh, block_table, b, t);
+    double s = 0.0;
+    if (page < 0) {
+      free(x);
+      return PA_ORACLE_BAD_PAGE;
+    }
+    for (int d = 0; d < D; ++d)
+      s += pa_oracle_bf16_to_double(qrow[d]) *
+           kv_element(sh, k_cache, k_scale, page, g, t % sh->page_size, d);
+    x[j] = sh->sm_scale * s;
+    if (x[j] > m) m = x[j];
+  }
+  for (int j = 0; j < ntok; ++j) {
+    int t = tokens[j];
+    int page = token_page(sh, block_table, b, t);
+    double w = exp(x[j] - m);
+    l += w;
+    for (int d = 0; d < D; ++d)
+      o_out[d] += w * kv_element(sh, v_cache, v_scale, page, g, t % sh->page_size, d);
+  }
+  free(x);
+  *m_out = m;
+  *l_out = l;
+  return PA_ORACLE_OK;
+}
+
+/* Merge partials j = 0..n-1 in order, with an optional sink logit. */
+void pa_oracle_merge(int n, int D, const double* m, const double* l, const double* o, int has_sink,
+                     double sink, double* out) {
+  double M = -INFINITY, L = 0.0;
+  for (int j = 0; j < n; ++j)
+    if (m[j] > M) M = m[j];
+  if (has_sink && sink > M) M = sink;
+  for (int d = 0; d < D; ++d) out[d] = 0.0;
+  if (M == -INFINITY) return; /* no token, no sink */
+  for (int j = 0; j < n; ++j) {
+    double a;
+    if (m[j] == -INFINITY) continue; /* empty partial contributes nothing */
+    a = exp(m[j] - M);
+    L += l[j] * a;
+    for (int d = 0; d < D; ++d) out[d] += o[(size_t)j * D + d] * a;
+  }
+  if (has_sink) L += exp(sink - M);
+  if (L == 0.0) {
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    return;
+  }
+  for (int d = 0; d < D; ++d) out[d] /= L;
+}
+
+static int check_shape(const pa_oracle_shape* sh) {
+  if (sh->batch < 0 || sh->num_q_heads <= 0 || sh->num_kv_heads <= 0 || sh->head_dim <= 0 ||
+      sh->query_len <= 0 || sh->page_size <= 0 || sh->max_pages_per_seq <= 0 || sh->num_pages <= 0)
+    return PA_ORACLE_BAD_ARG;
+  if (sh->num_q_heads % sh->num_kv_heads != 0) return PA_ORACLE_BAD_ARG;
+  if (sh->topk > 0 && sh->query_len != 1) return PA_ORACLE_BAD_ARG;
+  if (sh->window < 0) return PA_ORACLE_BAD_ARG;
+  return PA_ORACLE_OK;
+}
+
+/* Full decode. out: double [B*QL, Hq, D]. unit_mask (optional, [B*Hkv]):
+ * rows of units whose mask byte is 0 are skipped (left untouched). */
+int pa_oracle_decode(const pa_oracle_shape* sh, const uint16_t* q, const void* k_cache,
+                     const void* v_cache, const int32_t* block_table, const int32_t* ctx_lens,
+                     const float* k_scale, const float* v_scale, const float* sinks,
+                     const int32_t* topk_idx, const uint8_t* unit_mask, double* out) {
+  int rc = check_shape(sh);
+  int D, G, maxL = 0;
+  int32_t* tokens;
+  double* o;
+  if (rc) return rc;
+  D = sh->head_dim;
+  G = sh->num_q_heads / sh->num_kv_heads;
+  for (int b = 0; b < sh->batch; ++b)
+    if (ctx_lens[b] > maxL) maxL = ctx_lens[b];
+  if (sh->topk > maxL) maxL = sh->topk;
+  for (int b = 0; b < sh->batch; ++b)
+    if ((long long)ctx_lens[b] > (long long)sh->max_pages_per_seq * sh->page_size || ctx_lens[b] < 0)
+      return PA_ORACLE_BAD_ARG;
+  tokens = (int32_t*)malloc(sizeof(int32_t) * (maxL > 0 ? maxL : 1));
+  o = (double*)malloc(sizeof(double) * D);
+  if (!tokens || !o) {
+    free(tokens);
+    free(o);
+    return PA_ORACLE_NO_MEM;
+  }
+  for (int b = 0; b < sh->batch && rc == PA_ORACLE_OK; ++b) {
+    for (int i = 0; i < sh->query_len && rc == PA_ORACLE_OK; ++i) {
+      int ntok = visible_tokens(sh, ctx_lens, topk_idx, b, i, tokens);
+      for (int h = 0; h < sh->num_q_heads; ++h) {
+        double m, l;
+        double* dst = out + (((size_t)b * sh->query_len + i) * sh->num_q_heads + h) * D;
+        if (unit_mask && !unit_mask[(size_t)b * sh->num_kv_heads + h / G]) continue;
+        rc = pa_oracle_row_partial(sh, q, k_cache, v_cache, block_table, k_scale, v_scale, b, i, h,
+                                   tokens, ntok, &m, &l, o);
+        if (rc) break;
+        if (ntok == 0) {
+          for (int d = 0; d < D; ++d) dst[d] = 0.0;
+          continue;
+        }
+        {
+          double den = l;
+          double M = m;
+          double a = 1.0;
+          if (sh->has_sinks) {
+            double s = (double)sinks[h];
+            if (s > M) M = s;
+            a = exp(m - M);
+            den = l * a + exp(s - M);
+          }
+          for (int d = 0; d < D; ++d) dst[d] = o[d] * a / den;
+        }
+      }
+    }
+  }
+  free(tokens);
+  free(o);
+  return rc;
+}
+
+/* Round a double array to BF16 bit patterns. */
+void pa_oracle_round_bf16_array(const double* x, uint16_t* bits, size_t n) {
+  for (size_t k = 0; k < n; ++k) bits[k] = pa_oracle_round_bf16(x[k]);
+}

@@ -1,0 +1,63 @@
+"""Plant plausible mistakes in copies of the oracle and check that the pins
+catch every one of them (CPU only; the shipped oracle is untouched)."""
+
+import os
+import tempfile
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+# (what the mistake is, original text, broken text)
+MUTANTS = [
+    ("causal bound off by one", "if (sh->causal && t > p) continue;",
+     "if (sh->causal && t >= p) continue;"),
+    ("window bound off by one", "t <= p - sh->window) continue;", "t < p - sh->window) continue;"),
+    ("query position reversed", "int p = L - sh->query_len + i;", "int p = L - 1 - i;"),
+    ("GQA mapping modulo", "int g = h / G;", "int g = h % sh->num_kv_heads;"),
+    ("slot off by one", "kv_element(sh, k_cache, k_scale, page, g, t % sh->page_size, d)",
+     "kv_element(sh, k_cache, k_scale, page, g, (t + 1) % sh->page_size, d)"),
+    ("block-table row stride", "block_table[(size_t)b * sh->max_pages_per_seq + t / sh->page_size]",
+     "block_table[(size_t)b * (sh->max_pages_per_seq - 1) + t / sh->page_size]"),
+    ("sm_scale dropped", "x[j] = sh->sm_scale * s;", "x[j] = s;"),
+    ("sink dropped", "den = l * a + exp(s - M);", "den = l * a;"),
+    ("sink sign", "den = l * a + exp(s - M);", "den = l * a + exp(M - s);"),
+    ("e4m3 bias", "ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    ("e4m3 subnormal", "ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
+    ("per-token scale slot", "* sh->page_size + slot];", "* sh->page_size];"),
+    ("V uses K scale", "kv_element(sh, v_cache, v_scale,", "kv_element(sh, v_cache, k_scale,"),
+    ("q operand reversed", "pa_oracle_bf16_to_double(qrow[d]) *", "pa_oracle_bf16_to_double(qrow[D - 1 - d]) *"),
+    ("sparse context filter", "if (t >= 0 && t < L) tokens[n++] = t;", "if (t >= 0) tokens[n++] = t;"),
+    ("merge without rescale", "out[d] += o[(size_t)j * D + d] * a;", "out[d] += o[(size_t)j * D + d];"),
+    ("merge without sink", "if (has_sink) L += exp(sink - M);", "if (0) L += exp(sink - M);"),
+    ("round ties away", "r = nearbyint(ldexp(a, -qexp));", "r = round(ldexp(a, -qexp));"),
+    ("bf16 widen shift", "uint32_t w = (uint32_t)bits << 16;", "uint32_t w = (uint32_t)bits << 15;"),
+    ("no empty-row guard", "if (ntok == 0) {", "if (ntok < 0) {"),
+    ("exp sign", "double w = exp(x[j] - m);", "double w = exp(m - x[j]);"),
+    ("window ignored", "if (sh->window > 0 && t <= p - sh->window) continue;", ""),
+]
+
+
+def test_mutants_are_well_formed():
+    src = open(oracle.SOURCE).read()
+    for name, old, _ in MUTANTS:
+        assert src.count(old) == 1, f"mutation site for '{name}' must occur exactly once"
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(name, old, new):
+    src = open(oracle.SOURCE).read()
+    with tempfile.TemporaryDirectory() as tmp:
+        path = os.path.join(tmp, "mutant.c")
+        with open(path, "w") as f:
+            f.write(src.replace(old, new, 1))
+        lib = oracle.build(source=path, out=os.path.join(tmp, "libmutant.so"), force=True)
+        mutant = oracle.Oracle(lib)
+        caught = []
+        for pin in ALL_PINS:
+            try:
+                pin(mutant)
+            except Exception as e:  # AssertionError or an oracle error code
+                caught.append((pin.__name__, type(e).__name__))
+        assert caught, f"no pin catches the mutant '{name}'"
