@@ -1,0 +1,196 @@
+/*
+ * pa_decode.h — C ABI of the GB300 (sm_103a) paged-attention decode library.
+ *
+ * What the library computes
+ * -------------------------
+ * For every sequence b, query index i in [0, query_len), query head h and its
+ * KV head g = h / (num_q_heads / num_kv_heads), the BF16 output row
+ *
+ *     out[b*QL + i, h, :] = sum_t softmax_t(x) * v_t      (t in the visible set)
+ *     x_t = sm_scale * <q[b*QL + i, h, :], k_t>
+ *
+ * over a KV cache split into fixed-size pages that a per-sequence int32 block
+ * table addresses (PR "Add paged-attention Tile kernel": pa_decode(output,
+ * query, key_cache, value_cache, block_tables, context_lengths, key_scale,
+ * value_scale, ...) and its shape checks). The visible set of row (b, i) is
+ * t in [0, L_b) with, for causal multi-token (MTP) queries, t <= p and, for a
+ * sliding window W > 0, t > p - W, where p = L_b - QL + i (PR "Extend packed
+ * D256 PA decode pipe to page16, transposed V and sliding windows": windows
+ * 0/1/17/257/8193, QL 1-4). Optional per-query-head sink logits add e^(s - m)
+ * to the softmax denominator only (PR "Merge gfx1250 PA decode partitions in
+ * the tile kernel and speed up dense decode": sinks keep a merge path). An
+ * empty visible set gives a zero row.
+ *
+ * The KV range is split into partitions whose online-softmax partials
+ * (running max, running sum, unnormalised output) are merged in partition
+ * order, inside a thread-block cluster over distributed shared memory, by the
+ * last-arriving CTA through device-scope arrival counters, or by a standalone
+ * reducer kernel (same PR, "Partition merges"). All merge mechanisms use the
+ * same arithmetic in the same order, so for one plan schedule they give
+ * bit-identical outputs.
+ *
+ * Layouts (all tensors are caller-owned device memory, row-major, contiguous)
+ * --------------------------------------------------------------------------
+ *   q, out        [batch*query_len, num_q_heads, head_dim]     BF16
+ *   k_cache,
+ *   v_cache       [num_pages, num_kv_heads, page_size, head_dim]
+ *                 FP8 e4m3fn bytes (OCP) or BF16
+ *   block_table   [batch, max_pages_per_seq]  int32 physical page ids; only
+ *                 the entries covering [0, L_b) are ever read
+ *   ctx_lens      [batch]  int32, 0 <= L_b <= max_pages_per_seq * page_size
+ *   k_scale,
+ *   v_scale       float32 [1] (per tensor) or [num_pages, num_kv_heads,
+ *                 page_size] (per token); NULL when scale_mode is NONE
+ *   sinks         float32 [num_q_heads] (natural-log units, not multiplied
+ *                 by sm_scale) or NULL
+ *   topk_idx      int32 [batch, sparse_topk] logical token positions;
+ *                 entries outside [0, L_b) are ignored (sparse decode only)
+ * Every pointer must be 16-byte aligned.
+ *
+ * Errors and ownership
+ * --------------------
+ * Functions return a pa_status; on failure a thread-local message is
+ * available from pa_last_error(). Nothing aborts. pa_decode* allocates no
+ * memory, never synchronises the stream and launches only on the given
+ * stream, so calls can be captured in a CUDA graph. The plan owns host
+ * metadata only; its workspace (partials, arrival counters, a device status
+ * word) is caller-allocated device memory, bound once with
+ * pa_plan_set_workspace and zero-filled by the caller before first use.
+ * Arrival counters reset themselves, so the workspace needs no clearing
+ * between calls. A plan (its workspace) must not be used by two decodes that
+ * can run concurrently.
+ */
+#ifndef PA_DECODE_H
+#define PA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or shape */
+  PA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (head_dim, rows, ...) */
+  PA_ERR_WORKSPACE = 3,    /* workspace missing or too small */
+  PA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+  PA_ERR_DEVICE_STATUS = 5 /* a kernel reported a timeout in its status word */
+} pa_status;
+
+enum { PA_KV_FP8_E4M3 = 0, PA_KV_BF16 = 1 };
+enum { PA_SCALE_NONE = 0, PA_SCALE_PER_TENSOR = 1, PA_SCALE_PER_TOKEN = 2 };
+
+/* How partitions of one (sequence, KV head) are merged. */
+enum {
+  PA_MERGE_AUTO = 0,
+  PA_MERGE_DIRECT = 1,       /* one partition per unit: the tile writes output */
+  PA_MERGE_CLUSTER = 2,      /* P in [2, 16] CTAs of a cluster merge over DSMEM */
+  PA_MERGE_LAST_ARRIVER = 3, /* the last CTA to arrive on a unit merges it */
+  PA_MERGE_REDUCER = 4       /* a second kernel merges the partials */
+};
+
+/* How KV chunks are assigned to CTAs. */
+enum {
+  PA_SCHED_AUTO = 0,
+  PA_SCHED_BALANCED = 1, /* all units' chunks split evenly over a persistent grid */
+  PA_SCHED_PER_UNIT = 2  /* P CTAs per (sequence, KV head), P = partitions */
+};
+
+typedef struct pa_plan_desc {
+  int batch;
+  int num_q_heads;
+  int num_kv_heads;      /* num_q_heads % num_kv_heads == 0 */
+  int head_dim;          /* 128 or 256 */
+  int query_len;         /* 1..4 (MTP rows); rows = query_len * group <= 64 */
+  int page_size;         /* 16, 32, 64, 128 or 256 tokens */
+  int max_pages_per_seq; /* block-table row stride (int32 elements) */
+  int num_pages;         /* pages in the cache pool */
+  int max_context_len;   /* host bound used for automatic choices; 0 = unknown */
+  int kv_dtype;          /* PA_KV_* */
+  int scale_mode;        /* PA_SCALE_* (FP8 only; BF16 requires NONE) */
+  int causal;            /* causal mask among the query_len new tokens */
+  int has_sinks;
+  int sparse_topk;       /* 0 = dense decode; > 0 = index-list decode (query_len 1) */
+  float sm_scale;        /* 0 => 1/sqrt(head_dim); must be > 0 otherwise */
+  int max_partitions;    /* per-unit schedule partitions; 0 => automatic */
+  int merge_mode;        /* PA_MERGE_* */
+  int schedule;          /* PA_SCHED_* */
+  int sm_count_override; /* 0 => device attribute (tests: simulated SM counts) */
+  int ctas_per_sm_override; /* 0 => occupancy query */
+  int device;            /* CUDA device ordinal the plan is for */
+} pa_plan_desc;
+
+typedef struct pa_plan_info {
+  int merge_mode;      /* resolved PA_MERGE_* */
+  int schedule;        /* resolved PA_SCHED_* */
+  int num_partitions;  /* per-unit schedule: P; balanced: 0 */
+  int stage_tokens;    /* tokens per ring stage (= chunk granularity) */
+  int num_stages;      /* shared-memory ring depth */
+  int rows;            /* query rows per (sequence, KV head) = group * query_len */
+  int rows_per_warp;   /* 8 or 16 */
+  int row_warps;       /* consumer warps splitting the rows */
+  int token_warps;     /* consumer warps splitting each stage's tokens */
+  int block_threads;   /* consumer warps * 32 + one producer warp */
+  int grid;            /* CTAs of the tile kernel */
+  int cluster;         /* cluster size (1 = none) */
+  int ctas_per_sm;
+  int sm_count;
+  int launches_per_call;
+  int units;           /* batch * num_kv_heads */
+  size_t smem_bytes;   /* dynamic shared memory of the tile kernel */
+  size_t workspace_bytes;
+  size_t partial_slots;
+  size_t status_offset; /* byte offset of the int32 device status word */
+} pa_plan_info;
+
+typedef struct pa_plan pa_plan_t;
+
+/* Validate desc, size partitions from the SM count and occupancy, pick the
+ * merge mechanism. Host only: with both overrides set it touches no device. */
+PA_API pa_status pa_plan_create(const pa_plan_desc* desc, pa_plan_t** out);
+
+/* Bytes of caller-owned device workspace the plan needs (partials, arrival
+ * counters at one 128-byte line each, status word). */
+PA_API size_t pa_plan_workspace_bytes(const pa_plan_t* plan);
+
+/* Bind zero-filled device memory of at least pa_plan_workspace_bytes bytes
+ * (16-byte aligned). The plan does not take ownership. */
+PA_API pa_status pa_plan_set_workspace(pa_plan_t* plan, void* dev_ptr, size_t bytes);
+
+PA_API pa_status pa_plan_get_info(const pa_plan_t* plan, pa_plan_info* info);
+
+PA_API void pa_plan_destroy(pa_plan_t* plan);
+
+/* Dense paged decode of one batch on `stream` (a cudaStream_t; NULL = legacy
+ * default stream). window: 0 = off, else W >= 1 (requires causal or
+ * query_len 1). Returns after enqueueing; errors in the kernel's bounded
+ * waits show up in the status word (pa_plan_info.status_offset). */
+PA_API pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_table, const int32_t* ctx_lens, const float* k_scale,
+                    const float* v_scale, int window, const float* sinks, const pa_plan_t* plan,
+                    void* stream);
+
+/* Sparse (top-k index list) decode: query_len 1, no causal mask or window. */
+PA_API pa_status pa_decode_sparse(void* out, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_table, const int32_t* ctx_lens,
+                           const int32_t* topk_idx, const float* k_scale, const float* v_scale,
+                           const float* sinks, const pa_plan_t* plan, void* stream);
+
+PA_API const char* pa_strerror(pa_status status);
+
+/* Message of the last failure on this thread ("" if none). */
+PA_API const char* pa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_DECODE_H */

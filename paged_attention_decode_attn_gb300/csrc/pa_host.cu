@@ -1,0 +1,554 @@
+// Host side of the C ABI: plan sizing, argument validation, TMA descriptors
+// and kernel launches. No memory allocation, no stream synchronisation.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <new>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "pa_decode.h"
+#include "pa_internal.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+pa_status fail(pa_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+pa_status fail(pa_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+pa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+struct pa_plan {
+  pa_plan_desc desc;
+  pa_plan_info info;
+  pa::PaParams base;
+  const void* tile_fn = nullptr;
+  const void* reduce_fn = nullptr;
+  bool attrs_set = false;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  size_t off_part_o = 0, off_part_ml = 0, off_counters = 0, off_desc = 0, off_status = 0;
+  // TMA descriptor cache (re-encoded when the cache pointers change)
+  const void* tm_k = nullptr;
+  const void* tm_v = nullptr;
+  CUtensorMap tmK, tmV;
+  bool tm_valid = false;
+};
+
+namespace {
+
+// Largest dynamic shared memory a CTA may use while two CTAs share an SM.
+constexpr int kSmemTwoPerSm = 112 * 1024;
+constexpr int kSmemOnePerSm = 226 * 1024;
+
+struct KernelShape {
+  int nt, rw, wr, wt, ncw, rpad, elt, rb, nch, tt, bh;
+  bool vtok;
+};
+
+KernelShape kernel_shape(const pa_plan_desc& d) {
+  KernelShape k;
+  const int G = d.num_q_heads / d.num_kv_heads;
+  const int R = G * d.query_len;
+  k.nt = (d.head_dim == 128 && R > 8) ? 2 : 1;
+  k.rw = 8 * k.nt;
+  k.wr = (R + k.rw - 1) / k.rw;
+  k.wt = k.wr >= 4 ? 1 : 4 / k.wr;
+  k.ncw = k.wr * k.wt;
+  k.rpad = k.wr * k.rw;
+  k.elt = d.kv_dtype == PA_KV_FP8_E4M3 ? 1 : 2;
+  k.rb = d.head_dim * k.elt;
+  k.nch = k.rb / 128;
+  int tt = 16384 / (2 * k.rb);
+  k.tt = tt < 16 ? 16 : (tt > 64 ? 64 : tt);
+  k.bh = d.page_size < k.tt ? d.page_size : k.tt;
+  k.vtok = d.kv_dtype == PA_KV_FP8_E4M3 && d.scale_mode == PA_SCALE_PER_TOKEN;
+  return k;
+}
+
+// Shared-memory layout for `ns` ring stages.
+pa::SmemLayout smem_layout(const pa_plan_desc& d, const KernelShape& k, int ns, bool cluster) {
+  pa::SmemLayout L;
+  L.stage_bytes = 2 * k.tt * k.rb + (d.scale_mode == PA_SCALE_PER_TOKEN ? 1024 : 0);
+  L.off_scale = 2 * k.tt * k.rb;
+  L.off_stage = 0;
+  size_t off = (size_t)ns * L.stage_bytes;
+  L.off_merge = (int)off;
+  off += align_up((size_t)k.wt * k.rpad * d.head_dim * 4 + (size_t)k.wt * k.rpad * 8, 128);
+  L.off_cpart = (int)off;
+  if (cluster) off += align_up((size_t)k.rpad * d.head_dim * 4 + (size_t)k.rpad * 8, 128);
+  L.off_hdr = (int)off;
+  off += (size_t)ns * 64;
+  L.off_bar = (int)off;
+  off += (size_t)ns * 16;
+  L.off_misc = (int)off;
+  off += 64;
+  L.total = (int)(off + 1024);  // slack for aligning the base to 1024 bytes
+  return L;
+}
+
+const void* pick_tile_kernel(const pa_plan_desc& d, const KernelShape& k) {
+  if (d.kv_dtype == PA_KV_FP8_E4M3) {
+    if (d.head_dim == 128) return pa::tile_kernel_fp8_d128(k.nt, k.vtok);
+    return pa::tile_kernel_fp8_d256(k.nt, k.vtok);
+  }
+  return pa::tile_kernel_bf16(d.head_dim, k.nt);
+}
+
+pa_status validate_desc(const pa_plan_desc& d) {
+  if (d.batch < 0) return fail(PA_ERR_INVALID_ARG, "batch must be >= 0 (got %d)", d.batch);
+  if (d.num_q_heads <= 0 || d.num_kv_heads <= 0)
+    return fail(PA_ERR_INVALID_ARG, "head counts must be positive (%d, %d)", d.num_q_heads, d.num_kv_heads);
+  if (d.num_q_heads % d.num_kv_heads != 0)
+    return fail(PA_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", d.num_q_heads,
+                d.num_kv_heads);
+  if (d.head_dim != 128 && d.head_dim != 256)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim %d unsupported (128 or 256)", d.head_dim);
+  if (d.query_len < 1) return fail(PA_ERR_INVALID_ARG, "query_len must be >= 1 (got %d)", d.query_len);
+  const long long rows = (long long)(d.num_q_heads / d.num_kv_heads) * d.query_len;
+  if (rows > pa::kMaxRows)
+    return fail(PA_ERR_UNSUPPORTED, "group*query_len = %lld query rows per KV head exceeds %d", rows, pa::kMaxRows);
+  if (d.page_size != 16 && d.page_size != 32 && d.page_size != 64 && d.page_size != 128 && d.page_size != 256)
+    return fail(PA_ERR_UNSUPPORTED, "page_size %d unsupported (16, 32, 64, 128, 256)", d.page_size);
+  if (d.max_pages_per_seq < 1 || d.num_pages < 1)
+    return fail(PA_ERR_INVALID_ARG, "max_pages_per_seq and num_pages must be >= 1");
+  if ((long long)d.num_pages * d.num_kv_heads * d.page_size >= (1ll << 31))
+    return fail(PA_ERR_UNSUPPORTED, "cache has 2^31 or more token rows per tensor");
+  if ((long long)d.max_pages_per_seq * d.page_size >= (1ll << 30))
+    return fail(PA_ERR_UNSUPPORTED, "max_pages_per_seq * page_size too large");
+  if (d.kv_dtype != PA_KV_FP8_E4M3 && d.kv_dtype != PA_KV_BF16)
+    return fail(PA_ERR_INVALID_ARG, "unknown kv_dtype %d", d.kv_dtype);
+  if (d.scale_mode < PA_SCALE_NONE || d.scale_mode > PA_SCALE_PER_TOKEN)
+    return fail(PA_ERR_INVALID_ARG, "unknown scale_mode %d", d.scale_mode);
+  if (d.kv_dtype == PA_KV_BF16 && d.scale_mode != PA_SCALE_NONE)
+    return fail(PA_ERR_INVALID_ARG, "BF16 caches take no K/V scales");
+  if (d.sparse_topk < 0) return fail(PA_ERR_INVALID_ARG, "sparse_topk must be >= 0");
+  if (d.sparse_topk > 0 && d.query_len != 1)
+    return fail(PA_ERR_UNSUPPORTED, "sparse decode needs query_len 1 (got %d)", d.query_len);
+  if (!(d.sm_scale >= 0.f) || std::isinf(d.sm_scale))
+    return fail(PA_ERR_INVALID_ARG, "sm_scale must be finite and >= 0 (0 = 1/sqrt(head_dim))");
+  if (d.max_partitions < 0 || d.max_partitions > 256)
+    return fail(PA_ERR_INVALID_ARG, "max_partitions must be in [0, 256]");
+  if (d.merge_mode < PA_MERGE_AUTO || d.merge_mode > PA_MERGE_REDUCER)
+    return fail(PA_ERR_INVALID_ARG, "unknown merge_mode %d", d.merge_mode);
+  if (d.schedule < PA_SCHED_AUTO || d.schedule > PA_SCHED_PER_UNIT)
+    return fail(PA_ERR_INVALID_ARG, "unknown schedule %d", d.schedule);
+  if (d.sm_count_override < 0 || d.ctas_per_sm_override < 0)
+    return fail(PA_ERR_INVALID_ARG, "overrides must be >= 0");
+  return PA_OK;
+}
+
+// Resolve schedule, partitions and merge mechanism (pure host arithmetic).
+pa_status resolve_schedule(const pa_plan_desc& d, const KernelShape& k, int sm_count, int ctas_per_sm, int& sched,
+                           int& merge, int& P) {
+  const int units = d.batch * d.num_kv_heads;
+  sched = d.schedule;
+  merge = d.merge_mode;
+  P = d.max_partitions;
+  if (merge == PA_MERGE_DIRECT) {
+    if (sched == PA_SCHED_BALANCED) return fail(PA_ERR_INVALID_ARG, "direct output needs the per-unit schedule");
+    if (P > 1) return fail(PA_ERR_INVALID_ARG, "direct output needs one partition per unit");
+    sched = PA_SCHED_PER_UNIT;
+    P = 1;
+  }
+  if (merge == PA_MERGE_CLUSTER) {
+    if (sched == PA_SCHED_BALANCED) return fail(PA_ERR_INVALID_ARG, "cluster merge needs the per-unit schedule");
+    sched = PA_SCHED_PER_UNIT;
+  }
+  if (sched == PA_SCHED_AUTO) sched = d.sparse_topk > 0 ? PA_SCHED_PER_UNIT : PA_SCHED_BALANCED;
+  if (sched == PA_SCHED_PER_UNIT) {
+    if (P == 0) {
+      // Fill the resident CTA slots once: P = slots / units, in [1, 16], and
+      // no more partitions than the longest unit has chunks.
+      const long long slots = (long long)sm_count * ctas_per_sm;
+      long long p = units > 0 ? slots / units : 1;
+      if (p < 1) p = 1;
+      if (p > 16) p = 16;
+      long long max_tokens = d.sparse_topk > 0 ? d.sparse_topk : d.max_context_len;
+      if (max_tokens > 0) {
+        const long long chunks = (max_tokens + k.tt - 1) / k.tt;
+        if (p > chunks) p = chunks;
+      }
+      if (p < 1) p = 1;
+      P = (int)p;
+      if (merge == PA_MERGE_CLUSTER && P < 2) P = 2;
+    }
+  } else {
+    P = 0;
+  }
+  if (merge == PA_MERGE_AUTO) {
+    if (sched == PA_SCHED_BALANCED)
+      merge = PA_MERGE_LAST_ARRIVER;
+    else
+      merge = P == 1 ? PA_MERGE_DIRECT : (P <= 8 ? PA_MERGE_CLUSTER : PA_MERGE_LAST_ARRIVER);
+  }
+  if (merge == PA_MERGE_CLUSTER && (P < 2 || P > 16))
+    return fail(PA_ERR_UNSUPPORTED, "cluster merge needs 2..16 partitions (got %d)", P);
+  if (sched == PA_SCHED_PER_UNIT && P == 1) merge = PA_MERGE_DIRECT;
+  return PA_OK;
+}
+
+pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
+  const pa_plan_desc& d = pl->desc;
+  const KernelShape k = kernel_shape(d);
+  pa_plan_info& in = pl->info;
+  std::memset(&in, 0, sizeof in);
+  pl->tile_fn = pick_tile_kernel(d, k);
+  pl->reduce_fn = pa::reduce_kernel(d.head_dim);
+  if (!pl->tile_fn || !pl->reduce_fn) return fail(PA_ERR_UNSUPPORTED, "no kernel for this configuration");
+
+  // Ring depth: as many 16 KiB stages as fit two CTAs per SM (at least 3),
+  // else one CTA per SM.
+  int ns = 0;
+  int budget = kSmemTwoPerSm;
+  for (int attempt = 0; attempt < 2 && ns < 3; ++attempt) {
+    budget = attempt == 0 ? kSmemTwoPerSm : kSmemOnePerSm;
+    const pa::SmemLayout l0 = smem_layout(d, k, 0, true);
+    const int stage = l0.stage_bytes + 64 + 16;
+    ns = (budget - l0.total) / stage;
+    if (ns > 8) ns = 8;
+  }
+  if (ns < 2) return fail(PA_ERR_UNSUPPORTED, "shared memory too small for two ring stages");
+
+  int ctas_per_sm = ctas_override;
+  if (ctas_per_sm == 0) ctas_per_sm = budget == kSmemTwoPerSm ? 2 : 1;  // refined by the occupancy query
+
+  int sched, merge, P;
+  pa_status st = resolve_schedule(d, k, sm_count, ctas_per_sm, sched, merge, P);
+  if (st != PA_OK) return st;
+  const bool cluster = merge == PA_MERGE_CLUSTER;
+  const pa::SmemLayout L = smem_layout(d, k, ns, cluster);
+
+  const int units = d.batch * d.num_kv_heads;
+  const int G = d.num_q_heads / d.num_kv_heads;
+  const int R = G * d.query_len;
+  long long grid = sched == PA_SCHED_BALANCED ? (long long)sm_count * ctas_per_sm : (long long)units * P;
+  if (units == 0) grid = 0;
+  size_t slots = 0;
+  if (sched == PA_SCHED_BALANCED)
+    slots = 2 * (size_t)grid;
+  else if (P > 1 && !cluster)
+    slots = (size_t)units * P;
+
+  // workspace: partial O, partial (max, sum), arrival counters, reducer
+  // descriptors, status word
+  size_t off = 0;
+  pl->off_part_o = off;
+  off = align_up(off + slots * k.rpad * d.head_dim * 4, 256);
+  pl->off_part_ml = off;
+  off = align_up(off + slots * k.rpad * 8, 256);
+  pl->off_counters = off;
+  if (merge == PA_MERGE_LAST_ARRIVER) off = align_up(off + (size_t)units * pa::kCounterStride * 4, 256);
+  pl->off_desc = off;
+  if (merge == PA_MERGE_REDUCER) off = align_up(off + (size_t)units * 16, 256);
+  pl->off_status = off;
+  off += 256;
+
+  in.merge_mode = merge;
+  in.schedule = sched;
+  in.num_partitions = sched == PA_SCHED_PER_UNIT ? P : 0;
+  in.stage_tokens = k.tt;
+  in.num_stages = ns;
+  in.rows = R;
+  in.rows_per_warp = k.rw;
+  in.row_warps = k.wr;
+  in.token_warps = k.wt;
+  in.block_threads = (k.ncw + 1) * 32;
+  in.grid = (int)grid;
+  in.cluster = cluster ? P : 1;
+  in.ctas_per_sm = ctas_per_sm;
+  in.sm_count = sm_count;
+  in.launches_per_call = merge == PA_MERGE_REDUCER ? 2 : 1;
+  in.units = units;
+  in.smem_bytes = (size_t)L.total;
+  in.workspace_bytes = off;
+  in.partial_slots = slots;
+  in.status_offset = pl->off_status;
+
+  pa::PaParams& p = pl->base;
+  std::memset(&p, 0, sizeof p);
+  p.B = d.batch;
+  p.Hq = d.num_q_heads;
+  p.Hkv = d.num_kv_heads;
+  p.G = G;
+  p.QL = d.query_len;
+  p.D = d.head_dim;
+  p.S = d.page_size;
+  p.maxp = d.max_pages_per_seq;
+  p.num_pages = d.num_pages;
+  p.R = R;
+  p.Rpad = k.rpad;
+  p.causal = d.causal ? 1 : 0;
+  p.topk = d.sparse_topk;
+  p.has_sinks = d.has_sinks ? 1 : 0;
+  p.scale_mode = d.kv_dtype == PA_KV_FP8_E4M3 ? d.scale_mode : pa::kScaleNone;
+  const float sm_scale = d.sm_scale > 0.f ? d.sm_scale : 1.0f / std::sqrt((float)d.head_dim);
+  p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  p.sched = sched;
+  p.merge = merge;
+  p.C = sched == PA_SCHED_BALANCED ? (int)grid : 0;
+  p.P = sched == PA_SCHED_PER_UNIT ? P : 0;
+  p.TT = k.tt;
+  p.NS = ns;
+  p.Wr = k.wr;
+  p.Wt = k.wt;
+  p.NCW = k.ncw;
+  p.BH = k.bh;
+  p.swz = d.sparse_topk > 0 ? 0 : 7;
+  p.off_stage = L.off_stage;
+  p.stage_bytes = L.stage_bytes;
+  p.off_scale = L.off_scale;
+  p.off_hdr = L.off_hdr;
+  p.off_bar = L.off_bar;
+  p.off_merge = L.off_merge;
+  p.off_cpart = L.off_cpart;
+  p.off_misc = L.off_misc;
+  return PA_OK;
+}
+
+pa_status set_kernel_attrs(pa_plan* pl) {
+  if (pl->attrs_set) return PA_OK;
+  cudaError_t e = cudaSetDevice(pl->desc.device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+  e = cudaFuncSetAttribute(pl->tile_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl->info.smem_bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
+  if (pl->info.cluster > 8) {
+    e = cudaFuncSetAttribute(pl->tile_fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(non-portable cluster)");
+  }
+  pl->attrs_set = true;
+  return PA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2-D view of a paged cache: rows = (page, kv head, slot), columns = head dims.
+pa_status encode_cache_map(const pa_plan* pl, const void* base, CUtensorMap* tm) {
+  const pa_plan_desc& d = pl->desc;
+  auto fn = encode_fn();
+  if (!fn) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const int elt = d.kv_dtype == PA_KV_FP8_E4M3 ? 1 : 2;
+  const bool sparse = d.sparse_topk > 0;
+  cuuint64_t dims[2] = {(cuuint64_t)d.head_dim, (cuuint64_t)d.num_pages * d.num_kv_heads * d.page_size};
+  cuuint64_t strides[1] = {(cuuint64_t)d.head_dim * elt};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / elt), sparse ? 1u : (cuuint32_t)pl->base.BH};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(tm, elt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  sparse ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return PA_OK;
+}
+
+pa_status launch(const pa_plan* cpl, void* out, const void* q, const void* k_cache, const void* v_cache,
+                 const int32_t* block_table, const int32_t* ctx_lens, const int32_t* topk_idx, const float* k_scale,
+                 const float* v_scale, int window, const float* sinks, void* stream) {
+  pa_plan* pl = const_cast<pa_plan*>(cpl);
+  const pa_plan_desc& d = pl->desc;
+  if (d.batch == 0) return PA_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_table || !ctx_lens)
+    return fail(PA_ERR_INVALID_ARG, "null tensor pointer");
+  const void* ptrs[] = {out, q, k_cache, v_cache, block_table, ctx_lens, topk_idx, k_scale, v_scale, sinks};
+  for (const void* ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return fail(PA_ERR_INVALID_ARG, "tensor pointer %p is not 16-byte aligned", ptr);
+  if (d.kv_dtype == PA_KV_FP8_E4M3 && d.scale_mode != PA_SCALE_NONE && (!k_scale || !v_scale))
+    return fail(PA_ERR_INVALID_ARG, "FP8 scales are required by the plan's scale_mode");
+  if (d.has_sinks && !sinks) return fail(PA_ERR_INVALID_ARG, "the plan has sinks but sinks is null");
+  if (window < 0) return fail(PA_ERR_INVALID_ARG, "window must be >= 0");
+  if (window > 0 && !d.causal && d.query_len > 1)
+    return fail(PA_ERR_UNSUPPORTED, "a window with non-causal multi-token queries is not defined");
+  if (!pl->ws) return fail(PA_ERR_WORKSPACE, "no workspace bound to the plan");
+  pa_status st = set_kernel_attrs(pl);
+  if (st != PA_OK) return st;
+  if (!pl->tm_valid || pl->tm_k != k_cache || pl->tm_v != v_cache) {
+    st = encode_cache_map(pl, k_cache, &pl->tmK);
+    if (st != PA_OK) return st;
+    st = encode_cache_map(pl, v_cache, &pl->tmV);
+    if (st != PA_OK) return st;
+    pl->tm_k = k_cache;
+    pl->tm_v = v_cache;
+    pl->tm_valid = true;
+  }
+  pa::PaParams p = pl->base;
+  uint8_t* ws = static_cast<uint8_t*>(pl->ws);
+  p.out = static_cast<uint16_t*>(out);
+  p.q = static_cast<const uint16_t*>(q);
+  p.block_table = block_table;
+  p.ctx_lens = ctx_lens;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.sinks = d.has_sinks ? sinks : nullptr;
+  p.topk_idx = topk_idx;
+  p.window = d.sparse_topk > 0 ? 0 : window;
+  p.part_o = reinterpret_cast<float*>(ws + pl->off_part_o);
+  p.part_ml = reinterpret_cast<float*>(ws + pl->off_part_ml);
+  p.counters = reinterpret_cast<int*>(ws + pl->off_counters);
+  p.unit_desc = reinterpret_cast<int4*>(ws + pl->off_desc);
+  p.status = reinterpret_cast<int*>(ws + pl->off_status);
+
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3((unsigned)pl->info.grid, 1, 1);
+  cfg.blockDim = dim3((unsigned)pl->info.block_threads, 1, 1);
+  cfg.dynamicSmemBytes = pl->info.smem_bytes;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  if (pl->info.cluster > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)pl->info.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  void* args[] = {&p, &pl->tmK, &pl->tmV};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, pl->tile_fn, args);
+  if (e != cudaSuccess) return cuda_fail(e, "tile kernel launch");
+  if (pl->info.merge_mode == PA_MERGE_REDUCER) {
+    cudaLaunchConfig_t rc;
+    std::memset(&rc, 0, sizeof rc);
+    rc.gridDim = dim3((unsigned)pl->info.units, 1, 1);
+    rc.blockDim = dim3(128, 1, 1);
+    rc.stream = static_cast<cudaStream_t>(stream);
+    void* rargs[] = {&p};
+    e = cudaLaunchKernelExC(&rc, pl->reduce_fn, rargs);
+    if (e != cudaSuccess) return cuda_fail(e, "reducer launch");
+  }
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_plan_create(const pa_plan_desc* desc, pa_plan_t** out) {
+  if (!desc || !out) return fail(PA_ERR_INVALID_ARG, "null argument");
+  *out = nullptr;
+  pa_status st = validate_desc(*desc);
+  if (st != PA_OK) return st;
+  pa_plan* pl = new (std::nothrow) pa_plan();
+  if (!pl) return fail(PA_ERR_INVALID_ARG, "out of host memory");
+  pl->desc = *desc;
+  int sm_count = desc->sm_count_override;
+  const bool host_only = desc->sm_count_override > 0 && desc->ctas_per_sm_override > 0;
+  if (sm_count == 0) {
+    cudaError_t e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, desc->device);
+    if (e != cudaSuccess) {
+      delete pl;
+      return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    }
+  }
+  st = compute_plan(pl, sm_count, desc->ctas_per_sm_override);
+  if (st == PA_OK && !host_only && desc->ctas_per_sm_override == 0 && pl->info.schedule == PA_SCHED_BALANCED) {
+    // Size the persistent grid by the measured occupancy of the chosen kernel.
+    st = set_kernel_attrs(pl);
+    int n = 0;
+    if (st == PA_OK) {
+      cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pl->tile_fn, pl->info.block_threads,
+                                                                    pl->info.smem_bytes);
+      if (e != cudaSuccess) st = cuda_fail(e, "occupancy query");
+    }
+    if (st == PA_OK) {
+      if (n < 1) n = 1;
+      if (n != pl->info.ctas_per_sm) {
+        const bool attrs = pl->attrs_set;
+        st = compute_plan(pl, sm_count, n);
+        pl->attrs_set = attrs;
+      }
+    }
+  }
+  if (st != PA_OK) {
+    delete pl;
+    return st;
+  }
+  *out = pl;
+  return PA_OK;
+}
+
+size_t pa_plan_workspace_bytes(const pa_plan_t* plan) { return plan ? plan->info.workspace_bytes : 0; }
+
+pa_status pa_plan_set_workspace(pa_plan_t* plan, void* dev_ptr, size_t bytes) {
+  if (!plan) return fail(PA_ERR_INVALID_ARG, "null plan");
+  if (!dev_ptr) return fail(PA_ERR_WORKSPACE, "null workspace");
+  if ((reinterpret_cast<uintptr_t>(dev_ptr) & 255u) != 0)
+    return fail(PA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (bytes < plan->info.workspace_bytes)
+    return fail(PA_ERR_WORKSPACE, "workspace has %zu bytes, the plan needs %zu", bytes, plan->info.workspace_bytes);
+  plan->ws = dev_ptr;
+  plan->ws_bytes = bytes;
+  return PA_OK;
+}
+
+pa_status pa_plan_get_info(const pa_plan_t* plan, pa_plan_info* info) {
+  if (!plan || !info) return fail(PA_ERR_INVALID_ARG, "null argument");
+  *info = plan->info;
+  return PA_OK;
+}
+
+void pa_plan_destroy(pa_plan_t* plan) { delete plan; }
+
+pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                    const int32_t* ctx_lens, const float* k_scale, const float* v_scale, int window,
+                    const float* sinks, const pa_plan_t* plan, void* stream) {
+  if (!plan) return fail(PA_ERR_INVALID_ARG, "null plan");
+  if (plan->desc.sparse_topk > 0) return fail(PA_ERR_INVALID_ARG, "the plan is for sparse decode");
+  return launch(plan, out, q, k_cache, v_cache, block_table, ctx_lens, nullptr, k_scale, v_scale, window, sinks,
+                stream);
+}
+
+pa_status pa_decode_sparse(void* out, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_table, const int32_t* ctx_lens, const int32_t* topk_idx,
+                           const float* k_scale, const float* v_scale, const float* sinks, const pa_plan_t* plan,
+                           void* stream) {
+  if (!plan) return fail(PA_ERR_INVALID_ARG, "null plan");
+  if (plan->desc.sparse_topk == 0) return fail(PA_ERR_INVALID_ARG, "the plan is for dense decode");
+  if (!topk_idx) return fail(PA_ERR_INVALID_ARG, "null topk_idx");
+  return launch(plan, out, q, k_cache, v_cache, block_table, ctx_lens, topk_idx, k_scale, v_scale, 0, sinks, stream);
+}
+
+const char* pa_strerror(pa_status s) {
+  switch (s) {
+    case PA_OK: return "success";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PA_ERR_WORKSPACE: return "workspace missing or too small";
+    case PA_ERR_CUDA: return "CUDA error";
+    case PA_ERR_DEVICE_STATUS: return "kernel reported an error in its status word";
+  }
+  return "unknown status";
+}
+
+const char* pa_last_error(void) { return g_err.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,71 @@
+// Internal definitions shared by the host side (plan, launch) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+enum : int { kSchedBalanced = 1, kSchedPerUnit = 2 };
+enum : int { kMergeDirect = 1, kMergeCluster = 2, kMergeLastArriver = 3, kMergeReducer = 4 };
+enum : int { kScaleNone = 0, kScalePerTensor = 1, kScalePerToken = 2 };
+
+// Device status bits (int32 in the workspace).
+enum : int { kStatusTimeout = 1, kStatusBadPage = 2 };
+
+// Stage header flags.
+enum : int { kSegFirst = 1, kSegLast = 2, kSegWhole = 4 };
+
+constexpr int kMaxRows = 64;
+constexpr int kCounterStride = 32;  // int32 per arrival counter: one 128-byte line
+
+// Everything a tile/reducer launch needs, passed by value (__grid_constant__).
+struct PaParams {
+  // tensors
+  uint16_t* out;              // BF16 [B*QL, Hq, D]
+  const uint16_t* q;          // BF16 [B*QL, Hq, D]
+  const int32_t* block_table; // [B, maxp]
+  const int32_t* ctx_lens;    // [B]
+  const float* k_scale;       // [1] or [num_pages, Hkv, S]
+  const float* v_scale;
+  const float* sinks;         // [Hq] or null
+  const int32_t* topk_idx;    // [B, topk] or null
+  float* part_o;              // [slots, Rpad, D]
+  float* part_ml;             // [slots, Rpad, 2]  (max, sum) in log2 units
+  int* counters;              // [U, kCounterStride]
+  int4* unit_desc;            // [U] (nseg, s0, sbase, sstride) for the reducer
+  int* status;                // device status word
+  // shape
+  int B, Hq, Hkv, G, QL, D, S, maxp, num_pages, R, Rpad;
+  int window, causal, topk, has_sinks, scale_mode;
+  float sm_scale_log2;  // sm_scale * log2(e)
+  // schedule
+  int sched, merge;
+  int C;   // balanced: CTAs in the grid
+  int P;   // per-unit: partitions per unit
+  int TT;  // tokens per stage (= chunk)
+  int NS;  // ring stages
+  int Wr, Wt, NCW;  // row warps, token warps, consumer warps
+  int BH;           // rows per dense TMA box = min(S, TT)
+  int swz;          // XOR mask of the 128-byte swizzle (7) or 0 (linear rows)
+  // dynamic shared memory layout (byte offsets from a 1024-aligned base)
+  int off_stage, stage_bytes, off_scale;  // off_scale: within a stage
+  int off_hdr, off_bar, off_merge, off_cpart, off_misc;
+};
+
+// Host-visible shared-memory sizing for a kernel configuration.
+struct SmemLayout {
+  int stage_bytes, off_stage, off_scale, off_hdr, off_bar, off_merge, off_cpart, off_misc, total;
+};
+
+using KernelFn = void (*)(PaParams, CUtensorMap, CUtensorMap);
+
+// Tile-kernel instantiations (defined in the pa_tile_*.cu files).
+// Returns null when the combination is not instantiated.
+const void* tile_kernel_fp8_d128(int nt, int vtok);
+const void* tile_kernel_fp8_d256(int nt, int vtok);
+const void* tile_kernel_bf16(int d, int nt);
+const void* reduce_kernel(int d);
+
+}  // namespace pa

@@ -1,0 +1,1185 @@
+// Split-KV paged-attention decode tile kernel for sm_103a.
+//
+// Roles inside one CTA:
+//  * one producer warp walks the CTA's share of (sequence, KV head) token
+//    chunks, stages block-table page ids in its registers (32 per coalesced
+//    load, the next batch prefetched), and fills a ring of shared-memory
+//    stages with TMA copies (cp.async.bulk.tensor, 128-byte swizzle; sparse
+//    rows with tile::gather4), completing on mbarriers;
+//  * NCW consumer warps read each stage, compute S^T = K Q^T and O^T += V^T P^T
+//    with mma.sync m16n8k16 (tokens or head dims on the M side, query rows on
+//    the N side, so a GQA8 group fills the 8-wide N tile exactly), scale and
+//    mask the scores, keep the online softmax in registers (warp shuffles), and
+//    at each segment end merge their token groups and either write the BF16
+//    output or a partial (max, sum, unnormalised O) that the last-arriver,
+//    cluster or reducer merge combines in partition order.
+//
+// Sources of the method: PR "Add paged-attention Tile kernel" (API, layouts,
+// per-tensor/per-token scales, split partitions and their reduction), PR
+// "Extend packed D256 PA decode pipe to page16, transposed V and sliding
+// windows" (page-id staging, window-bounded page ranges, scale before mask,
+// per-token scales, MTP rows), PR "Merge gfx1250 PA decode partitions in the
+// tile kernel and speed up dense decode" (cluster merge, last-arriver merge
+// with self-resetting arrival counters, row scale folded into the exponent,
+// interior tiles without masks, double-buffered pages with asynchronous scale
+// copies).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "pa_internal.h"
+
+namespace pa {
+namespace dev {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
+
+struct alignas(16) StageHdr {
+  int kind;  // 0 = data, 1 = end of work
+  int flags; // kSeg*
+  int unit, b;
+  int g, tbase, t0, t1;  // tbase: token (index position) of stage row 0; [t0, t1): rows to use
+  int L;
+  unsigned mask_lo, mask_hi;  // sparse: validity of stage rows 0..31, 32..63
+  int slot;                   // partial slot of this segment
+  int nseg, s0, sbase, sstride;
+};
+static_assert(sizeof(StageHdr) == 64, "header size");
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, int count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t tx) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_timer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait on a phase; false after ~2 s (the caller records a timeout).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer() - t0 > kWaitLimitNs) return false;
+  }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int x, int y0, int y1, int y2, int y3,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void named_bar(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+  uint32_t r;
+  uint16_t v = static_cast<uint16_t>(two_bytes & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+// f16x2 -> bf16x2; exact for values that came from e4m3.
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
+  __half2 hv = *reinterpret_cast<__half2*>(&h);
+  float2 f = __half22float2(hv);
+  __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t movm_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  if constexpr (F16) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+// ------------------------------------------------------- schedule arithmetic
+// Visible token range of sequence b as a chunk range (union over the QL rows).
+struct UnitRange {
+  int L, lo, hi, c_lo, n;  // n = chunks touching [lo, hi) (0 if empty)
+};
+__device__ __forceinline__ UnitRange unit_range(const PaParams& p, int b) {
+  UnitRange r;
+  int L = __ldg(p.ctx_lens + b);
+  L = max(0, min(L, p.maxp * p.S));
+  r.L = L;
+  if (p.topk > 0) {
+    r.lo = 0;
+    r.hi = p.topk;
+    r.c_lo = 0;
+    r.n = (p.topk + p.TT - 1) / p.TT;
+    return r;
+  }
+  int lo = 0;
+  if (p.window > 0) lo = max(0, L - p.QL + 1 - p.window);
+  r.lo = lo;
+  r.hi = L;
+  if (L > lo) {
+    r.c_lo = lo / p.TT;
+    r.n = (L + p.TT - 1) / p.TT - r.c_lo;
+  } else {
+    r.c_lo = 0;
+    r.n = 0;
+  }
+  return r;
+}
+// Balanced schedule: chunk x of the global list belongs to CTA owner(x);
+// CTA c starts at start(c) = floor(c * N / C).
+__device__ __forceinline__ long long sched_start(long long c, long long N, long long C) { return c * N / C; }
+__device__ __forceinline__ long long sched_owner(long long x, long long N, long long C) {
+  return ((x + 1) * C - 1) / N;
+}
+// Total chunk count of the balanced schedule (warp-collective).
+__device__ __forceinline__ long long balanced_total(const PaParams& p, int lane) {
+  long long tot = 0;
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    int b = b0 + lane;
+    long long cnt = 0;
+    if (b < p.B) cnt = (long long)p.Hkv * max(1, unit_range(p, b).n);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+    tot += cnt;
+  }
+  return tot;
+}
+// Sequence containing global chunk x and the chunk count before it (warp-collective).
+__device__ __forceinline__ void balanced_find(const PaParams& p, int lane, long long x, int& b_out, long long& excl_out) {
+  long long base = 0;
+  b_out = p.B;
+  excl_out = base;
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    int b = b0 + lane;
+    long long cnt = 0;
+    if (b < p.B) cnt = (long long)p.Hkv * max(1, unit_range(p, b).n);
+    long long incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      long long v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    long long total = __shfl_sync(0xffffffffu, incl, 31);
+    unsigned hit = __ballot_sync(0xffffffffu, b < p.B && base + incl > x);
+    if (hit) {
+      int first = __ffs(hit) - 1;
+      long long ex = __shfl_sync(0xffffffffu, incl - cnt, first);
+      b_out = b0 + first;
+      excl_out = base + ex;
+      return;
+    }
+    base += total;
+  }
+}
+// Merge descriptor of a unit in the balanced schedule.
+struct MergeDesc {
+  int nseg, s0, sbase, sstride;
+};
+__device__ __forceinline__ MergeDesc balanced_desc(long long Pu, long long nu, long long N, long long C) {
+  MergeDesc d;
+  long long c1 = sched_owner(Pu, N, C), c2 = sched_owner(Pu + nu - 1, N, C);
+  d.nseg = (int)(c2 - c1 + 1);
+  d.s0 = (int)(2 * c1 + (sched_start(c1, N, C) < Pu ? 1 : 0));
+  d.sbase = (int)(2 * c1);
+  d.sstride = 2;
+  return d;
+}
+__device__ __forceinline__ int merge_slot(const MergeDesc& d, int k) { return k == 0 ? d.s0 : d.sbase + k * d.sstride; }
+
+// ------------------------------------------------------------ shared layout
+struct Smem {
+  uint8_t* base;
+  uint32_t base_u32;
+  __device__ __forceinline__ uint32_t stage(int s, const PaParams& p) const {
+    return base_u32 + p.off_stage + s * p.stage_bytes;
+  }
+  __device__ __forceinline__ StageHdr* hdr(int s, const PaParams& p) const {
+    return reinterpret_cast<StageHdr*>(base + p.off_hdr) + s;
+  }
+  __device__ __forceinline__ uint32_t full(int s, const PaParams& p) const { return base_u32 + p.off_bar + 8 * s; }
+  __device__ __forceinline__ uint32_t empty(int s, const PaParams& p) const {
+    return base_u32 + p.off_bar + 8 * (p.NS + s);
+  }
+  __device__ __forceinline__ volatile int* misc(const PaParams& p) const {
+    return reinterpret_cast<volatile int*>(base + p.off_misc);
+  }
+};
+
+__device__ __forceinline__ void flag_status(const PaParams& p, int bits) {
+  if (p.status) atomicOr(p.status, bits);
+}
+
+// ------------------------------------------------------------ merge math
+// out = O * (1/L) (* per-tensor V scale), with an optional sink logit added to
+// the denominator (natural-log units, converted to log2 here).
+template <int D>
+__device__ __forceinline__ void finalize_store(const PaParams& p, float vscale, float4 O, float M, float L, int b,
+                                               int g, int r, int d) {
+  const int i = r / p.G;
+  const int head = g * p.G + r % p.G;
+  if (p.has_sinks) {
+    const float s2 = __ldg(p.sinks + head) * kLog2e;
+    const float M2 = fmaxf(M, s2);
+    const float a = (M == -INFINITY) ? 0.f : ex2(M - M2);
+    L = fmaf(L, a, ex2(s2 - M2));
+    O.x *= a;
+    O.y *= a;
+    O.z *= a;
+    O.w *= a;
+  }
+  const float inv = (L > 0.f) ? (1.f / L) * vscale : 0.f;
+  uint2 st;
+  st.x = pack_bf16(O.x * inv, O.y * inv);
+  st.y = pack_bf16(O.z * inv, O.w * inv);
+  *reinterpret_cast<uint2*>(p.out + ((size_t)(b * p.QL + i) * p.Hq + head) * D + d) = st;
+}
+
+// Merge n partials (max, sum, O) in order k = 0..n-1 for output elements
+// [e0, e1) (groups of 4 head dims) and store the BF16 rows. Every merge path
+// (last arriver, cluster, reducer) goes through this function.
+template <int D, class LoadML, class LoadO>
+__device__ __forceinline__ void merge_elems(const PaParams& p, float vscale, int n, int b, int g, int tid, int nthr,
+                                            int e0, int e1, LoadML load_ml, LoadO load_o) {
+  for (int e = e0 + tid; e < e1; e += nthr) {
+    const int r = e / (D / 4);
+    const int d = (e % (D / 4)) * 4;
+    float M = -INFINITY;
+    for (int k = 0; k < n; ++k) M = fmaxf(M, load_ml(k, r).x);
+    float L = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < n; ++k) {
+      const float2 ml = load_ml(k, r);
+      if (ml.x == -INFINITY) continue;
+      const float a = ex2(ml.x - M);
+      const float4 ok = load_o(k, r, d);
+      L = fmaf(ml.y, a, L);
+      O.x = fmaf(ok.x, a, O.x);
+      O.y = fmaf(ok.y, a, O.y);
+      O.z = fmaf(ok.z, a, O.z);
+      O.w = fmaf(ok.w, a, O.w);
+    }
+    finalize_store<D>(p, vscale, O, M, L, b, g, r, d);
+  }
+}
+
+__device__ __forceinline__ float per_tensor_vscale(const PaParams& p) {
+  return p.scale_mode == kScalePerTensor ? __ldg(p.v_scale) : 1.f;
+}
+
+// ================================================================ producer
+template <int ELT, int NCH>
+struct Producer {
+  const PaParams& p;
+  const CUtensorMap* tmK;
+  const CUtensorMap* tmV;
+  Smem sm;
+  int lane;
+  int n = 0;  // stages filled so far
+  bool ok = true;
+  // page-id staging: lane l holds the physical page of logical page pbase + l
+  int pid_b = -1, pbase = 0, pid_cur = -1, pid_next = -1, npages_b = 0;
+
+  __device__ Producer(const PaParams& p_, const CUtensorMap* k, const CUtensorMap* v, Smem s)
+      : p(p_), tmK(k), tmV(v), sm(s), lane(threadIdx.x & 31) {}
+
+  __device__ __forceinline__ int load_pid(int b, int lp) const {
+    if (lp < 0 || lp >= npages_b) return -1;
+    return __ldg(p.block_table + (size_t)b * p.maxp + lp);
+  }
+  // Physical page of logical page lp0 + lane for lanes < cnt (cnt <= 4, inside one aligned batch).
+  __device__ __forceinline__ int staged_pages(int b, int L, int lp0, int align) {
+    if (b != pid_b) {
+      pid_b = b;
+      npages_b = (L + p.S - 1) / p.S;
+      pbase = -(1 << 30);
+    }
+    if (lp0 < pbase || lp0 >= pbase + 32) {
+      if (lp0 >= pbase + 32 && lp0 < pbase + 64) {
+        pid_cur = pid_next;
+        pbase += 32;
+      } else {
+        pbase = lp0 - lp0 % align;
+        pid_cur = load_pid(b, pbase + lane);
+      }
+      pid_next = load_pid(b, pbase + 32 + lane);
+    }
+    return __shfl_sync(0xffffffffu, pid_cur, (lp0 - pbase + lane) & 31);
+  }
+
+  __device__ __forceinline__ bool acquire_stage(int& s) {
+    s = n % p.NS;
+    const uint32_t par = ((n / p.NS) & 1) ^ 1;
+    bool got = mbar_wait(sm.empty(s, p), par);
+    got = __all_sync(0xffffffffu, got);
+    if (!got) {
+      ok = false;
+      if (lane == 0) {
+        flag_status(p, kStatusTimeout);
+        sm.misc(p)[0] = 1;
+      }
+    }
+    return got;
+  }
+
+  __device__ void emit_dense(const StageHdr& h) {
+    int s;
+    if (!acquire_stage(s)) return;
+    const int S = p.S, TT = p.TT, BH = p.BH;
+    int nbox = 0, lp0 = 0, row0 = 0, yoff = 0;
+    if (h.t1 > h.t0) {
+      if (S >= TT) {
+        nbox = 1;
+        lp0 = h.tbase / S;
+        yoff = h.tbase % S;
+        row0 = 0;
+      } else {
+        lp0 = h.t0 / S;
+        nbox = (h.t1 - 1) / S - lp0 + 1;
+        row0 = lp0 * S - h.tbase;
+      }
+    }
+    int phys = 0;
+    if (nbox > 0) phys = staged_pages(h.b, h.L, lp0, S < TT ? TT / S : 1);
+    const bool ktok = p.scale_mode == kScalePerToken;
+    const uint32_t bytes = (uint32_t)nbox * BH * 128u * NCH * 2u + (ktok ? (uint32_t)nbox * BH * 8u : 0u);
+    if (lane == 0) {
+      *sm.hdr(s, p) = h;
+      if (bytes)
+        mbar_arrive_tx(sm.full(s, p), bytes);
+      else
+        mbar_arrive(sm.full(s, p));
+    }
+    __syncwarp();
+    if (lane < nbox) {
+      if (phys < 0 || phys >= p.num_pages) {
+        flag_status(p, kStatusBadPage);
+        phys = 0;
+      }
+      const int y = (phys * p.Hkv + h.g) * S + yoff;
+      const int row = row0 + lane * BH;
+      const uint32_t kst = sm.stage(s, p);
+      const uint32_t vst = kst + (uint32_t)TT * 128u * NCH;
+      const uint32_t bar = sm.full(s, p);
+#pragma unroll
+      for (int cb = 0; cb < NCH; ++cb) {
+        tma_load_2d(kst + (uint32_t)(cb * TT + row) * 128u, tmK, cb * (128 / ELT), y, bar);
+        tma_load_2d(vst + (uint32_t)(cb * TT + row) * 128u, tmV, cb * (128 / ELT), y, bar);
+      }
+      if (ktok) {
+        const uint32_t sc = kst + p.off_scale;
+        bulk_load(sc + row * 4, p.k_scale + y, BH * 4, bar);
+        bulk_load(sc + TT * 4 + row * 4, p.v_scale + y, BH * 4, bar);
+      }
+    }
+  }
+
+  __device__ void emit_sparse(StageHdr h) {
+    int s;
+    if (!acquire_stage(s)) return;
+    const int TT = p.TT;
+    const uint32_t kst = sm.stage(s, p);
+    const uint32_t vst = kst + (uint32_t)TT * 128u * NCH;
+    const bool ktok = p.scale_mode == kScalePerToken;
+    int yv[2] = {0, 0};
+    unsigned masks[2] = {0u, 0u};
+    const bool empty = !(h.t1 > h.t0);
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int row = rr * 32 + lane;
+      const int pos = h.tbase + row;
+      bool valid = false;
+      int y = 0;
+      if (!empty && row < TT && pos < h.t1) {
+        const int t = __ldg(p.topk_idx + (size_t)h.b * p.topk + pos);
+        if (t >= 0 && t < h.L) {
+          int phys = __ldg(p.block_table + (size_t)h.b * p.maxp + t / p.S);
+          if (phys < 0 || phys >= p.num_pages) {
+            flag_status(p, kStatusBadPage);
+            phys = 0;
+          }
+          y = (phys * p.Hkv + h.g) * p.S + t % p.S;
+          valid = true;
+        }
+      }
+      yv[rr] = y;
+      masks[rr] = __ballot_sync(0xffffffffu, valid);
+      if (ktok && valid) {
+        const uint32_t sc = kst + p.off_scale;
+        float kv = __ldg(p.k_scale + y), vv = __ldg(p.v_scale + y);
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(sc + row * 4), "f"(kv) : "memory");
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(sc + TT * 4 + row * 4), "f"(vv) : "memory");
+      }
+    }
+    h.mask_lo = masks[0];
+    h.mask_hi = masks[1];
+    const uint32_t bytes = empty ? 0u : (uint32_t)TT * 128u * NCH * 2u;
+    __syncwarp();
+    if (lane == 0) {
+      *sm.hdr(s, p) = h;
+      if (bytes)
+        mbar_arrive_tx(sm.full(s, p), bytes);
+      else
+        mbar_arrive(sm.full(s, p));
+    }
+    __syncwarp();
+    if (!empty) {
+      int y4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int src = (4 * lane + i) & 31;
+        const int v0 = __shfl_sync(0xffffffffu, yv[0], src);
+        const int v1 = __shfl_sync(0xffffffffu, yv[1], src);
+        y4[i] = (4 * lane + i < 32) ? v0 : v1;
+      }
+      if (lane < TT / 4) {
+        const uint32_t bar = sm.full(s, p);
+#pragma unroll
+        for (int cb = 0; cb < NCH; ++cb) {
+          tma_gather4(kst + (uint32_t)(cb * TT + 4 * lane) * 128u, tmK, cb * (128 / ELT), y4[0], y4[1], y4[2], y4[3], bar);
+          tma_gather4(vst + (uint32_t)(cb * TT + 4 * lane) * 128u, tmV, cb * (128 / ELT), y4[0], y4[1], y4[2], y4[3], bar);
+        }
+      }
+    }
+  }
+
+  __device__ void emit_end() {
+    int s;
+    if (!acquire_stage(s)) return;
+    if (lane == 0) {
+      StageHdr* hp = sm.hdr(s, p);
+      hp->kind = 1;
+      mbar_arrive(sm.full(s, p));
+    }
+    __syncwarp();
+    ++n;
+  }
+
+  // Emit the stages of one segment: chunks [k0, k1) of unit (b, g).
+  __device__ void segment(int b, int g, const UnitRange& r, int k0, int k1, bool whole, int slot, const MergeDesc& md) {
+    StageHdr h;
+    h.kind = 0;
+    h.unit = b * p.Hkv + g;
+    h.b = b;
+    h.g = g;
+    h.L = r.L;
+    h.mask_lo = h.mask_hi = 0u;
+    h.slot = slot;
+    h.nseg = md.nseg;
+    h.s0 = md.s0;
+    h.sbase = md.sbase;
+    h.sstride = md.sstride;
+    const int kend = (k1 > k0) ? k1 : k0 + 1;
+    for (int k = k0; k < kend && ok; ++k) {
+      h.flags = (k == k0 ? kSegFirst : 0) | (k == kend - 1 ? kSegLast : 0) | (whole ? kSegWhole : 0);
+      if (k1 > k0) {
+        h.tbase = (r.c_lo + k) * p.TT;
+        h.t0 = max(h.tbase, r.lo);
+        h.t1 = min(h.tbase + p.TT, r.hi);
+      } else {
+        h.tbase = 0;
+        h.t0 = h.t1 = 0;
+      }
+      if (p.topk > 0)
+        emit_sparse(h);
+      else
+        emit_dense(h);
+      if (!ok) return;
+      ++n;
+    }
+  }
+
+  __device__ void run() {
+    if (lane == 0) {
+      prefetch_tmap(tmK);
+      prefetch_tmap(tmV);
+    }
+    if (p.sched == kSchedPerUnit) {
+      const int u = blockIdx.x / p.P, j = blockIdx.x % p.P;
+      const int b = u / p.Hkv, g = u % p.Hkv;
+      const UnitRange r = unit_range(p, b);
+      const int k0 = (int)((long long)j * r.n / p.P), k1 = (int)((long long)(j + 1) * r.n / p.P);
+      MergeDesc md{p.P, u * p.P, u * p.P, 1};
+      segment(b, g, r, k0, k1, p.P == 1, u * p.P + j, md);
+    } else {
+      const long long N = balanced_total(p, lane);
+      const long long C = p.C;
+      const long long c = blockIdx.x;
+      long long x = sched_start(c, N, C);
+      const long long x1 = sched_start(c + 1, N, C);
+      if (x < x1) {
+        int b;
+        long long excl;
+        balanced_find(p, lane, x, b, excl);
+        UnitRange r = unit_range(p, b);
+        long long nb = max(1, r.n);
+        int g = (int)((x - excl) / nb);
+        while (x < x1 && ok) {
+          const long long Pu = excl + g * nb;
+          const long long kin = x - Pu;
+          const long long take = min(nb - kin, x1 - x);
+          const MergeDesc md = balanced_desc(Pu, nb, N, C);
+          const int slot = (int)(2 * c + ((c == sched_owner(Pu, N, C) && sched_start(c, N, C) < Pu) ? 1 : 0));
+          if (r.n > 0)
+            segment(b, g, r, (int)kin, (int)(kin + take), md.nseg == 1, slot, md);
+          else
+            segment(b, g, r, 0, 0, md.nseg == 1, slot, md);
+          x += take;
+          if (++g == p.Hkv) {
+            g = 0;
+            excl += (long long)p.Hkv * nb;
+            ++b;
+            if (b < p.B) {
+              r = unit_range(p, b);
+              nb = max(1, r.n);
+            }
+          }
+        }
+      }
+    }
+    if (ok) emit_end();
+    if (!ok) {
+      // Wait (bounded) for copies this warp issued that may still be in flight.
+      const int first = max(0, n - p.NS);
+      for (int m = first; m < n; ++m) (void)mbar_wait(sm.full(m % p.NS, p), (m / p.NS) & 1);
+    }
+  }
+};
+
+// ================================================================ consumers
+template <bool FP8, int D, int NT, bool VTOK>
+struct Consumer {
+  static constexpr int ELT = FP8 ? 1 : 2;
+  static constexpr int NCH = D * ELT / 128;
+  static constexpr int KSTEPS = D / 16;
+  static constexpr int MT = D / 16;
+  static constexpr int KS_BLK = KSTEPS / NCH;
+  static constexpr int MT_BLK = MT / NCH;
+  static constexpr bool QK_F16 = FP8;
+  static constexpr bool PV_F16 = FP8 && !VTOK;
+  static constexpr int RW = 8 * NT;
+  static constexpr int DPB = 128 / ELT;  // head dims per 128-byte block
+
+  const PaParams& p;
+  Smem sm;
+  int lane, g4, t4, cw, wr, wt;
+  float kscale = 1.f, vscale = 1.f;
+  // per segment
+  uint32_t qf[NT][KSTEPS][2];
+  float crow[NT][2];
+  int prow[NT][2];  // query position p_r of the thread's two rows per n-tile (dense masks)
+  float mrun[NT][2], lrun[NT][2];
+  float o[MT][NT][4];
+
+  __device__ Consumer(const PaParams& p_, Smem s) : p(p_), sm(s) {
+    lane = threadIdx.x & 31;
+    g4 = lane >> 2;
+    t4 = lane & 3;
+    cw = threadIdx.x >> 5;
+    wr = cw % p.Wr;
+    wt = cw / p.Wr;
+    if (FP8 && p.scale_mode == kScalePerTensor) kscale = __ldg(p.k_scale);
+    vscale = per_tensor_vscale(p);
+  }
+
+  __device__ __forceinline__ int row_of(int j, int rho) const { return wr * RW + 8 * j + 2 * t4 + rho; }
+
+  __device__ void begin_segment(const StageHdr& h) {
+    // Q rows of this warp's slice as MMA B fragments (row n = g4), with the
+    // head-dim permutation that matches how K rows are read from shared memory.
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const int r = wr * RW + 8 * j + g4;
+      const bool valid = r < p.R;
+      const int i = valid ? r / p.G : 0;
+      const int head = h.g * p.G + (valid ? r % p.G : 0);
+      const uint16_t* qrow = p.q + ((size_t)(h.b * p.QL + i) * p.Hq + head) * D;
+      float crow_n = 0.f;
+      if constexpr (FP8) {
+        // 32 values per block: d in [cb*128 + 32*t4, +32)
+        float amax = 0.f;
+        uint4 raw[NCH][4];
+#pragma unroll
+        for (int cb = 0; cb < NCH; ++cb)
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            raw[cb][v] = valid ? __ldg(reinterpret_cast<const uint4*>(qrow + cb * 128 + 32 * t4) + v) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int cb = 0; cb < NCH; ++cb)
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint32_t w[4] = {raw[cb][v].x, raw[cb][v].y, raw[cb][v].z, raw[cb][v].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[e] & 0xFFFFu)));
+              amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[e] >> 16)));
+            }
+          }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        // power-of-two row scale: amax * 2^e in [2^14, 2^15) keeps every
+        // BF16 value exact in FP16 apart from far-below-max tails
+        int e = 0;
+        if (amax > 0.f) {
+          const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+          e = max(-126, min(126, 14 - ex));
+        }
+        const float sc = __uint_as_float((uint32_t)(e + 127) << 23);
+        const float inv = __uint_as_float((uint32_t)(127 - e) << 23);
+#pragma unroll
+        for (int cb = 0; cb < NCH; ++cb)
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint32_t w[4] = {raw[cb][v].x, raw[cb][v].y, raw[cb][v].z, raw[cb][v].w};
+            // words w[0..3] hold d = 32*t4 + 8v + {0..7}; k-step s_local = 2v + (e>>1)
+#pragma unroll
+            for (int hw = 0; hw < 2; ++hw) {
+              const int s = cb * KS_BLK + 2 * v + hw;
+              qf[j][s][0] = pack_f16(bf16_bits_to_f32(w[2 * hw] & 0xFFFFu) * sc, bf16_bits_to_f32(w[2 * hw] >> 16) * sc);
+              qf[j][s][1] =
+                  pack_f16(bf16_bits_to_f32(w[2 * hw + 1] & 0xFFFFu) * sc, bf16_bits_to_f32(w[2 * hw + 1] >> 16) * sc);
+            }
+          }
+        crow_n = valid ? inv * p.sm_scale_log2 * (p.scale_mode == kScalePerTensor ? kscale : 1.f) : 0.f;
+      } else {
+        // 16 values per block: d in [cb*64 + 16*t4, +16)
+#pragma unroll
+        for (int cb = 0; cb < NCH; ++cb)
+#pragma unroll
+          for (int v = 0; v < 2; ++v) {
+            const uint4 w = valid ? __ldg(reinterpret_cast<const uint4*>(qrow + cb * 64 + 16 * t4) + v) : make_uint4(0, 0, 0, 0);
+            const int s0 = cb * KS_BLK + 2 * v;
+            qf[j][s0][0] = w.x;
+            qf[j][s0][1] = w.y;
+            qf[j][s0 + 1][0] = w.z;
+            qf[j][s0 + 1][1] = w.w;
+          }
+        crow_n = valid ? p.sm_scale_log2 : 0.f;
+      }
+#pragma unroll
+      for (int rho = 0; rho < 2; ++rho) {
+        crow[j][rho] = __shfl_sync(0xffffffffu, crow_n, (2 * t4 + rho) * 4);
+        const int rr = row_of(j, rho);
+        prow[j][rho] = (rr < p.R) ? (h.L - p.QL + rr / p.G) : -(1 << 30);
+        mrun[j][rho] = -INFINITY;
+        lrun[j][rho] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[mt][j][e] = 0.f;
+  }
+
+  // Does stage row `row` (absolute token t) carry real data for every row?
+  __device__ __forceinline__ bool token_ok(const StageHdr& h, int row) const {
+    if (p.topk > 0) return ((row < 32 ? h.mask_lo >> row : h.mask_hi >> (row - 32)) & 1u) != 0u;
+    const int t = h.tbase + row;
+    return t >= h.t0 && t < h.t1;
+  }
+  __device__ __forceinline__ bool score_ok(const StageHdr& h, int row, int j, int rho) const {
+    if (!token_ok(h, row)) return false;
+    if (p.topk > 0) return prow[j][rho] > -(1 << 29);
+    const int t = h.tbase + row;
+    const int pr = prow[j][rho];
+    bool ok = pr > -(1 << 29);
+    if (p.causal) ok = ok && t <= pr;
+    if (p.window > 0) ok = ok && t > pr - p.window;
+    return ok;
+  }
+
+  __device__ void tile(const StageHdr& h, uint32_t kst, uint32_t vst, uint32_t sst, int tau) {
+    const int TT = p.TT;
+    const int swz = p.swz;
+    const int rowA = 16 * tau + g4, rowB = rowA + 8;
+    bool interior;
+    if (p.topk > 0) {
+      const unsigned m16 = (tau < 2 ? (h.mask_lo >> (16 * tau)) : (h.mask_hi >> (16 * (tau - 2)))) & 0xFFFFu;
+      if (m16 == 0u) return;
+      interior = (m16 == 0xFFFFu);
+    } else {
+      const int ta = h.tbase + 16 * tau;
+      if (ta >= h.t1 || ta + 16 <= h.t0) return;
+      const int lo_all = p.window > 0 ? max(0, h.L - p.window) : 0;
+      const int hi_all = p.causal ? h.L - p.QL + 1 : h.L;
+      interior = ta >= max(h.t0, lo_all) && ta + 16 <= min(h.t1, hi_all);
+    }
+    // ---- S^T = K Q^T ------------------------------------------------------
+    float sacc[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[j][e] = 0.f;
+#pragma unroll
+    for (int cb = 0; cb < NCH; ++cb) {
+#pragma unroll
+      for (int hl = 0; hl < 2; ++hl) {
+        const int ch = 2 * t4 + hl;
+        const uint4 ka = lds128(kst + (uint32_t)(cb * TT + rowA) * 128u + (uint32_t)((ch ^ (rowA & swz)) << 4));
+        const uint4 kb = lds128(kst + (uint32_t)(cb * TT + rowB) * 128u + (uint32_t)((ch ^ (rowB & swz)) << 4));
+        const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w};
+        const uint32_t wb[4] = {kb.x, kb.y, kb.z, kb.w};
+        if constexpr (FP8) {
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int s = cb * KS_BLK + hl * 4 + w;
+            const uint32_t a0 = e4m3x2_to_f16x2(wa[w]), a2 = e4m3x2_to_f16x2(wa[w] >> 16);
+            const uint32_t a1 = e4m3x2_to_f16x2(wb[w]), a3 = e4m3x2_to_f16x2(wb[w] >> 16);
+#pragma unroll
+            for (int j = 0; j < NT; ++j) mma16816<true>(sacc[j], a0, a1, a2, a3, qf[j][s][0], qf[j][s][1]);
+          }
+        } else {
+#pragma unroll
+          for (int w2 = 0; w2 < 2; ++w2) {
+            const int s = cb * KS_BLK + hl * 2 + w2;
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+              mma16816<false>(sacc[j], wa[2 * w2], wb[2 * w2], wa[2 * w2 + 1], wb[2 * w2 + 1], qf[j][s][0], qf[j][s][1]);
+          }
+        }
+      }
+    }
+    // ---- scale (before masking), mask, online softmax -------------------------
+    const bool ktok = FP8 && p.scale_mode == kScalePerToken;
+    float ksA = 1.f, ksB = 1.f, vsA = 1.f, vsB = 1.f;
+    if (ktok) {
+      ksA = lds_f32(sst + rowA * 4);
+      ksB = lds_f32(sst + rowB * 4);
+    }
+    if constexpr (VTOK) {
+      vsA = lds_f32(sst + TT * 4 + rowA * 4);
+      vsB = lds_f32(sst + TT * 4 + rowB * 4);
+    }
+    uint32_t pb[NT][2];
+    float alpha[NT][2];
+    bool rescale = false;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      float x[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int rho = e & 1;
+        x[e] = sacc[j][e] * crow[j][rho] * (e < 2 ? ksA : ksB);
+      }
+      if (!interior) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (!score_ok(h, e < 2 ? rowA : rowB, j, e & 1)) x[e] = -INFINITY;
+      }
+      float pe[4];
+#pragma unroll
+      for (int rho = 0; rho < 2; ++rho) {
+        float mx = fmaxf(x[rho], x[rho + 2]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mnew = fmaxf(mrun[j][rho], mx);
+        const float muse = (mnew == -INFINITY) ? 0.f : mnew;
+        const float a = ex2(mrun[j][rho] - muse);
+        pe[rho] = ex2(x[rho] - muse);
+        pe[rho + 2] = ex2(x[rho + 2] - muse);
+        lrun[j][rho] = lrun[j][rho] * a + (pe[rho] + pe[rho + 2]);
+        mrun[j][rho] = mnew;
+        alpha[j][rho] = a;
+        rescale |= (a != 1.f);
+      }
+      if constexpr (VTOK) {
+        // per-token V scale folded into P before rounding (masked tokens: 0)
+        pe[0] *= vsA;
+        pe[1] *= vsA;
+        pe[2] *= vsB;
+        pe[3] *= vsB;
+        if (!interior) {
+          if (!token_ok(h, rowA)) pe[0] = pe[1] = 0.f;
+          if (!token_ok(h, rowB)) pe[2] = pe[3] = 0.f;
+        }
+      }
+      uint32_t x0, x1;
+      if constexpr (PV_F16) {
+        x0 = pack_f16(pe[0], pe[1]);
+        x1 = pack_f16(pe[2], pe[3]);
+      } else {
+        x0 = pack_bf16(pe[0], pe[1]);
+        x1 = pack_bf16(pe[2], pe[3]);
+      }
+      pb[j][0] = movm_trans(x0);
+      pb[j][1] = movm_trans(x1);
+    }
+    if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          o[mt][j][0] *= alpha[j][0];
+          o[mt][j][2] *= alpha[j][0];
+          o[mt][j][1] *= alpha[j][1];
+          o[mt][j][3] *= alpha[j][1];
+        }
+    }
+    // ---- O^T += V^T P^T ---------------------------------------------------------
+    const int vr0 = 16 * tau + 2 * t4;
+    const int vrow[4] = {vr0, vr0 + 1, vr0 + 8, vr0 + 9};
+    bool vok[4] = {true, true, true, true};
+    if (!interior) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) vok[k] = token_ok(h, vrow[k]);
+    }
+#pragma unroll
+    for (int cb = 0; cb < NCH; ++cb) {
+      uint4 vv[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        vv[k] = lds128(vst + (uint32_t)(cb * TT + vrow[k]) * 128u + (uint32_t)((g4 ^ (vrow[k] & swz)) << 4));
+        if (!vok[k]) vv[k] = make_uint4(0, 0, 0, 0);
+      }
+      const uint32_t va[4] = {vv[0].x, vv[0].y, vv[0].z, vv[0].w};
+      const uint32_t vb[4] = {vv[1].x, vv[1].y, vv[1].z, vv[1].w};
+      const uint32_t vc[4] = {vv[2].x, vv[2].y, vv[2].z, vv[2].w};
+      const uint32_t vd[4] = {vv[3].x, vv[3].y, vv[3].z, vv[3].w};
+      if constexpr (FP8) {
+#pragma unroll
+        for (int mt = 0; mt < MT_BLK; ++mt) {
+          const int wi = mt >> 1;
+          const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+          const uint32_t x01 = __byte_perm(va[wi], vb[wi], sel);
+          const uint32_t x23 = __byte_perm(vc[wi], vd[wi], sel);
+          uint32_t r0 = e4m3x2_to_f16x2(x01), r1 = e4m3x2_to_f16x2(x01 >> 16);
+          uint32_t r2 = e4m3x2_to_f16x2(x23), r3 = e4m3x2_to_f16x2(x23 >> 16);
+          if constexpr (!PV_F16) {
+            r0 = f16x2_to_bf16x2(r0);
+            r1 = f16x2_to_bf16x2(r1);
+            r2 = f16x2_to_bf16x2(r2);
+            r3 = f16x2_to_bf16x2(r3);
+          }
+#pragma unroll
+          for (int j = 0; j < NT; ++j) mma16816<PV_F16>(o[cb * MT_BLK + mt][j], r0, r1, r2, r3, pb[j][0], pb[j][1]);
+        }
+      } else {
+#pragma unroll
+        for (int mt = 0; mt < MT_BLK; ++mt) {
+          const uint32_t r0 = __byte_perm(va[mt], vb[mt], 0x5410u);
+          const uint32_t r1 = __byte_perm(va[mt], vb[mt], 0x7632u);
+          const uint32_t r2 = __byte_perm(vc[mt], vd[mt], 0x5410u);
+          const uint32_t r3 = __byte_perm(vc[mt], vd[mt], 0x7632u);
+#pragma unroll
+          for (int j = 0; j < NT; ++j) mma16816<false>(o[cb * MT_BLK + mt][j], r0, r1, r2, r3, pb[j][0], pb[j][1]);
+        }
+      }
+    }
+  }
+
+  __device__ void end_segment(const StageHdr& h) {
+    const int nthr = p.NCW * 32;
+    const int tid = threadIdx.x;
+    float* mb_o = reinterpret_cast<float*>(sm.base + p.off_merge);
+    float* mb_ml = mb_o + (size_t)p.Wt * p.Rpad * D;
+    // 1. per-warp row sums across the 8 token lanes, publish to shared memory
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int rho = 0; rho < 2; ++rho) {
+        float l = lrun[j][rho];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        const int r = row_of(j, rho);
+        if (g4 == 0) {
+          mb_ml[((size_t)wt * p.Rpad + r) * 2 + 0] = mrun[j][rho];
+          mb_ml[((size_t)wt * p.Rpad + r) * 2 + 1] = l;
+        }
+#pragma unroll
+        for (int cb = 0; cb < NCH; ++cb) {
+          // this thread holds d = cb*DPB + (DPB/8)*g4 + {0 .. DPB/8 - 1} of row r
+          float v[DPB / 8];
+#pragma unroll
+          for (int mt = 0; mt < MT_BLK; ++mt) {
+            v[2 * mt] = o[cb * MT_BLK + mt][j][rho];
+            v[2 * mt + 1] = o[cb * MT_BLK + mt][j][rho + 2];
+          }
+          float4* dst = reinterpret_cast<float4*>(mb_o + ((size_t)wt * p.Rpad + r) * D + cb * DPB + (DPB / 8) * g4);
+#pragma unroll
+          for (int q4 = 0; q4 < DPB / 32; ++q4) dst[q4] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+        }
+      }
+    named_bar(1, nthr);
+    // 2. merge the token groups; write output, a global partial, or the cluster partial
+    const bool whole = (h.flags & kSegWhole) != 0;
+    const bool cluster = p.merge == kMergeCluster;
+    float* cp_o = reinterpret_cast<float*>(sm.base + p.off_cpart);
+    float* cp_ml = cp_o + (size_t)p.Rpad * D;
+    const int E = p.R * (D / 4);
+    for (int e = tid; e < E; e += nthr) {
+      const int r = e / (D / 4);
+      const int d = (e % (D / 4)) * 4;
+      float M = -INFINITY;
+      for (int w = 0; w < p.Wt; ++w) M = fmaxf(M, mb_ml[((size_t)w * p.Rpad + r) * 2]);
+      float L = 0.f;
+      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int w = 0; w < p.Wt; ++w) {
+        const float mw = mb_ml[((size_t)w * p.Rpad + r) * 2];
+        if (mw == -INFINITY) continue;
+        const float a = ex2(mw - M);
+        const float4 ow = *reinterpret_cast<const float4*>(mb_o + ((size_t)w * p.Rpad + r) * D + d);
+        L = fmaf(mb_ml[((size_t)w * p.Rpad + r) * 2 + 1], a, L);
+        O.x = fmaf(ow.x, a, O.x);
+        O.y = fmaf(ow.y, a, O.y);
+        O.z = fmaf(ow.z, a, O.z);
+        O.w = fmaf(ow.w, a, O.w);
+      }
+      if (whole) {
+        finalize_store<D>(p, vscale, O, M, L, h.b, h.g, r, d);
+      } else if (cluster) {
+        *reinterpret_cast<float4*>(cp_o + (size_t)r * D + d) = O;
+        if (d == 0) *reinterpret_cast<float2*>(cp_ml + 2 * r) = make_float2(M, L);
+      } else {
+        *reinterpret_cast<float4*>(p.part_o + ((size_t)h.slot * p.Rpad + r) * D + d) = O;
+        if (d == 0) *reinterpret_cast<float2*>(p.part_ml + ((size_t)h.slot * p.Rpad + r) * 2) = make_float2(M, L);
+      }
+    }
+    if (!whole && !cluster) {
+      __threadfence();
+      named_bar(1, nthr);
+      if (p.merge == kMergeReducer) {
+        if (tid == 0 && h.slot == h.s0) p.unit_desc[h.unit] = make_int4(h.nseg, h.s0, h.sbase, h.sstride);
+      } else if (p.merge == kMergeLastArriver) {
+        volatile int* misc = sm.misc(p);
+        if (tid == 0) {
+          const int prev = atomicAdd(p.counters + (size_t)h.unit * kCounterStride, 1);
+          const int last = (prev == h.nseg - 1);
+          if (last) atomicExch(p.counters + (size_t)h.unit * kCounterStride, 0);
+          misc[1] = last;
+        }
+        named_bar(1, nthr);
+        if (misc[1]) {
+          __threadfence();
+          const MergeDesc md{h.nseg, h.s0, h.sbase, h.sstride};
+          merge_elems<D>(
+              p, vscale, h.nseg, h.b, h.g, tid, nthr, 0, E,
+              [&](int k, int r) {
+                return __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((size_t)merge_slot(md, k) * p.Rpad + r) * 2));
+              },
+              [&](int k, int r, int d) {
+                return __ldcg(reinterpret_cast<const float4*>(p.part_o + ((size_t)merge_slot(md, k) * p.Rpad + r) * D + d));
+              });
+        }
+      }
+    }
+    named_bar(1, nthr);  // the merge buffer is reused by the next segment
+  }
+
+  __device__ void run() {
+    int n = 0;
+    StageHdr h;
+    while (true) {
+      const int s = n % p.NS;
+      bool got = mbar_wait(sm.full(s, p), (n / p.NS) & 1);
+      got = __all_sync(0xffffffffu, got);
+      if (!got) {
+        if (lane == 0) {
+          flag_status(p, kStatusTimeout);
+          sm.misc(p)[0] = 1;
+        }
+        break;
+      }
+      h = *sm.hdr(s, p);
+      if (h.kind != 0) break;
+      if (h.flags & kSegFirst) begin_segment(h);
+      const uint32_t kst = sm.stage(s, p);
+      const uint32_t vst = kst + (uint32_t)p.TT * 128u * NCH;
+      const uint32_t sst = kst + p.off_scale;
+      for (int tau = wt; tau < p.TT / 16; tau += p.Wt) tile(h, kst, vst, sst, tau);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.empty(s, p));
+      if (h.flags & kSegLast) end_segment(h);
+      ++n;
+    }
+  }
+
+  // Cluster merge: CTA `rank` of the cluster merges its share of the rows of
+  // all partitions' partials, read over distributed shared memory.
+  __device__ void cluster_merge(int unit) {
+    const int b = unit / p.Hkv, g = unit % p.Hkv;
+    uint32_t rank;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    const int E = p.R * (D / 4);
+    const int e0 = (int)((long long)rank * E / p.P), e1 = (int)((long long)(rank + 1) * E / p.P);
+    const uint32_t cp_local = sm.base_u32 + p.off_cpart;
+    const uint32_t ml_off = (uint32_t)p.Rpad * D * 4u;
+    merge_elems<D>(
+        p, vscale, p.P, b, g, threadIdx.x, p.NCW * 32, e0, e1,
+        [&](int k, int r) {
+          uint32_t remote;
+          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(cp_local + ml_off + 8u * r), "r"(k));
+          float2 v;
+          asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(remote));
+          return v;
+        },
+        [&](int k, int r, int d) {
+          uint32_t remote;
+          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                       : "=r"(remote)
+                       : "r"(cp_local + (uint32_t)(r * D + d) * 4u), "r"(k));
+          float4 v;
+          asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                       : "r"(remote));
+          return v;
+        });
+  }
+};
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <bool FP8, int D, int NT, bool VTOK>
+__global__ void __launch_bounds__(288) pa_tile_kernel(const __grid_constant__ PaParams p,
+                                                      const __grid_constant__ CUtensorMap tmK,
+                                                      const __grid_constant__ CUtensorMap tmV) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem sm;
+  {
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t aligned = (raw + 1023u) & ~1023u;
+    sm.base = smem_raw + (aligned - raw);
+    sm.base_u32 = aligned;
+  }
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.NS; ++s) {
+      mbar_init(sm.full(s, p), 1);
+      mbar_init(sm.empty(s, p), p.NCW);
+    }
+    sm.misc(p)[0] = 0;
+    sm.misc(p)[1] = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  constexpr int ELT = FP8 ? 1 : 2;
+  constexpr int NCH = D * ELT / 128;
+  if (warp == p.NCW) {
+    Producer<ELT, NCH> prod(p, &tmK, &tmV, sm);
+    prod.run();
+  } else {
+    Consumer<FP8, D, NT, VTOK> cons(p, sm);
+    cons.run();
+    if (p.merge == kMergeCluster) {
+      cluster_sync_all();
+      cons.cluster_merge(blockIdx.x / p.P);
+      cluster_sync_all();
+      return;
+    }
+  }
+  if (p.merge == kMergeCluster && warp == p.NCW) {
+    cluster_sync_all();
+    cluster_sync_all();
+  }
+}
+
+// Standalone reducer: one CTA per unit merges the unit's partials in order.
+template <int D>
+__device__ void reduce_unit(const PaParams& p) {
+  const int unit = blockIdx.x;
+  __shared__ int4 desc_s;
+  if (threadIdx.x == 0) desc_s = p.unit_desc[unit];
+  __syncthreads();
+  const int4 desc = desc_s;
+  if (desc.x < 2) return;
+  const MergeDesc md{desc.x, desc.y, desc.z, desc.w};
+  const int b = unit / p.Hkv, g = unit % p.Hkv;
+  merge_elems<D>(
+      p, per_tensor_vscale(p), md.nseg, b, g, threadIdx.x, blockDim.x, 0, p.R * (D / 4),
+      [&](int k, int r) {
+        return __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((size_t)merge_slot(md, k) * p.Rpad + r) * 2));
+      },
+      [&](int k, int r, int d) {
+        return __ldcg(reinterpret_cast<const float4*>(p.part_o + ((size_t)merge_slot(md, k) * p.Rpad + r) * D + d));
+      });
+  __syncthreads();
+  if (threadIdx.x == 0) p.unit_desc[unit].x = 0;
+}
+
+}  // namespace dev
+}  // namespace pa

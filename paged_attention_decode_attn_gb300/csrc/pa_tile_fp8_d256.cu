@@ -1,0 +1,10 @@
+// FP8 e4m3 caches, head_dim 256: tile-kernel instantiations.
+#include "pa_tile.cuh"
+
+namespace pa {
+const void* tile_kernel_fp8_d256(int nt, int vtok) {
+  if (nt == 1 && !vtok) return reinterpret_cast<const void*>(&dev::pa_tile_kernel<true, 256, 1, false>);
+  if (nt == 1 && vtok) return reinterpret_cast<const void*>(&dev::pa_tile_kernel<true, 256, 1, true>);
+  return nullptr;
+}
+}  // namespace pa

@@ -1,0 +1,102 @@
+"""Python restatement of the plan sizing rule, for bit-exact plan tests.
+
+Mirrors the documented behaviour of pa_plan_create with both overrides set:
+kernel shape (rows per warp, warp split, stage tokens), ring depth from the
+shared-memory budget, schedule/merge resolution, grid, partial slots and
+workspace layout.
+"""
+
+SMEM_TWO = 112 * 1024
+SMEM_ONE = 226 * 1024
+COUNTER_STRIDE = 32
+
+
+def align(x, a):
+    return (x + a - 1) // a * a
+
+
+def kernel_shape(d):
+    G = d["num_q_heads"] // d["num_kv_heads"]
+    R = G * d["query_len"]
+    nt = 2 if (d["head_dim"] == 128 and R > 8) else 1
+    rw = 8 * nt
+    wr = -(-R // rw)
+    wt = 1 if wr >= 4 else 4 // wr
+    elt = 1 if d["kv_dtype"] == 0 else 2
+    rb = d["head_dim"] * elt
+    tt = min(64, max(16, 16384 // (2 * rb)))
+    return dict(R=R, G=G, nt=nt, rw=rw, wr=wr, wt=wt, ncw=wr * wt, rpad=wr * rw, elt=elt, rb=rb,
+                tt=tt, bh=min(d["page_size"], tt))
+
+
+def smem_total(d, k, ns, cluster):
+    stage = 2 * k["tt"] * k["rb"] + (1024 if d["scale_mode"] == 2 else 0)
+    off = ns * stage
+    off += align(k["wt"] * k["rpad"] * d["head_dim"] * 4 + k["wt"] * k["rpad"] * 8, 128)
+    if cluster:
+        off += align(k["rpad"] * d["head_dim"] * 4 + k["rpad"] * 8, 128)
+    off += ns * 64 + ns * 16 + 64
+    return stage, off + 1024
+
+
+def plan(d):
+    """Expected pa_plan_info fields for a descriptor dict with overrides set."""
+    k = kernel_shape(d)
+    ns, budget = 0, SMEM_TWO
+    for attempt in range(2):
+        if ns >= 3:
+            break
+        budget = SMEM_TWO if attempt == 0 else SMEM_ONE
+        stage, total0 = smem_total(d, k, 0, True)
+        ns = min(8, (budget - total0) // (stage + 80))
+    assert ns >= 2
+    sm, cps = d["sm_count_override"], d["ctas_per_sm_override"]
+    units = d["batch"] * d["num_kv_heads"]
+    sched, merge, P = d.get("schedule", 0), d.get("merge_mode", 0), d.get("max_partitions", 0)
+    if merge == 1:
+        sched, P = 2, 1
+    if merge == 2:
+        sched = 2
+    if sched == 0:
+        sched = 2 if d.get("sparse_topk", 0) > 0 else 1
+    if sched == 2:
+        if P == 0:
+            p = sm * cps // units if units > 0 else 1
+            p = max(1, min(16, p))
+            mt = d.get("sparse_topk", 0) or d.get("max_context_len", 0)
+            if mt > 0:
+                p = min(p, -(-mt // k["tt"]))
+            P = max(1, p)
+            if merge == 2 and P < 2:
+                P = 2
+    else:
+        P = 0
+    if merge == 0:
+        merge = 3 if sched == 1 else (1 if P == 1 else (2 if P <= 8 else 3))
+    if sched == 2 and P == 1:
+        merge = 1
+    cluster = merge == 2
+    _, smem = smem_total(d, k, ns, cluster)
+    grid = sm * cps if sched == 1 else units * P
+    if units == 0:
+        grid = 0
+    if sched == 1:
+        slots = 2 * grid
+    elif P > 1 and not cluster:
+        slots = units * P
+    else:
+        slots = 0
+    off = align(slots * k["rpad"] * d["head_dim"] * 4, 256)
+    off = align(off + slots * k["rpad"] * 8, 256)
+    if merge == 3:
+        off = align(off + units * COUNTER_STRIDE * 4, 256)
+    if merge == 4:
+        off = align(off + units * 16, 256)
+    status = off
+    off += 256
+    return dict(merge_mode=merge, schedule=sched, num_partitions=P if sched == 2 else 0,
+                stage_tokens=k["tt"], num_stages=ns, rows=k["R"], rows_per_warp=k["rw"],
+                row_warps=k["wr"], token_warps=k["wt"], block_threads=(k["ncw"] + 1) * 32,
+                grid=grid, cluster=P if cluster else 1, ctas_per_sm=cps, sm_count=sm,
+                launches_per_call=2 if merge == 4 else 1, units=units, smem_bytes=smem,
+                workspace_bytes=off, partial_slots=slots, status_offset=status)

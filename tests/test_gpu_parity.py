@@ -1,0 +1,151 @@
+"""GPU parity against the CPU oracle on small seeded inputs (every output
+element), across cache formats, masks, sinks, sparse lists and all merge
+paths. Inputs span several stages and tiles with ragged tails."""
+
+import numpy as np
+import pytest
+
+import oracle
+import paged_attention_decode_attn_gb300 as pa
+import pa_workloads as pw
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+from gpu_util import DeviceWorkload, assert_parity, decode  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.get()
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_attention_decode_attn_gb300 import _build
+
+    _build.build()
+
+
+EDGE_LENS = [0, 1, 15, 16, 17, 63, 64, 65, 127, 200, 777, 1500, 2049]
+
+MODES = [
+    dict(),  # automatic: balanced schedule, last-arriver merge
+    dict(sm_count_override=3, ctas_per_sm_override=1),  # few CTAs: units split across CTAs
+    dict(sm_count_override=5, ctas_per_sm_override=2, merge_mode=pa.PA_MERGE_REDUCER),
+    dict(merge_mode=pa.PA_MERGE_DIRECT),
+    dict(schedule=pa.PA_SCHED_PER_UNIT, max_partitions=3, merge_mode=pa.PA_MERGE_LAST_ARRIVER),
+    dict(schedule=pa.PA_SCHED_PER_UNIT, max_partitions=4, merge_mode=pa.PA_MERGE_CLUSTER),
+    dict(schedule=pa.PA_SCHED_PER_UNIT, max_partitions=5, merge_mode=pa.PA_MERGE_REDUCER),
+]
+MODE_IDS = ["auto", "balanced3", "reducer", "direct", "unit3-la", "cluster4", "unit5-reducer"]
+
+
+def test_tiny(orc):
+    w = pw.tiny()
+    ref = orc.decode(w)
+    dw = DeviceWorkload(w)
+    for m in MODES:
+        gpu, _ = decode(dw, **m)
+        assert_parity(gpu, ref, what=f"tiny {m}")
+
+
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+def test_dense_fp8_edges(orc, mode):
+    w = pw.make_dense("edges", batch=len(EDGE_LENS), hkv=2, group=8, head_dim=128, query_len=1,
+                      page_size=16, ctx_lens=EDGE_LENS, kv_dtype=pw.KV_FP8,
+                      scale_mode=pw.SCALE_PER_TENSOR, seed=7)
+    gpu, _ = decode(DeviceWorkload(w), **mode)
+    assert_parity(gpu, orc.decode(w), what=f"fp8 edges {mode}")
+
+
+@pytest.mark.parametrize("mode", MODES[:4], ids=MODE_IDS[:4])
+def test_dense_bf16(orc, mode):
+    w = pw.make_dense("bf16", batch=6, hkv=2, group=8, head_dim=128, query_len=1, page_size=32,
+                      ctx_lens=[0, 5, 33, 300, 1111, 2500], kv_dtype=pw.KV_BF16,
+                      scale_mode=pw.SCALE_NONE, seed=8)
+    gpu, _ = decode(DeviceWorkload(w), **mode)
+    assert_parity(gpu, orc.decode(w), what=f"bf16 {mode}")
+
+
+@pytest.mark.parametrize("ql", [1, 2, 3, 4])
+@pytest.mark.parametrize("window", [0, 1, 17, 257])
+def test_d256_per_token_mtp_windows(orc, ql, window):
+    lens = [0, 1, 2, 63, 64, 65, 700, 2113, 3001]
+    w = pw.make_dense("d256s", batch=len(lens), hkv=2, group=8, head_dim=256, query_len=ql,
+                      page_size=64, ctx_lens=lens, kv_dtype=pw.KV_FP8, scale_mode=pw.SCALE_PER_TOKEN,
+                      seed=100 + ql, causal=1, window=window, with_sinks=(window % 2 == 1))
+    ref = orc.decode(w)
+    dw = DeviceWorkload(w)
+    for m in (dict(), dict(sm_count_override=4, ctas_per_sm_override=1)):
+        gpu, _ = decode(dw, **m)
+        assert_parity(gpu, ref, what=f"d256 ql{ql} w{window} {m}")
+
+
+@pytest.mark.parametrize("kv", [pw.KV_FP8, pw.KV_BF16], ids=["fp8", "bf16"])
+@pytest.mark.parametrize("mode", MODES[:2] + MODES[4:6], ids=MODE_IDS[:2] + MODE_IDS[4:6])
+def test_mtp4_gqa16(orc, kv, mode):
+    lens = [3, 4, 5, 128, 129, 1000, 2600]
+    w = pw.make_dense("mtp4s", batch=len(lens), hkv=2, group=16, head_dim=128, query_len=4,
+                      page_size=128, ctx_lens=lens, kv_dtype=kv,
+                      scale_mode=pw.SCALE_PER_TENSOR if kv == pw.KV_FP8 else pw.SCALE_NONE,
+                      seed=30, causal=1)
+    gpu, _ = decode(DeviceWorkload(w), **mode)
+    assert_parity(gpu, orc.decode(w), what=f"mtp4 {mode}")
+
+
+@pytest.mark.parametrize("page", [16, 32, 64, 128, 256])
+def test_page_sizes(orc, page):
+    w = pw.make_dense("pages", batch=4, hkv=1, group=4, head_dim=128, query_len=2, page_size=page,
+                      ctx_lens=[1, 100, 513, 1200], kv_dtype=pw.KV_FP8, scale_mode=pw.SCALE_PER_TOKEN,
+                      seed=40 + page, causal=1, window=100)
+    gpu, _ = decode(DeviceWorkload(w))
+    assert_parity(gpu, orc.decode(w), what=f"page {page}")
+
+
+@pytest.mark.parametrize("group,ql", [(1, 1), (2, 3), (4, 4), (12, 5), (8, 8), (64, 1)])
+def test_group_shapes(orc, group, ql):
+    w = pw.make_dense("groups", batch=3, hkv=2, group=group, head_dim=128, query_len=ql,
+                      page_size=16, ctx_lens=[ql, 90, 700], kv_dtype=pw.KV_BF16,
+                      scale_mode=pw.SCALE_NONE, seed=50 + group, causal=1, with_sinks=True)
+    gpu, _ = decode(DeviceWorkload(w))
+    assert_parity(gpu, orc.decode(w), what=f"group {group} ql {ql}")
+
+
+def test_noncausal_mtp(orc):
+    w = pw.make_dense("nc", batch=3, hkv=1, group=8, head_dim=128, query_len=3, page_size=16,
+                      ctx_lens=[2, 40, 300], kv_dtype=pw.KV_FP8, scale_mode=pw.SCALE_PER_TENSOR,
+                      seed=60, causal=0)
+    gpu, _ = decode(DeviceWorkload(w))
+    assert_parity(gpu, orc.decode(w), what="non-causal")
+
+
+SPARSE_MODES = [dict()] + [dict(schedule=pa.PA_SCHED_PER_UNIT, max_partitions=p,
+                                merge_mode=pa.PA_MERGE_CLUSTER) for p in (2, 4, 8, 16)] + [
+    dict(schedule=pa.PA_SCHED_PER_UNIT, max_partitions=8, merge_mode=pa.PA_MERGE_REDUCER),
+    dict(schedule=pa.PA_SCHED_PER_UNIT, max_partitions=8, merge_mode=pa.PA_MERGE_LAST_ARRIVER),
+    dict(schedule=pa.PA_SCHED_BALANCED, merge_mode=pa.PA_MERGE_LAST_ARRIVER),
+    dict(merge_mode=pa.PA_MERGE_DIRECT),
+]
+
+
+@pytest.mark.parametrize("kv", [pw.KV_FP8, pw.KV_BF16], ids=["fp8", "bf16"])
+def test_sparse_small(orc, kv):
+    w = pw.small_sparse(kv_dtype=kv, rows=5, topk=300, context=1000)
+    ref = orc.decode(w)
+    dw = DeviceWorkload(w)
+    for m in SPARSE_MODES:
+        gpu, _ = decode(dw, **m)
+        assert_parity(gpu, ref, what=f"sparse {m}")
+
+
+def test_sparse_per_token_and_sinks(orc):
+    base = pw.make_dense("spt", batch=3, hkv=2, group=4, head_dim=128, query_len=1, page_size=16,
+                         ctx_lens=[500, 37, 0], kv_dtype=pw.KV_FP8, scale_mode=pw.SCALE_PER_TOKEN,
+                         seed=70, causal=0, with_sinks=True)
+    rng = np.random.default_rng(3)
+    idx = np.stack([rng.permutation(600)[:200] for _ in range(3)]).astype(np.int32)
+    w = base.with_(topk=200, topk_idx=idx)
+    gpu, _ = decode(DeviceWorkload(w))
+    assert_parity(gpu, orc.decode(w), what="sparse per-token sinks")
