@@ -1,0 +1,345 @@
+"""Benchmark: paged FP8 decode on one GB300 (dense decode workload).
+
+Workload: batch 64, 8 KV heads, GQA8 (64 query heads), head_dim 128, query
+length 1, page 16, context lengths uniform in [1024, 8192], pages dealt from a
+random permutation of a 40,000-page pool, FP8 e4m3 K/V with per-tensor scales,
+BF16 Q/output (synthetic, seeded).
+
+One step = one pa_decode call over the whole batch. Each timed step is
+preceded by an L2 flush (a 512 MiB device write, outside the events); the
+decode itself is timed with CUDA events on the stream it is launched on.
+`value` is achieved algorithmic HBM bandwidth (K/V of visible tokens,
+block-table entries, context lengths, Q and output, counted once per call),
+aggregated over all ranks; `us_per_call` is the mean device time per call.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+For N > 1 (torchrun) every rank decodes its own batch (replicas; no
+collective on the data path) and rank 0 reports the aggregate over the max
+time across ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import pa_workloads as pw  # noqa: E402
+
+METRIC = "µs/call and achieved HBM GB/s (% of GB300 peak) for paged FP8 decode, 1 GPU"
+WORKLOAD = ("dense FP8 paged decode: batch 64, 8 KV heads, GQA8, head_dim 128, query length 1, "
+            "page 16, contexts U[1024, 8192], 40k-page pool, per-tensor scales")
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+CPU_SAMPLE_UNITS = 48
+
+
+def measured_peak_gbs():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBps", "hbm"):
+            if key in peaks and float(peaks[key]) > 0:
+                return float(peaks[key]), "measured"
+    except (OSError, ValueError, TypeError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    csrc = os.path.join(ROOT, "paged_attention_decode_attn_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "pa_tile_dense_fp8_b64.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_bytes.group(1))
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[2:]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(local_seconds: float, local_bytes: int, group=None):
+    """Max time and total bytes over ranks (timing only; nothing on the data path)."""
+    import torch
+    import torch.distributed as dist
+
+    if not dist.is_initialized():
+        return local_seconds, local_bytes
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=dev)
+    b = torch.tensor([float(local_bytes)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), int(b.item())
+
+
+def cpu_baseline(w, units=CPU_SAMPLE_UNITS, seed=0):
+    """The oracle, as it is, on a bounded sample of units (single thread)."""
+    import oracle
+
+    orc = oracle.get()
+    U = w.batch * w.num_kv_heads
+    rng = np.random.default_rng(seed)
+    pick = rng.choice(U, size=min(units, U), replace=False)
+    mask = np.zeros(U, dtype=np.uint8)
+    mask[pick] = 1
+    t0 = time.perf_counter()
+    orc.decode(w, unit_mask=mask)
+    dt = time.perf_counter() - t0
+    sub_bytes = 0
+    L = w.ctx_lens.astype(np.int64)
+    per_tok = w.head_dim * w.elt_bytes * 2
+    for u in pick:
+        b = int(u) // w.num_kv_heads
+        sub_bytes += int(L[b]) * per_tok + ((int(L[b]) + w.page_size - 1) // w.page_size) * 4
+        sub_bytes += 2 * w.group * w.query_len * w.head_dim * 2
+    return {"value": sub_bytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(pick)} of {U} (sequence, KV head) units of the same workload, "
+                      f"{dt:.1f} s single-threaded C (double precision)",
+            "seconds": dt}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = pw.dense()
+    vals, secs = [], 0.0
+    units = max(4, CPU_SAMPLE_UNITS // 4)
+    for s in range(args.warmup_ref + args.steps_ref):
+        r = cpu_baseline(w, units=units, seed=s)
+        if s >= args.warmup_ref:
+            vals.append(r["value"])
+            secs += r["seconds"]
+    value = float(np.mean(vals))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps_ref, "warmup": args.warmup_ref, "ms_per_step": 1000 * secs / len(vals),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": 64, "seq_len": "U[1024,8192]",
+                       "parallelism": "replicas", "l2": "cpu"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{units} random units per step of the same workload"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.steps_ref = max(1, min(args.steps, 5))
+    args.warmup_ref = 1 if args.warmup > 0 else 0
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    import paged_attention_decode_attn_gb300 as pa
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    w = pw.dense(seed=1002 + rank)
+    alg = pw.algorithmic_bytes(w)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    host = {
+        "q": torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "k": torch.from_numpy(w.k_cache).pin_memory(),
+        "v": torch.from_numpy(w.v_cache).pin_memory(),
+        "bt": torch.from_numpy(w.block_table).pin_memory(),
+        "ctx": torch.from_numpy(w.ctx_lens).pin_memory(),
+        "ks": torch.from_numpy(w.k_scale).pin_memory(),
+        "vs": torch.from_numpy(w.v_scale).pin_memory(),
+    }
+    d = {k: v.to(dev) for k, v in host.items()}
+    out = torch.empty_like(d["q"])
+    plan = pa.Plan(device=dev, batch=w.batch, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                   head_dim=w.head_dim, query_len=w.query_len, page_size=w.page_size,
+                   max_pages_per_seq=w.max_pages_per_seq, num_pages=w.num_pages,
+                   max_context_len=8192, kv_dtype=w.kv_dtype, scale_mode=w.scale_mode, causal=1)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        plan.decode(out, d["q"], d["k"], d["v"], d["bt"], d["ctx"], d["ks"], d["vs"], 0, None, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with Clocks(dev.index) as clk:
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    per_call_ms = np.array([s.elapsed_time(e) for s, e in zip(starts, ends)])
+    local_s = float(per_call_ms.sum()) / 1000.0
+    tot_s, tot_bytes = aggregate(local_s, alg * K)
+    status = plan.device_status()
+
+    # end to end through the public API: pinned host inputs -> device, decode, output -> host
+    e2e_steps = args.e2e_steps
+    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out.numel() * out.element_size()
+    for i in range(e2e_steps + 2):
+        if i == 2:
+            torch.cuda.synchronize(dev)
+            if world > 1:
+                dist.barrier()
+            t0 = time.perf_counter()
+        for k_, v_ in host.items():
+            d[k_].copy_(v_, non_blocking=True)
+        step()
+        out_host.copy_(out, non_blocking=True)
+        torch.cuda.synchronize(dev)
+    e2e_local = time.perf_counter() - t0
+    e2e_s, e2e_bytes = aggregate(e2e_local, alg * e2e_steps)
+
+    if rank == 0:
+        peak, peak_kind = measured_peak_gbs()
+        per_launch_us = float(np.mean(per_call_ms)) * 1000.0
+        achieved = alg / (per_launch_us * 1e-6) / 1e9
+        value = tot_bytes / tot_s / 1e9
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": float(np.mean(per_call_ms)),
+            "us_per_call": per_launch_us, "us_per_call_median": float(np.median(per_call_ms)) * 1000.0,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 (KV), bf16 (Q/O), f32 accumulate",
+            "data": "synthetic (seeded pa_workloads.dense)",
+            "config": {"workload": WORKLOAD, "global_batch": 64 * world, "seq_len": "U[1024,8192]",
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "l2": "flushed before every timed call (512 MiB write); KV 604 MB > L2",
+                       "plan": {k: plan.info[k] for k in ("schedule", "merge_mode", "grid", "block_threads",
+                                                         "num_stages", "stage_tokens", "ctas_per_sm")}},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": peak_kind, "traffic": profiled_traffic(),
+                         "algorithmic_bytes_per_launch": alg, "kernel": "pa_tile_kernel<fp8,128,1>"},
+            "e2e": {"value": e2e_bytes / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h), "steps": e2e_steps},
+            "gpu_launches": int(K * plan.info["launches_per_call"]),
+            "clocks": clk.summary(),
+            "device_status": status,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            cb = cpu_baseline(w)
+            cb.pop("seconds")
+            line["cpu_baseline"] = cb
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

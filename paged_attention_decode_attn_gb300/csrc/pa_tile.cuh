@@ -581,11 +581,13 @@ struct Producer {
       MergeDesc md{p.P, u * p.P, u * p.P, 1};
       segment(b, g, r, k0, k1, p.P == 1, u * p.P + j, md);
     } else {
+      // With fewer chunks than CTAs only the first N CTAs take work, so every
+      // CTA between a unit's first and last owner holds part of that unit.
       const long long N = balanced_total(p, lane);
-      const long long C = p.C;
+      const long long C = min((long long)p.C, N);
       const long long c = blockIdx.x;
-      long long x = sched_start(c, N, C);
-      const long long x1 = sched_start(c + 1, N, C);
+      long long x = c < C ? sched_start(c, N, C) : 0;
+      const long long x1 = c < C ? sched_start(c + 1, N, C) : 0;
       if (x < x1) {
         int b;
         long long excl;
