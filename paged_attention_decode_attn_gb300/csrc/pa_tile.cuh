@@ -138,13 +138,6 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
   return r;
 }
-// f16x2 -> bf16x2; exact for values that came from e4m3.
-__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
-  __half2 hv = *reinterpret_cast<__half2*>(&h);
-  float2 f = __half22float2(hv);
-  __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
-  return *reinterpret_cast<uint32_t*>(&b);
-}
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -637,7 +630,7 @@ struct Consumer {
   static constexpr int KS_BLK = KSTEPS / NCH;
   static constexpr int MT_BLK = MT / NCH;
   static constexpr bool QK_F16 = FP8;
-  static constexpr bool PV_F16 = FP8 && !VTOK;
+  static constexpr bool PV_F16 = FP8;
   static constexpr int RW = 8 * NT;
   static constexpr int DPB = 128 / ELT;  // head dims per 128-byte block
 
@@ -651,6 +644,9 @@ struct Consumer {
   int prow[NT][2];  // query position p_r of the thread's two rows per n-tile (dense masks)
   float mrun[NT][2], lrun[NT][2];
   float o[MT][NT][4];
+  // Per-token V scales: O is kept in units of 2^vexp so that P * v_scale / 2^vexp
+  // stays <= 1 and is rounded to FP16 (exact power-of-two rescales of O).
+  int vexp = -127;
 
   __device__ Consumer(const PaParams& p_, Smem s) : p(p_), sm(s) {
     lane = threadIdx.x & 31;
@@ -752,6 +748,7 @@ struct Consumer {
       for (int j = 0; j < NT; ++j)
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[mt][j][e] = 0.f;
+    vexp = -127;
   }
 
   // Does stage row `row` (absolute token t) carry real data for every row?
@@ -829,13 +826,30 @@ struct Consumer {
       ksA = lds_f32(sst + rowA * 4);
       ksB = lds_f32(sst + rowB * 4);
     }
-    if constexpr (VTOK) {
-      vsA = lds_f32(sst + TT * 4 + rowA * 4);
-      vsB = lds_f32(sst + TT * 4 + rowB * 4);
-    }
     uint32_t pb[NT][2];
     float alpha[NT][2];
     bool rescale = false;
+    float vfix = 1.f;
+    if constexpr (VTOK) {
+      vsA = lds_f32(sst + TT * 4 + rowA * 4);
+      vsB = lds_f32(sst + TT * 4 + rowB * 4);
+      // the tile's largest valid V scale sets the power-of-two unit of O
+      float vm = fmaxf((interior || token_ok(h, rowA)) ? vsA : 0.f, (interior || token_ok(h, rowB)) ? vsB : 0.f);
+      vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 4));
+      vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 8));
+      vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 16));
+      if (vm > 0.f) {
+        const int et = min(120, (int)((__float_as_uint(vm) >> 23) & 0xFF) - 126);  // vm < 2^et
+        if (et > vexp) {
+          vfix = vexp <= -127 ? 0.f : __uint_as_float((uint32_t)max(0, vexp - et + 127) << 23);
+          vexp = et;
+          rescale = true;
+        }
+      }
+      const float inv = __uint_as_float((uint32_t)(127 - max(vexp, -126)) << 23);
+      vsA *= inv;
+      vsB *= inv;
+    }
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       float x[4];
@@ -863,7 +877,7 @@ struct Consumer {
         pe[rho + 2] = ex2(x[rho + 2] - muse);
         lrun[j][rho] = lrun[j][rho] * a + (pe[rho] + pe[rho + 2]);
         mrun[j][rho] = mnew;
-        alpha[j][rho] = a;
+        alpha[j][rho] = a * vfix;
         rescale |= (a != 1.f);
       }
       if constexpr (VTOK) {
@@ -926,14 +940,8 @@ struct Consumer {
           const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
           const uint32_t x01 = __byte_perm(va[wi], vb[wi], sel);
           const uint32_t x23 = __byte_perm(vc[wi], vd[wi], sel);
-          uint32_t r0 = e4m3x2_to_f16x2(x01), r1 = e4m3x2_to_f16x2(x01 >> 16);
-          uint32_t r2 = e4m3x2_to_f16x2(x23), r3 = e4m3x2_to_f16x2(x23 >> 16);
-          if constexpr (!PV_F16) {
-            r0 = f16x2_to_bf16x2(r0);
-            r1 = f16x2_to_bf16x2(r1);
-            r2 = f16x2_to_bf16x2(r2);
-            r3 = f16x2_to_bf16x2(r3);
-          }
+          const uint32_t r0 = e4m3x2_to_f16x2(x01), r1 = e4m3x2_to_f16x2(x01 >> 16);
+          const uint32_t r2 = e4m3x2_to_f16x2(x23), r3 = e4m3x2_to_f16x2(x23 >> 16);
 #pragma unroll
           for (int j = 0; j < NT; ++j) mma16816<PV_F16>(o[cb * MT_BLK + mt][j], r0, r1, r2, r3, pb[j][0], pb[j][1]);
         }
@@ -956,6 +964,8 @@ struct Consumer {
     const int tid = threadIdx.x;
     float* mb_o = reinterpret_cast<float*>(sm.base + p.off_merge);
     float* mb_ml = mb_o + (size_t)p.Wt * p.Rpad * D;
+    // O in true units (per-token V scales: undo the power-of-two unit)
+    const float ounit = VTOK ? __uint_as_float((uint32_t)(max(vexp, -126) + 127) << 23) : 1.f;
     // 1. per-warp row sums across the 8 token lanes, publish to shared memory
 #pragma unroll
     for (int j = 0; j < NT; ++j)
@@ -976,8 +986,8 @@ struct Consumer {
           float v[DPB / 8];
 #pragma unroll
           for (int mt = 0; mt < MT_BLK; ++mt) {
-            v[2 * mt] = o[cb * MT_BLK + mt][j][rho];
-            v[2 * mt + 1] = o[cb * MT_BLK + mt][j][rho + 2];
+            v[2 * mt] = o[cb * MT_BLK + mt][j][rho] * ounit;
+            v[2 * mt + 1] = o[cb * MT_BLK + mt][j][rho + 2] * ounit;
           }
           float4* dst = reinterpret_cast<float4*>(mb_o + ((size_t)wt * p.Rpad + r) * D + cb * DPB + (DPB / 8) * g4);
 #pragma unroll
@@ -1117,7 +1127,7 @@ __device__ __forceinline__ void cluster_sync_all() {
 }
 
 template <bool FP8, int D, int NT, bool VTOK>
-__global__ void __launch_bounds__(288) pa_tile_kernel(const __grid_constant__ PaParams p,
+__global__ void __launch_bounds__(D == 256 ? 288 : 160) pa_tile_kernel(const __grid_constant__ PaParams p,
                                                       const __grid_constant__ CUtensorMap tmK,
                                                       const __grid_constant__ CUtensorMap tmV) {
   extern __shared__ uint8_t smem_raw[];
