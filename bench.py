@@ -274,6 +274,9 @@ def main():
         dist.barrier()
     torch.cuda.synchronize(dev)
     with Clocks(dev.index) as clk:
+        # Keep the GPU busy while the host enqueues the timed steps, so that no
+        # host-side gap falls between a step's start and end events.
+        torch.cuda._sleep(int(3e8))
         for i in range(K):
             flush.fill_(i & 0xFF)
             starts[i].record(stream)

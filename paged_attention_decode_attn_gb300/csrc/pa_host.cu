@@ -61,7 +61,7 @@ constexpr int kSmemTwoPerSm = 112 * 1024;
 constexpr int kSmemOnePerSm = 226 * 1024;
 
 struct KernelShape {
-  int nt, rw, wr, wt, ncw, rpad, elt, rb, nch, tt, bh;
+  int nt, rw, wr, wt, ncw, rpad, elt, rb, nch, tt, tw, bh;
   bool vtok;
 };
 
@@ -78,8 +78,11 @@ KernelShape kernel_shape(const pa_plan_desc& d) {
   k.elt = d.kv_dtype == PA_KV_FP8_E4M3 ? 1 : 2;
   k.rb = d.head_dim * k.elt;
   k.nch = k.rb / 128;
-  int tt = 16384 / (2 * k.rb);
-  k.tt = tt < 16 ? 16 : (tt > 64 ? 64 : tt);
+  // 32 KiB of K+V per ring stage; FP8 head_dim 128 steps two 16-token tiles
+  // per warp (128-token stages), every other format one tile.
+  int tt = 32768 / (2 * k.rb);
+  k.tt = tt < 16 ? 16 : (tt > 128 ? 128 : tt);
+  k.tw = (d.kv_dtype == PA_KV_FP8_E4M3 && d.head_dim == 128) ? 2 : 1;
   k.bh = d.page_size < k.tt ? d.page_size : k.tt;
   k.vtok = d.kv_dtype == PA_KV_FP8_E4M3 && d.scale_mode == PA_SCALE_PER_TOKEN;
   return k;
@@ -93,25 +96,26 @@ pa::SmemLayout smem_layout(const pa_plan_desc& d, const KernelShape& k, int ns, 
   L.off_stage = 0;
   size_t off = (size_t)ns * L.stage_bytes;
   L.off_merge = (int)off;
-  off += align_up((size_t)k.wt * k.rpad * d.head_dim * 4 + (size_t)k.wt * k.rpad * 8, 128);
-  L.off_cpart = (int)off;
-  if (cluster) off += align_up((size_t)k.rpad * d.head_dim * 4 + (size_t)k.rpad * 8, 128);
+  L.off_cpart = (int)off;  // cluster merge: per-warp partials of this CTA
+  if (cluster) off += align_up((size_t)k.wt * k.rpad * d.head_dim * 4 + (size_t)k.wt * k.rpad * 8, 128);
   L.off_hdr = (int)off;
-  off += (size_t)ns * 64;
+  off += (size_t)ns * 128;
   L.off_bar = (int)off;
   off += (size_t)ns * 16;
   L.off_misc = (int)off;
   off += 64;
+  L.off_pend = (int)off;  // queued last-arriver merges: 32 entries of 32 bytes
+  off += 32 * 32;
   L.total = (int)(off + 1024);  // slack for aligning the base to 1024 bytes
   return L;
 }
 
 const void* pick_tile_kernel(const pa_plan_desc& d, const KernelShape& k) {
   if (d.kv_dtype == PA_KV_FP8_E4M3) {
-    if (d.head_dim == 128) return pa::tile_kernel_fp8_d128(k.nt, k.vtok);
-    return pa::tile_kernel_fp8_d256(k.nt, k.vtok);
+    if (d.head_dim == 128) return pa::tile_kernel_fp8_d128(k.nt, k.vtok, k.tw);
+    return pa::tile_kernel_fp8_d256(k.nt, k.vtok, k.tw);
   }
-  return pa::tile_kernel_bf16(d.head_dim, k.nt);
+  return pa::tile_kernel_bf16(d.head_dim, k.nt, k.tw);
 }
 
 pa_status validate_desc(const pa_plan_desc& d) {
@@ -127,6 +131,8 @@ pa_status validate_desc(const pa_plan_desc& d) {
   const long long rows = (long long)(d.num_q_heads / d.num_kv_heads) * d.query_len;
   if (rows > pa::kMaxRows)
     return fail(PA_ERR_UNSUPPORTED, "group*query_len = %lld query rows per KV head exceeds %d", rows, pa::kMaxRows);
+  if (d.head_dim == 256 && rows > 32)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim 256 supports at most 32 query rows per KV head (got %lld)", rows);
   if (d.page_size != 16 && d.page_size != 32 && d.page_size != 64 && d.page_size != 128 && d.page_size != 256)
     return fail(PA_ERR_UNSUPPORTED, "page_size %d unsupported (16, 32, 64, 128, 256)", d.page_size);
   if (d.max_pages_per_seq < 1 || d.num_pages < 1)
@@ -216,14 +222,17 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   pl->reduce_fn = pa::reduce_kernel(d.head_dim);
   if (!pl->tile_fn || !pl->reduce_fn) return fail(PA_ERR_UNSUPPORTED, "no kernel for this configuration");
 
-  // Ring depth: as many 16 KiB stages as fit two CTAs per SM (at least 3),
-  // else one CTA per SM.
+  // Ring depth. Kernels light enough for two CTAs per SM (head_dim 128 with
+  // 8-row warp tiles: at most 168 registers, so three warps share an SM
+  // sub-partition's register file) get as many stages as fit 112 KiB (at
+  // least 3); the others one CTA per SM and up to 226 KiB.
+  const bool two_per_sm = d.head_dim == 128 && k.nt == 1;
   int ns = 0;
   int budget = kSmemTwoPerSm;
-  for (int attempt = 0; attempt < 2 && ns < 3; ++attempt) {
+  for (int attempt = two_per_sm ? 0 : 1; attempt < 2 && ns < 3; ++attempt) {
     budget = attempt == 0 ? kSmemTwoPerSm : kSmemOnePerSm;
-    const pa::SmemLayout l0 = smem_layout(d, k, 0, true);
-    const int stage = l0.stage_bytes + 64 + 16;
+    const pa::SmemLayout l0 = smem_layout(d, k, 0, d.sparse_topk > 0 || d.merge_mode == PA_MERGE_CLUSTER);
+    const int stage = l0.stage_bytes + 128 + 16;
     ns = (budget - l0.total) / stage;
     if (ns > 8) ns = 8;
   }
@@ -243,21 +252,26 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   const int R = G * d.query_len;
   long long grid = sched == PA_SCHED_BALANCED ? (long long)sm_count * ctas_per_sm : (long long)units * P;
   if (units == 0) grid = 0;
+  // Partials are per (segment slot, token-group warp). A unit needs merging
+  // unless one warp group saw all of it (per-unit, one partition, Wt == 1).
   size_t slots = 0;
   if (sched == PA_SCHED_BALANCED)
-    slots = 2 * (size_t)grid;
-  else if (P > 1 && !cluster)
+    slots = units > 0 ? 2 * (size_t)grid + units : 0;
+  else if ((P > 1 && !cluster) || (P == 1 && k.wt > 1))
     slots = (size_t)units * P;
+  // Direct output with several token groups merges them like a last arriver.
+  const int kernel_merge = (merge == PA_MERGE_DIRECT) ? PA_MERGE_LAST_ARRIVER : merge;
+  const bool counters = kernel_merge == PA_MERGE_LAST_ARRIVER && slots > 0;
 
-  // workspace: partial O, partial (max, sum), arrival counters, reducer
-  // descriptors, status word
+  // workspace: partial O, partial (max, sum), arrival counters (one line per
+  // unit and row slice), reducer descriptors, status word
   size_t off = 0;
   pl->off_part_o = off;
-  off = align_up(off + slots * k.rpad * d.head_dim * 4, 256);
+  off = align_up(off + slots * k.wt * k.rpad * d.head_dim * 4, 256);
   pl->off_part_ml = off;
-  off = align_up(off + slots * k.rpad * 8, 256);
+  off = align_up(off + slots * k.wt * k.rpad * 8, 256);
   pl->off_counters = off;
-  if (merge == PA_MERGE_LAST_ARRIVER) off = align_up(off + (size_t)units * pa::kCounterStride * 4, 256);
+  if (counters) off = align_up(off + (size_t)units * k.wr * pa::kCounterStride * 4, 256);
   pl->off_desc = off;
   if (merge == PA_MERGE_REDUCER) off = align_up(off + (size_t)units * 16, 256);
   pl->off_status = off;
@@ -281,7 +295,7 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   in.units = units;
   in.smem_bytes = (size_t)L.total;
   in.workspace_bytes = off;
-  in.partial_slots = slots;
+  in.partial_slots = slots * k.wt;
   in.status_offset = pl->off_status;
 
   pa::PaParams& p = pl->base;
@@ -304,7 +318,7 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   const float sm_scale = d.sm_scale > 0.f ? d.sm_scale : 1.0f / std::sqrt((float)d.head_dim);
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   p.sched = sched;
-  p.merge = merge;
+  p.merge = kernel_merge;
   p.C = sched == PA_SCHED_BALANCED ? (int)grid : 0;
   p.P = sched == PA_SCHED_PER_UNIT ? P : 0;
   p.TT = k.tt;
@@ -322,6 +336,7 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   p.off_merge = L.off_merge;
   p.off_cpart = L.off_cpart;
   p.off_misc = L.off_misc;
+  p.off_pend = L.off_pend;
   return PA_OK;
 }
 

@@ -51,21 +51,22 @@ struct PaParams {
   int swz;          // XOR mask of the 128-byte swizzle (7) or 0 (linear rows)
   // dynamic shared memory layout (byte offsets from a 1024-aligned base)
   int off_stage, stage_bytes, off_scale;  // off_scale: within a stage
-  int off_hdr, off_bar, off_merge, off_cpart, off_misc;
+  int off_hdr, off_bar, off_merge, off_cpart, off_misc, off_pend;
 };
 
 // Host-visible shared-memory sizing for a kernel configuration.
 struct SmemLayout {
-  int stage_bytes, off_stage, off_scale, off_hdr, off_bar, off_merge, off_cpart, off_misc, total;
+  int stage_bytes, off_stage, off_scale, off_hdr, off_bar, off_merge, off_cpart, off_misc, off_pend, total;
 };
 
 using KernelFn = void (*)(PaParams, CUtensorMap, CUtensorMap);
 
 // Tile-kernel instantiations (defined in the pa_tile_*.cu files).
 // Returns null when the combination is not instantiated.
-const void* tile_kernel_fp8_d128(int nt, int vtok);
-const void* tile_kernel_fp8_d256(int nt, int vtok);
-const void* tile_kernel_bf16(int d, int nt);
+const void* tile_kernel_fp8_d128(int nt, int vtok, int tw);
+const void* tile_kernel_fp8_d256(int nt, int vtok, int tw);
+const void* tile_kernel_bf16(int d, int nt, int tw);
 const void* reduce_kernel(int d);
+
 
 }  // namespace pa

@@ -36,17 +36,24 @@ namespace dev {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
+// Stage header written by the producer before it arms the stage. Consumers
+// read the first 32 bytes on every stage (48 for sparse), the rest only at
+// segment boundaries.
 struct alignas(16) StageHdr {
-  int kind;  // 0 = data, 1 = end of work
-  int flags; // kSeg*
-  int unit, b;
-  int g, tbase, t0, t1;  // tbase: token (index position) of stage row 0; [t0, t1): rows to use
-  int L;
-  unsigned mask_lo, mask_hi;  // sparse: validity of stage rows 0..31, 32..63
-  int slot;                   // partial slot of this segment
-  int nseg, s0, sbase, sstride;
+  int kind_flags;  // kSeg* flags; kEnd marks the end of the CTA's work
+  int tbase;       // token (sparse: index position) of stage row 0
+  int t0, t1;      // rows [t0 - tbase, t1 - tbase) carry real tokens of the visible range
+  int L;           // context length of the sequence
+  int unit, b, g;  // (sequence, KV head) unit
+  unsigned mask[4];  // sparse: validity of stage rows 0..127
+  int slot;          // partial slot of this segment
+  int nseg, s0, sbase;
+  int sstride;       // merge slot list: k == 0 -> s0, else sbase + k * sstride
+  int pad[15];
 };
-static_assert(sizeof(StageHdr) == 64, "header size");
+static_assert(sizeof(StageHdr) == 128, "header size");
+constexpr int kEnd = 1 << 8;
+constexpr int kPendingMax = 32;  // queued last-arriver merges per CTA
 
 // ---------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -68,11 +75,13 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
+  // The suspend-time hint lets the warp sleep until the phase completes
+  // instead of spinning on the barrier.
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(1000000u)
       : "memory");
   return ok != 0;
 }
@@ -87,7 +96,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   const unsigned long long t0 = global_timer();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 64; ++i)
+    for (int i = 0; i < 4; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (global_timer() - t0 > kWaitLimitNs) return false;
   }
@@ -117,6 +126,11 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ int4 lds128i(uint32_t addr) {
+  int4 v;
+  asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
   return v;
 }
 __device__ __forceinline__ float lds_f32(uint32_t addr) {
@@ -269,6 +283,9 @@ struct Smem {
   __device__ __forceinline__ StageHdr* hdr(int s, const PaParams& p) const {
     return reinterpret_cast<StageHdr*>(base + p.off_hdr) + s;
   }
+  __device__ __forceinline__ uint32_t hdr_u32(int s, const PaParams& p) const {
+    return base_u32 + p.off_hdr + 128u * s;
+  }
   __device__ __forceinline__ uint32_t full(int s, const PaParams& p) const { return base_u32 + p.off_bar + 8 * s; }
   __device__ __forceinline__ uint32_t empty(int s, const PaParams& p) const {
     return base_u32 + p.off_bar + 8 * (p.NS + s);
@@ -307,32 +324,59 @@ __device__ __forceinline__ void finalize_store(const PaParams& p, float vscale, 
   *reinterpret_cast<uint2*>(p.out + ((size_t)(b * p.QL + i) * p.Hq + head) * D + d) = st;
 }
 
-// Merge n partials (max, sum, O) in order k = 0..n-1 for output elements
-// [e0, e1) (groups of 4 head dims) and store the BF16 rows. Every merge path
-// (last arriver, cluster, reducer) goes through this function.
+// Merge n partials (max, sum, O) in order q = 0..n-1 for output elements
+// [e0, e1) (groups of 4 head dims, row-major over the unit's rows) and store
+// the BF16 rows. Every merge path (last arriver, cluster, reducer) goes
+// through this function with the same partial order, so they agree bit for bit.
 template <int D, class LoadML, class LoadO>
 __device__ __forceinline__ void merge_elems(const PaParams& p, float vscale, int n, int b, int g, int tid, int nthr,
                                             int e0, int e1, LoadML load_ml, LoadO load_o) {
+  constexpr int kStaged = 16;  // partials whose (max, sum) are loaded up front
   for (int e = e0 + tid; e < e1; e += nthr) {
     const int r = e / (D / 4);
     const int d = (e % (D / 4)) * 4;
     float M = -INFINITY;
-    for (int k = 0; k < n; ++k) M = fmaxf(M, load_ml(k, r).x);
+    float2 ml[kStaged];
+#pragma unroll
+    for (int q = 0; q < kStaged; ++q)
+      if (q < n) ml[q] = load_ml(q, r);
+#pragma unroll
+    for (int q = 0; q < kStaged; ++q)
+      if (q < n) M = fmaxf(M, ml[q].x);
+    for (int q = kStaged; q < n; ++q) M = fmaxf(M, load_ml(q, r).x);
     float L = 0.f;
     float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < n; ++k) {
-      const float2 ml = load_ml(k, r);
-      if (ml.x == -INFINITY) continue;
-      const float a = ex2(ml.x - M);
-      const float4 ok = load_o(k, r, d);
-      L = fmaf(ml.y, a, L);
-      O.x = fmaf(ok.x, a, O.x);
-      O.y = fmaf(ok.y, a, O.y);
-      O.z = fmaf(ok.z, a, O.z);
-      O.w = fmaf(ok.w, a, O.w);
+#pragma unroll
+    for (int q = 0; q < kStaged; ++q) {
+      if (q < n && ml[q].x != -INFINITY) {
+        const float a = ex2(ml[q].x - M);
+        const float4 oq = load_o(q, r, d);
+        L = fmaf(ml[q].y, a, L);
+        O.x = fmaf(oq.x, a, O.x);
+        O.y = fmaf(oq.y, a, O.y);
+        O.z = fmaf(oq.z, a, O.z);
+        O.w = fmaf(oq.w, a, O.w);
+      }
+    }
+    for (int q = kStaged; q < n; ++q) {
+      const float2 m2 = load_ml(q, r);
+      if (m2.x == -INFINITY) continue;
+      const float a = ex2(m2.x - M);
+      const float4 oq = load_o(q, r, d);
+      L = fmaf(m2.y, a, L);
+      O.x = fmaf(oq.x, a, O.x);
+      O.y = fmaf(oq.y, a, O.y);
+      O.z = fmaf(oq.z, a, O.z);
+      O.w = fmaf(oq.w, a, O.w);
     }
     finalize_store<D>(p, vscale, O, M, L, b, g, r, d);
   }
+}
+
+// Storage index of the q-th partial of a unit: segment k = q / Wt (in
+// schedule order), token group w = q % Wt.
+__device__ __forceinline__ size_t partial_index(const MergeDesc& md, int Wt, int q) {
+  return (size_t)merge_slot(md, q / Wt) * Wt + (q % Wt);
 }
 
 __device__ __forceinline__ float per_tensor_vscale(const PaParams& p) {
@@ -359,7 +403,8 @@ struct Producer {
     if (lp < 0 || lp >= npages_b) return -1;
     return __ldg(p.block_table + (size_t)b * p.maxp + lp);
   }
-  // Physical page of logical page lp0 + lane for lanes < cnt (cnt <= 4, inside one aligned batch).
+  // Physical page of logical page lp0 + lane (lanes < pages in the stage; the
+  // stage's pages lie inside one aligned batch of 32).
   __device__ __forceinline__ int staged_pages(int b, int L, int lp0, int align) {
     if (b != pid_b) {
       pid_b = b;
@@ -453,11 +498,10 @@ struct Producer {
     const uint32_t kst = sm.stage(s, p);
     const uint32_t vst = kst + (uint32_t)TT * 128u * NCH;
     const bool ktok = p.scale_mode == kScalePerToken;
-    int yv[2] = {0, 0};
-    unsigned masks[2] = {0u, 0u};
     const bool empty = !(h.t1 > h.t0);
+    int yv[4];
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
+    for (int rr = 0; rr < 4; ++rr) {
       const int row = rr * 32 + lane;
       const int pos = h.tbase + row;
       bool valid = false;
@@ -475,16 +519,14 @@ struct Producer {
         }
       }
       yv[rr] = y;
-      masks[rr] = __ballot_sync(0xffffffffu, valid);
+      h.mask[rr] = __ballot_sync(0xffffffffu, valid);
       if (ktok && valid) {
         const uint32_t sc = kst + p.off_scale;
-        float kv = __ldg(p.k_scale + y), vv = __ldg(p.v_scale + y);
+        const float kv = __ldg(p.k_scale + y), vv = __ldg(p.v_scale + y);
         asm volatile("st.shared.f32 [%0], %1;" ::"r"(sc + row * 4), "f"(kv) : "memory");
         asm volatile("st.shared.f32 [%0], %1;" ::"r"(sc + TT * 4 + row * 4), "f"(vv) : "memory");
       }
     }
-    h.mask_lo = masks[0];
-    h.mask_hi = masks[1];
     const uint32_t bytes = empty ? 0u : (uint32_t)TT * 128u * NCH * 2u;
     __syncwarp();
     if (lane == 0) {
@@ -496,13 +538,17 @@ struct Producer {
     }
     __syncwarp();
     if (!empty) {
+      // lane q gathers stage rows 4q .. 4q+3 (round 4q / 32 of the y registers)
       int y4[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int src = (4 * lane + i) & 31;
         const int v0 = __shfl_sync(0xffffffffu, yv[0], src);
         const int v1 = __shfl_sync(0xffffffffu, yv[1], src);
-        y4[i] = (4 * lane + i < 32) ? v0 : v1;
+        const int v2 = __shfl_sync(0xffffffffu, yv[2], src);
+        const int v3 = __shfl_sync(0xffffffffu, yv[3], src);
+        const int rnd = (4 * lane + i) >> 5;
+        y4[i] = rnd == 0 ? v0 : (rnd == 1 ? v1 : (rnd == 2 ? v2 : v3));
       }
       if (lane < TT / 4) {
         const uint32_t bar = sm.full(s, p);
@@ -519,8 +565,7 @@ struct Producer {
     int s;
     if (!acquire_stage(s)) return;
     if (lane == 0) {
-      StageHdr* hp = sm.hdr(s, p);
-      hp->kind = 1;
+      sm.hdr(s, p)->kind_flags = kEnd;
       mbar_arrive(sm.full(s, p));
     }
     __syncwarp();
@@ -530,12 +575,11 @@ struct Producer {
   // Emit the stages of one segment: chunks [k0, k1) of unit (b, g).
   __device__ void segment(int b, int g, const UnitRange& r, int k0, int k1, bool whole, int slot, const MergeDesc& md) {
     StageHdr h;
-    h.kind = 0;
     h.unit = b * p.Hkv + g;
     h.b = b;
     h.g = g;
     h.L = r.L;
-    h.mask_lo = h.mask_hi = 0u;
+    h.mask[0] = h.mask[1] = h.mask[2] = h.mask[3] = 0u;
     h.slot = slot;
     h.nseg = md.nseg;
     h.s0 = md.s0;
@@ -543,7 +587,7 @@ struct Producer {
     h.sstride = md.sstride;
     const int kend = (k1 > k0) ? k1 : k0 + 1;
     for (int k = k0; k < kend && ok; ++k) {
-      h.flags = (k == k0 ? kSegFirst : 0) | (k == kend - 1 ? kSegLast : 0) | (whole ? kSegWhole : 0);
+      h.kind_flags = (k == k0 ? kSegFirst : 0) | (k == kend - 1 ? kSegLast : 0) | (whole ? kSegWhole : 0);
       if (k1 > k0) {
         h.tbase = (r.c_lo + k) * p.TT;
         h.t0 = max(h.tbase, r.lo);
@@ -592,8 +636,17 @@ struct Producer {
           const long long Pu = excl + g * nb;
           const long long kin = x - Pu;
           const long long take = min(nb - kin, x1 - x);
-          const MergeDesc md = balanced_desc(Pu, nb, N, C);
-          const int slot = (int)(2 * c + ((c == sched_owner(Pu, N, C) && sched_start(c, N, C) < Pu) ? 1 : 0));
+          // Slots: a unit that one CTA covers alone owns slot 2*grid + unit; a
+          // split unit uses its CTAs' continuation slots (2c: the unit CTA c
+          // starts with, 2c + 1: the unit CTA c ends with).
+          MergeDesc md = balanced_desc(Pu, nb, N, C);
+          int slot;
+          if (md.nseg == 1) {
+            slot = 2 * p.C + b * p.Hkv + g;
+            md.s0 = md.sbase = slot;
+          } else {
+            slot = (int)(2 * c + ((c == sched_owner(Pu, N, C) && sched_start(c, N, C) < Pu) ? 1 : 0));
+          }
           if (r.n > 0)
             segment(b, g, r, (int)kin, (int)(kin + take), md.nseg == 1, slot, md);
           else
@@ -621,27 +674,39 @@ struct Producer {
 };
 
 // ================================================================ consumers
-template <bool FP8, int D, int NT, bool VTOK>
+// Per-stage header fields every consumer warp needs. The sparse validity
+// words are separate scalars (selected by comparison, never indexed with a
+// runtime value) so that the whole view stays in registers.
+struct StageView {
+  int flags, tbase, t0, t1, L, unit, b, g;
+  unsigned m0, m1, m2, m3;
+  __device__ __forceinline__ unsigned mask_word(int w) const {
+    return w == 0 ? m0 : (w == 1 ? m1 : (w == 2 ? m2 : m3));
+  }
+};
+
+template <bool FP8, int D, int NT, bool VTOK, int TW>
 struct Consumer {
   static constexpr int ELT = FP8 ? 1 : 2;
-  static constexpr int NCH = D * ELT / 128;
+  static constexpr int NCH = D * ELT / 128;  // 128-byte column blocks per token row
   static constexpr int KSTEPS = D / 16;
   static constexpr int MT = D / 16;
   static constexpr int KS_BLK = KSTEPS / NCH;
   static constexpr int MT_BLK = MT / NCH;
-  static constexpr bool QK_F16 = FP8;
-  static constexpr bool PV_F16 = FP8;
+  static constexpr bool PV_F16 = FP8;  // FP8 caches: FP16 P and V; BF16 caches: BF16 P
   static constexpr int RW = 8 * NT;
   static constexpr int DPB = 128 / ELT;  // head dims per 128-byte block
 
   const PaParams& p;
   Smem sm;
-  int lane, g4, t4, cw, wr, wt;
+  int lane, g4, t4, wr, wt;
+  uint32_t koff[NCH][2][2];  // [block][token g4 / g4+8][chunk half], tile-relative
+  uint32_t voff[NCH][4];     // [block][token 2t4, 2t4+1, 2t4+8, 2t4+9]
   float kscale = 1.f, vscale = 1.f;
   // per segment
   uint32_t qf[NT][KSTEPS][2];
   float crow[NT][2];
-  int prow[NT][2];  // query position p_r of the thread's two rows per n-tile (dense masks)
+  int prow[NT][2];  // query position of the thread's two rows per n-tile
   float mrun[NT][2], lrun[NT][2];
   float o[MT][NT][4];
   // Per-token V scales: O is kept in units of 2^vexp so that P * v_scale / 2^vexp
@@ -652,16 +717,32 @@ struct Consumer {
     lane = threadIdx.x & 31;
     g4 = lane >> 2;
     t4 = lane & 3;
-    cw = threadIdx.x >> 5;
+    const int cw = threadIdx.x >> 5;
     wr = cw % p.Wr;
     wt = cw / p.Wr;
     if (FP8 && p.scale_mode == kScalePerTensor) kscale = __ldg(p.k_scale);
     vscale = per_tensor_vscale(p);
+    // Swizzled shared-memory offsets: row r's 16-byte chunk c sits at chunk
+    // c ^ (r & 7) (128-byte swizzle; sparse stages are unswizzled).
+#pragma unroll
+    for (int cb = 0; cb < NCH; ++cb) {
+#pragma unroll
+      for (int ab = 0; ab < 2; ++ab) {
+        const int row = g4 + 8 * ab;
+#pragma unroll
+        for (int hl = 0; hl < 2; ++hl)
+          koff[cb][ab][hl] = (uint32_t)(cb * p.TT + row) * 128u + (uint32_t)(((2 * t4 + hl) ^ (row & p.swz)) << 4);
+      }
+      const int vr[4] = {2 * t4, 2 * t4 + 1, 2 * t4 + 8, 2 * t4 + 9};
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        voff[cb][k] = (uint32_t)(cb * p.TT + vr[k]) * 128u + (uint32_t)((g4 ^ (vr[k] & p.swz)) << 4);
+    }
   }
 
   __device__ __forceinline__ int row_of(int j, int rho) const { return wr * RW + 8 * j + 2 * t4 + rho; }
 
-  __device__ void begin_segment(const StageHdr& h) {
+  __device__ void begin_segment(int b, int g, int L) {
     // Q rows of this warp's slice as MMA B fragments (row n = g4), with the
     // head-dim permutation that matches how K rows are read from shared memory.
 #pragma unroll
@@ -669,8 +750,8 @@ struct Consumer {
       const int r = wr * RW + 8 * j + g4;
       const bool valid = r < p.R;
       const int i = valid ? r / p.G : 0;
-      const int head = h.g * p.G + (valid ? r % p.G : 0);
-      const uint16_t* qrow = p.q + ((size_t)(h.b * p.QL + i) * p.Hq + head) * D;
+      const int head = g * p.G + (valid ? r % p.G : 0);
+      const uint16_t* qrow = p.q + ((size_t)(b * p.QL + i) * p.Hq + head) * D;
       float crow_n = 0.f;
       if constexpr (FP8) {
         // 32 values per block: d in [cb*128 + 32*t4, +32)
@@ -708,7 +789,7 @@ struct Consumer {
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             const uint32_t w[4] = {raw[cb][v].x, raw[cb][v].y, raw[cb][v].z, raw[cb][v].w};
-            // words w[0..3] hold d = 32*t4 + 8v + {0..7}; k-step s_local = 2v + (e>>1)
+            // words w[0..3] hold d = 32*t4 + 8v + {0..7}; k-step 2v + hw takes 4 of them
 #pragma unroll
             for (int hw = 0; hw < 2; ++hw) {
               const int s = cb * KS_BLK + 2 * v + hw;
@@ -737,7 +818,7 @@ struct Consumer {
       for (int rho = 0; rho < 2; ++rho) {
         crow[j][rho] = __shfl_sync(0xffffffffu, crow_n, (2 * t4 + rho) * 4);
         const int rr = row_of(j, rho);
-        prow[j][rho] = (rr < p.R) ? (h.L - p.QL + rr / p.G) : -(1 << 30);
+        prow[j][rho] = (rr < p.R) ? (L - p.QL + rr / p.G) : -(1 << 30);
         mrun[j][rho] = -INFINITY;
         lrun[j][rho] = 0.f;
       }
@@ -751,90 +832,117 @@ struct Consumer {
     vexp = -127;
   }
 
-  // Does stage row `row` (absolute token t) carry real data for every row?
-  __device__ __forceinline__ bool token_ok(const StageHdr& h, int row) const {
-    if (p.topk > 0) return ((row < 32 ? h.mask_lo >> row : h.mask_hi >> (row - 32)) & 1u) != 0u;
+  // Does stage row `row` carry a real token (one that some query row may see)?
+  __device__ __forceinline__ bool token_ok(const StageView& h, int row) const {
+    if (p.topk > 0) return ((h.mask_word(row >> 5) >> (row & 31)) & 1u) != 0u;
     const int t = h.tbase + row;
     return t >= h.t0 && t < h.t1;
   }
-  __device__ __forceinline__ bool score_ok(const StageHdr& h, int row, int j, int rho) const {
+  __device__ __forceinline__ bool score_ok(const StageView& h, int row, int j, int rho) const {
     if (!token_ok(h, row)) return false;
-    if (p.topk > 0) return prow[j][rho] > -(1 << 29);
-    const int t = h.tbase + row;
     const int pr = prow[j][rho];
+    if (p.topk > 0) return pr > -(1 << 29);
+    const int t = h.tbase + row;
     bool ok = pr > -(1 << 29);
     if (p.causal) ok = ok && t <= pr;
     if (p.window > 0) ok = ok && t > pr - p.window;
     return ok;
   }
 
-  __device__ void tile(const StageHdr& h, uint32_t kst, uint32_t vst, uint32_t sst, int tau) {
-    const int TT = p.TT;
-    const int swz = p.swz;
-    const int rowA = 16 * tau + g4, rowB = rowA + 8;
-    bool interior;
-    if (p.topk > 0) {
-      const unsigned m16 = (tau < 2 ? (h.mask_lo >> (16 * tau)) : (h.mask_hi >> (16 * (tau - 2)))) & 0xFFFFu;
-      if (m16 == 0u) return;
-      interior = (m16 == 0xFFFFu);
-    } else {
-      const int ta = h.tbase + 16 * tau;
-      if (ta >= h.t1 || ta + 16 <= h.t0) return;
-      const int lo_all = p.window > 0 ? max(0, h.L - p.window) : 0;
-      const int hi_all = p.causal ? h.L - p.QL + 1 : h.L;
-      interior = ta >= max(h.t0, lo_all) && ta + 16 <= min(h.t1, hi_all);
+  // One warp step: TW consecutive 16-token tiles starting at tile tau0.
+  __device__ void step(const StageView& h, uint32_t kst, uint32_t vst, uint32_t sst, int tau0) {
+    bool interior[TW];
+    bool any = false;
+#pragma unroll
+    for (int u = 0; u < TW; ++u) {
+      const int tau = tau0 + u;
+      bool live;
+      if (p.topk > 0) {
+        const unsigned m16 = (h.mask_word(tau >> 1) >> (16 * (tau & 1))) & 0xFFFFu;
+        live = m16 != 0u;
+        interior[u] = m16 == 0xFFFFu;
+      } else {
+        const int ta = h.tbase + 16 * tau;
+        live = !(ta >= h.t1 || ta + 16 <= h.t0);
+        const int lo_all = p.window > 0 ? max(0, h.L - p.window) : 0;
+        const int hi_all = p.causal ? h.L - p.QL + 1 : h.L;
+        interior[u] = ta >= max(h.t0, lo_all) && ta + 16 <= min(h.t1, hi_all);
+      }
+      any |= live;
     }
-    // ---- S^T = K Q^T ------------------------------------------------------
-    float sacc[NT][4];
+    if (!any) return;
+    // ---- S^T = K Q^T for each tile ------------------------------------------
+    float sacc[TW][NT][4];
 #pragma unroll
-    for (int j = 0; j < NT; ++j)
+    for (int u = 0; u < TW; ++u)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) sacc[j][e] = 0.f;
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[u][j][e] = 0.f;
 #pragma unroll
     for (int cb = 0; cb < NCH; ++cb) {
 #pragma unroll
       for (int hl = 0; hl < 2; ++hl) {
-        const int ch = 2 * t4 + hl;
-        const uint4 ka = lds128(kst + (uint32_t)(cb * TT + rowA) * 128u + (uint32_t)((ch ^ (rowA & swz)) << 4));
-        const uint4 kb = lds128(kst + (uint32_t)(cb * TT + rowB) * 128u + (uint32_t)((ch ^ (rowB & swz)) << 4));
-        const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w};
-        const uint32_t wb[4] = {kb.x, kb.y, kb.z, kb.w};
-        if constexpr (FP8) {
+        uint4 ka[TW], kb[TW];
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const int s = cb * KS_BLK + hl * 4 + w;
-            const uint32_t a0 = e4m3x2_to_f16x2(wa[w]), a2 = e4m3x2_to_f16x2(wa[w] >> 16);
-            const uint32_t a1 = e4m3x2_to_f16x2(wb[w]), a3 = e4m3x2_to_f16x2(wb[w] >> 16);
+        for (int u = 0; u < TW; ++u) {
+          const uint32_t tb = kst + (uint32_t)(tau0 + u) * 2048u;
+          ka[u] = lds128(tb + koff[cb][0][hl]);
+          kb[u] = lds128(tb + koff[cb][1][hl]);
+        }
 #pragma unroll
-            for (int j = 0; j < NT; ++j) mma16816<true>(sacc[j], a0, a1, a2, a3, qf[j][s][0], qf[j][s][1]);
-          }
-        } else {
+        for (int u = 0; u < TW; ++u) {
+          const uint32_t wa[4] = {ka[u].x, ka[u].y, ka[u].z, ka[u].w};
+          const uint32_t wb[4] = {kb[u].x, kb[u].y, kb[u].z, kb[u].w};
+          if constexpr (FP8) {
 #pragma unroll
-          for (int w2 = 0; w2 < 2; ++w2) {
-            const int s = cb * KS_BLK + hl * 2 + w2;
+            for (int w = 0; w < 4; ++w) {
+              const int s = cb * KS_BLK + hl * 4 + w;
+              const uint32_t a0 = e4m3x2_to_f16x2(wa[w]), a2 = e4m3x2_to_f16x2(wa[w] >> 16);
+              const uint32_t a1 = e4m3x2_to_f16x2(wb[w]), a3 = e4m3x2_to_f16x2(wb[w] >> 16);
 #pragma unroll
-            for (int j = 0; j < NT; ++j)
-              mma16816<false>(sacc[j], wa[2 * w2], wb[2 * w2], wa[2 * w2 + 1], wb[2 * w2 + 1], qf[j][s][0], qf[j][s][1]);
+              for (int j = 0; j < NT; ++j) mma16816<true>(sacc[u][j], a0, a1, a2, a3, qf[j][s][0], qf[j][s][1]);
+            }
+          } else {
+#pragma unroll
+            for (int w2 = 0; w2 < 2; ++w2) {
+              const int s = cb * KS_BLK + hl * 2 + w2;
+#pragma unroll
+              for (int j = 0; j < NT; ++j)
+                mma16816<false>(sacc[u][j], wa[2 * w2], wb[2 * w2], wa[2 * w2 + 1], wb[2 * w2 + 1], qf[j][s][0],
+                                qf[j][s][1]);
+            }
           }
         }
       }
     }
-    // ---- scale (before masking), mask, online softmax -------------------------
+    // ---- scale (before masking), mask, online softmax over the TW tiles -----
     const bool ktok = FP8 && p.scale_mode == kScalePerToken;
-    float ksA = 1.f, ksB = 1.f, vsA = 1.f, vsB = 1.f;
-    if (ktok) {
-      ksA = lds_f32(sst + rowA * 4);
-      ksB = lds_f32(sst + rowB * 4);
+    float ks[TW][2], vs[TW][2];
+#pragma unroll
+    for (int u = 0; u < TW; ++u) {
+      const int rA = 16 * (tau0 + u) + g4;
+      ks[u][0] = ks[u][1] = vs[u][0] = vs[u][1] = 1.f;
+      if (ktok) {
+        ks[u][0] = lds_f32(sst + rA * 4);
+        ks[u][1] = lds_f32(sst + (rA + 8) * 4);
+      }
+      if constexpr (VTOK) {
+        vs[u][0] = lds_f32(sst + p.TT * 4 + rA * 4);
+        vs[u][1] = lds_f32(sst + p.TT * 4 + (rA + 8) * 4);
+      }
     }
-    uint32_t pb[NT][2];
-    float alpha[NT][2];
     bool rescale = false;
     float vfix = 1.f;
     if constexpr (VTOK) {
-      vsA = lds_f32(sst + TT * 4 + rowA * 4);
-      vsB = lds_f32(sst + TT * 4 + rowB * 4);
-      // the tile's largest valid V scale sets the power-of-two unit of O
-      float vm = fmaxf((interior || token_ok(h, rowA)) ? vsA : 0.f, (interior || token_ok(h, rowB)) ? vsB : 0.f);
+      // the step's largest valid V scale sets the power-of-two unit of O
+      float vm = 0.f;
+#pragma unroll
+      for (int u = 0; u < TW; ++u) {
+        const int rA = 16 * (tau0 + u) + g4;
+        vm = fmaxf(vm, (interior[u] || token_ok(h, rA)) ? vs[u][0] : 0.f);
+        vm = fmaxf(vm, (interior[u] || token_ok(h, rA + 8)) ? vs[u][1] : 0.f);
+      }
       vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 4));
       vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 8));
       vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 16));
@@ -847,60 +955,77 @@ struct Consumer {
         }
       }
       const float inv = __uint_as_float((uint32_t)(127 - max(vexp, -126)) << 23);
-      vsA *= inv;
-      vsB *= inv;
+#pragma unroll
+      for (int u = 0; u < TW; ++u) {
+        vs[u][0] *= inv;
+        vs[u][1] *= inv;
+      }
     }
+    uint32_t pb[TW][NT][2];
+    float alpha[NT][2];
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      float x[4];
+      float x[TW][4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int rho = e & 1;
-        x[e] = sacc[j][e] * crow[j][rho] * (e < 2 ? ksA : ksB);
-      }
-      if (!interior) {
+      for (int u = 0; u < TW; ++u) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (!score_ok(h, e < 2 ? rowA : rowB, j, e & 1)) x[e] = -INFINITY;
+        for (int e = 0; e < 4; ++e) x[u][e] = sacc[u][j][e] * crow[j][e & 1] * ks[u][e >> 1];
+        if (!interior[u]) {
+          const int rA = 16 * (tau0 + u) + g4;
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (!score_ok(h, e < 2 ? rA : rA + 8, j, e & 1)) x[u][e] = -INFINITY;
+        }
       }
-      float pe[4];
+      float pe[TW][4];
 #pragma unroll
       for (int rho = 0; rho < 2; ++rho) {
-        float mx = fmaxf(x[rho], x[rho + 2]);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < TW; ++u) mx = fmaxf(mx, fmaxf(x[u][rho], x[u][rho + 2]));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
         const float mnew = fmaxf(mrun[j][rho], mx);
         const float muse = (mnew == -INFINITY) ? 0.f : mnew;
         const float a = ex2(mrun[j][rho] - muse);
-        pe[rho] = ex2(x[rho] - muse);
-        pe[rho + 2] = ex2(x[rho + 2] - muse);
-        lrun[j][rho] = lrun[j][rho] * a + (pe[rho] + pe[rho + 2]);
+        float sum = 0.f;
+#pragma unroll
+        for (int u = 0; u < TW; ++u) {
+          pe[u][rho] = ex2(x[u][rho] - muse);
+          pe[u][rho + 2] = ex2(x[u][rho + 2] - muse);
+          sum += pe[u][rho] + pe[u][rho + 2];
+        }
+        lrun[j][rho] = lrun[j][rho] * a + sum;
         mrun[j][rho] = mnew;
         alpha[j][rho] = a * vfix;
         rescale |= (a != 1.f);
       }
-      if constexpr (VTOK) {
-        // per-token V scale folded into P before rounding (masked tokens: 0)
-        pe[0] *= vsA;
-        pe[1] *= vsA;
-        pe[2] *= vsB;
-        pe[3] *= vsB;
-        if (!interior) {
-          if (!token_ok(h, rowA)) pe[0] = pe[1] = 0.f;
-          if (!token_ok(h, rowB)) pe[2] = pe[3] = 0.f;
+#pragma unroll
+      for (int u = 0; u < TW; ++u) {
+        if constexpr (VTOK) {
+          // per-token V scale folded into P before rounding (masked tokens: 0)
+          pe[u][0] *= vs[u][0];
+          pe[u][1] *= vs[u][0];
+          pe[u][2] *= vs[u][1];
+          pe[u][3] *= vs[u][1];
+          if (!interior[u]) {
+            const int rA = 16 * (tau0 + u) + g4;
+            if (!token_ok(h, rA)) pe[u][0] = pe[u][1] = 0.f;
+            if (!token_ok(h, rA + 8)) pe[u][2] = pe[u][3] = 0.f;
+          }
         }
+        uint32_t x0, x1;
+        if constexpr (PV_F16) {
+          x0 = pack_f16(pe[u][0], pe[u][1]);
+          x1 = pack_f16(pe[u][2], pe[u][3]);
+        } else {
+          x0 = pack_bf16(pe[u][0], pe[u][1]);
+          x1 = pack_bf16(pe[u][2], pe[u][3]);
+        }
+        pb[u][j][0] = movm_trans(x0);
+        pb[u][j][1] = movm_trans(x1);
       }
-      uint32_t x0, x1;
-      if constexpr (PV_F16) {
-        x0 = pack_f16(pe[0], pe[1]);
-        x1 = pack_f16(pe[2], pe[3]);
-      } else {
-        x0 = pack_bf16(pe[0], pe[1]);
-        x1 = pack_bf16(pe[2], pe[3]);
-      }
-      pb[j][0] = movm_trans(x0);
-      pb[j][1] = movm_trans(x1);
     }
     if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
@@ -914,59 +1039,61 @@ struct Consumer {
         }
     }
     // ---- O^T += V^T P^T ---------------------------------------------------------
-    const int vr0 = 16 * tau + 2 * t4;
-    const int vrow[4] = {vr0, vr0 + 1, vr0 + 8, vr0 + 9};
-    bool vok[4] = {true, true, true, true};
-    if (!interior) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) vok[k] = token_ok(h, vrow[k]);
-    }
+    for (int u = 0; u < TW; ++u) {
 #pragma unroll
-    for (int cb = 0; cb < NCH; ++cb) {
-      uint4 vv[4];
+      for (int cb = 0; cb < NCH; ++cb) {
+        uint4 vv[4];
+        const uint32_t tb = vst + (uint32_t)(tau0 + u) * 2048u;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        vv[k] = lds128(vst + (uint32_t)(cb * TT + vrow[k]) * 128u + (uint32_t)((g4 ^ (vrow[k] & swz)) << 4));
-        if (!vok[k]) vv[k] = make_uint4(0, 0, 0, 0);
-      }
-      const uint32_t va[4] = {vv[0].x, vv[0].y, vv[0].z, vv[0].w};
-      const uint32_t vb[4] = {vv[1].x, vv[1].y, vv[1].z, vv[1].w};
-      const uint32_t vc[4] = {vv[2].x, vv[2].y, vv[2].z, vv[2].w};
-      const uint32_t vd[4] = {vv[3].x, vv[3].y, vv[3].z, vv[3].w};
-      if constexpr (FP8) {
+        for (int k = 0; k < 4; ++k) vv[k] = lds128(tb + voff[cb][k]);
+        if (!interior[u]) {
+          const int vr0 = 16 * (tau0 + u) + 2 * t4;
+          const int vrow[4] = {vr0, vr0 + 1, vr0 + 8, vr0 + 9};
 #pragma unroll
-        for (int mt = 0; mt < MT_BLK; ++mt) {
-          const int wi = mt >> 1;
-          const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-          const uint32_t x01 = __byte_perm(va[wi], vb[wi], sel);
-          const uint32_t x23 = __byte_perm(vc[wi], vd[wi], sel);
-          const uint32_t r0 = e4m3x2_to_f16x2(x01), r1 = e4m3x2_to_f16x2(x01 >> 16);
-          const uint32_t r2 = e4m3x2_to_f16x2(x23), r3 = e4m3x2_to_f16x2(x23 >> 16);
-#pragma unroll
-          for (int j = 0; j < NT; ++j) mma16816<PV_F16>(o[cb * MT_BLK + mt][j], r0, r1, r2, r3, pb[j][0], pb[j][1]);
+          for (int k = 0; k < 4; ++k)
+            if (!token_ok(h, vrow[k])) vv[k] = make_uint4(0, 0, 0, 0);
         }
-      } else {
+        const uint32_t va[4] = {vv[0].x, vv[0].y, vv[0].z, vv[0].w};
+        const uint32_t vb[4] = {vv[1].x, vv[1].y, vv[1].z, vv[1].w};
+        const uint32_t vc[4] = {vv[2].x, vv[2].y, vv[2].z, vv[2].w};
+        const uint32_t vd[4] = {vv[3].x, vv[3].y, vv[3].z, vv[3].w};
+        if constexpr (FP8) {
 #pragma unroll
-        for (int mt = 0; mt < MT_BLK; ++mt) {
-          const uint32_t r0 = __byte_perm(va[mt], vb[mt], 0x5410u);
-          const uint32_t r1 = __byte_perm(va[mt], vb[mt], 0x7632u);
-          const uint32_t r2 = __byte_perm(vc[mt], vd[mt], 0x5410u);
-          const uint32_t r3 = __byte_perm(vc[mt], vd[mt], 0x7632u);
+          for (int mt = 0; mt < MT_BLK; ++mt) {
+            const int wi = mt >> 1;
+            const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+            const uint32_t x01 = __byte_perm(va[wi], vb[wi], sel);
+            const uint32_t x23 = __byte_perm(vc[wi], vd[wi], sel);
+            const uint32_t r0 = e4m3x2_to_f16x2(x01), r1 = e4m3x2_to_f16x2(x01 >> 16);
+            const uint32_t r2 = e4m3x2_to_f16x2(x23), r3 = e4m3x2_to_f16x2(x23 >> 16);
 #pragma unroll
-          for (int j = 0; j < NT; ++j) mma16816<false>(o[cb * MT_BLK + mt][j], r0, r1, r2, r3, pb[j][0], pb[j][1]);
+            for (int j = 0; j < NT; ++j) mma16816<true>(o[cb * MT_BLK + mt][j], r0, r1, r2, r3, pb[u][j][0], pb[u][j][1]);
+          }
+        } else {
+#pragma unroll
+          for (int mt = 0; mt < MT_BLK; ++mt) {
+            const uint32_t r0 = __byte_perm(va[mt], vb[mt], 0x5410u);
+            const uint32_t r1 = __byte_perm(va[mt], vb[mt], 0x7632u);
+            const uint32_t r2 = __byte_perm(vc[mt], vd[mt], 0x5410u);
+            const uint32_t r3 = __byte_perm(vc[mt], vd[mt], 0x7632u);
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+              mma16816<false>(o[cb * MT_BLK + mt][j], r0, r1, r2, r3, pb[u][j][0], pb[u][j][1]);
+          }
         }
       }
     }
   }
 
-  __device__ void end_segment(const StageHdr& h) {
-    const int nthr = p.NCW * 32;
-    const int tid = threadIdx.x;
-    float* mb_o = reinterpret_cast<float*>(sm.base + p.off_merge);
-    float* mb_ml = mb_o + (size_t)p.Wt * p.Rpad * D;
-    // O in true units (per-token V scales: undo the power-of-two unit)
+  // ---------------------------------------------------------------- epilogue
+  // Segment end for this warp: either the output rows directly (a whole unit
+  // seen by one token group), or a per-warp partial that the last arriver,
+  // the cluster or the reducer merges.
+  __device__ void end_segment(const StageView& h, int slot, const MergeDesc& md) {
+    const bool whole = (h.flags & kSegWhole) != 0;
     const float ounit = VTOK ? __uint_as_float((uint32_t)(max(vexp, -126) + 127) << 23) : 1.f;
-    // 1. per-warp row sums across the 8 token lanes, publish to shared memory
+    float lsum[NT][2];
 #pragma unroll
     for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -975,11 +1102,19 @@ struct Consumer {
         l += __shfl_xor_sync(0xffffffffu, l, 4);
         l += __shfl_xor_sync(0xffffffffu, l, 8);
         l += __shfl_xor_sync(0xffffffffu, l, 16);
+        lsum[j][rho] = l;
+      }
+    const bool direct = whole && p.Wt == 1;
+    const bool cluster = p.merge == kMergeCluster;
+    const size_t pi = (size_t)slot * p.Wt + wt;
+    float* cp_o = reinterpret_cast<float*>(sm.base + p.off_cpart);
+    float* cp_ml = cp_o + (size_t)p.Wt * p.Rpad * D;
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int rho = 0; rho < 2; ++rho) {
         const int r = row_of(j, rho);
-        if (g4 == 0) {
-          mb_ml[((size_t)wt * p.Rpad + r) * 2 + 0] = mrun[j][rho];
-          mb_ml[((size_t)wt * p.Rpad + r) * 2 + 1] = l;
-        }
+        if (r >= p.R) continue;
 #pragma unroll
         for (int cb = 0; cb < NCH; ++cb) {
           // this thread holds d = cb*DPB + (DPB/8)*g4 + {0 .. DPB/8 - 1} of row r
@@ -989,80 +1124,94 @@ struct Consumer {
             v[2 * mt] = o[cb * MT_BLK + mt][j][rho] * ounit;
             v[2 * mt + 1] = o[cb * MT_BLK + mt][j][rho + 2] * ounit;
           }
-          float4* dst = reinterpret_cast<float4*>(mb_o + ((size_t)wt * p.Rpad + r) * D + cb * DPB + (DPB / 8) * g4);
+          const int d0 = cb * DPB + (DPB / 8) * g4;
 #pragma unroll
-          for (int q4 = 0; q4 < DPB / 32; ++q4) dst[q4] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+          for (int q4 = 0; q4 < DPB / 32; ++q4) {
+            const float4 f = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+            if (direct)
+              finalize_store<D>(p, vscale, f, mrun[j][rho], lsum[j][rho], h.b, h.g, r, d0 + 4 * q4);
+            else if (cluster)
+              *reinterpret_cast<float4*>(cp_o + ((size_t)wt * p.Rpad + r) * D + d0 + 4 * q4) = f;
+            else
+              *reinterpret_cast<float4*>(p.part_o + (pi * p.Rpad + r) * D + d0 + 4 * q4) = f;
+          }
+        }
+        if (g4 == 0 && !direct) {
+          const float2 ml = make_float2(mrun[j][rho], lsum[j][rho]);
+          if (cluster)
+            *reinterpret_cast<float2*>(cp_ml + ((size_t)wt * p.Rpad + r) * 2) = ml;
+          else
+            *reinterpret_cast<float2*>(p.part_ml + (pi * p.Rpad + r) * 2) = ml;
         }
       }
+    if (direct || cluster) return;
+    __threadfence();
+    __syncwarp();
+    const int npart = md.nseg * p.Wt;
+    if (p.merge == kMergeReducer) {
+      if (lane == 0 && wt == 0 && wr == 0 && slot == md.s0)
+        p.unit_desc[h.unit] = make_int4(md.nseg, md.s0, md.sbase, md.sstride);
+      return;
+    }
+    // last arriver among the unit's partials of this row slice merges the slice
+    int last = 0;
+    if (lane == 0) {
+      int* cnt = p.counters + ((size_t)h.unit * p.Wr + wr) * kCounterStride;
+      const int prev = atomicAdd(cnt, 1);
+      last = (prev == npart - 1);
+      if (last) atomicExch(cnt, 0);
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return;
+    // Queue the merge of this row slice; the CTA's consumer warps run the
+    // queue together once the stream is done (a merge here would hold up the
+    // shared stage ring). A full queue merges on the spot with this warp.
+    int idx = 0;
+    if (lane == 0) idx = atomicAdd(reinterpret_cast<int*>(sm.base + p.off_misc) + 2, 1);
+    idx = __shfl_sync(0xffffffffu, idx, 0);
+    if (idx < kPendingMax) {
+      if (lane == 0) {
+        int4* q = reinterpret_cast<int4*>(sm.base + p.off_pend) + 2 * idx;
+        q[0] = make_int4(h.b, h.g, wr, md.nseg);
+        q[1] = make_int4(md.s0, md.sbase, md.sstride, 0);
+      }
+      return;
+    }
+    __threadfence();
+    merge_slice(h.b, h.g, wr, md, lane, 32);
+  }
+
+  // Merge one row slice of a unit from its global partials.
+  __device__ void merge_slice(int b, int g, int slice, const MergeDesc& md, int tid, int nthr) const {
+    const int e0 = slice * RW * (D / 4);
+    const int e1 = min(p.R, (slice + 1) * RW) * (D / 4);
+    merge_elems<D>(
+        p, vscale, md.nseg * p.Wt, b, g, tid, nthr, e0, e1,
+        [&](int q, int r) {
+          return __ldcg(reinterpret_cast<const float2*>(p.part_ml + (partial_index(md, p.Wt, q) * p.Rpad + r) * 2));
+        },
+        [&](int q, int r, int d) {
+          return __ldcg(reinterpret_cast<const float4*>(p.part_o + (partial_index(md, p.Wt, q) * p.Rpad + r) * D + d));
+        });
+  }
+
+  // After the stream: all consumer warps run the queued merges together.
+  __device__ void run_pending() {
+    const int nthr = p.NCW * 32;
     named_bar(1, nthr);
-    // 2. merge the token groups; write output, a global partial, or the cluster partial
-    const bool whole = (h.flags & kSegWhole) != 0;
-    const bool cluster = p.merge == kMergeCluster;
-    float* cp_o = reinterpret_cast<float*>(sm.base + p.off_cpart);
-    float* cp_ml = cp_o + (size_t)p.Rpad * D;
-    const int E = p.R * (D / 4);
-    for (int e = tid; e < E; e += nthr) {
-      const int r = e / (D / 4);
-      const int d = (e % (D / 4)) * 4;
-      float M = -INFINITY;
-      for (int w = 0; w < p.Wt; ++w) M = fmaxf(M, mb_ml[((size_t)w * p.Rpad + r) * 2]);
-      float L = 0.f;
-      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int w = 0; w < p.Wt; ++w) {
-        const float mw = mb_ml[((size_t)w * p.Rpad + r) * 2];
-        if (mw == -INFINITY) continue;
-        const float a = ex2(mw - M);
-        const float4 ow = *reinterpret_cast<const float4*>(mb_o + ((size_t)w * p.Rpad + r) * D + d);
-        L = fmaf(mb_ml[((size_t)w * p.Rpad + r) * 2 + 1], a, L);
-        O.x = fmaf(ow.x, a, O.x);
-        O.y = fmaf(ow.y, a, O.y);
-        O.z = fmaf(ow.z, a, O.z);
-        O.w = fmaf(ow.w, a, O.w);
-      }
-      if (whole) {
-        finalize_store<D>(p, vscale, O, M, L, h.b, h.g, r, d);
-      } else if (cluster) {
-        *reinterpret_cast<float4*>(cp_o + (size_t)r * D + d) = O;
-        if (d == 0) *reinterpret_cast<float2*>(cp_ml + 2 * r) = make_float2(M, L);
-      } else {
-        *reinterpret_cast<float4*>(p.part_o + ((size_t)h.slot * p.Rpad + r) * D + d) = O;
-        if (d == 0) *reinterpret_cast<float2*>(p.part_ml + ((size_t)h.slot * p.Rpad + r) * 2) = make_float2(M, L);
-      }
+    const int cnt = min(*(reinterpret_cast<volatile int*>(sm.base + p.off_misc) + 2), kPendingMax);
+    if (cnt == 0) return;
+    __threadfence();
+    for (int i = 0; i < cnt; ++i) {
+      const int4* q = reinterpret_cast<const int4*>(sm.base + p.off_pend) + 2 * i;
+      const int4 a = q[0], c = q[1];
+      merge_slice(a.x, a.y, a.z, MergeDesc{a.w, c.x, c.y, c.z}, threadIdx.x, nthr);
     }
-    if (!whole && !cluster) {
-      __threadfence();
-      named_bar(1, nthr);
-      if (p.merge == kMergeReducer) {
-        if (tid == 0 && h.slot == h.s0) p.unit_desc[h.unit] = make_int4(h.nseg, h.s0, h.sbase, h.sstride);
-      } else if (p.merge == kMergeLastArriver) {
-        volatile int* misc = sm.misc(p);
-        if (tid == 0) {
-          const int prev = atomicAdd(p.counters + (size_t)h.unit * kCounterStride, 1);
-          const int last = (prev == h.nseg - 1);
-          if (last) atomicExch(p.counters + (size_t)h.unit * kCounterStride, 0);
-          misc[1] = last;
-        }
-        named_bar(1, nthr);
-        if (misc[1]) {
-          __threadfence();
-          const MergeDesc md{h.nseg, h.s0, h.sbase, h.sstride};
-          merge_elems<D>(
-              p, vscale, h.nseg, h.b, h.g, tid, nthr, 0, E,
-              [&](int k, int r) {
-                return __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((size_t)merge_slot(md, k) * p.Rpad + r) * 2));
-              },
-              [&](int k, int r, int d) {
-                return __ldcg(reinterpret_cast<const float4*>(p.part_o + ((size_t)merge_slot(md, k) * p.Rpad + r) * D + d));
-              });
-        }
-      }
-    }
-    named_bar(1, nthr);  // the merge buffer is reused by the next segment
   }
 
   __device__ void run() {
     int n = 0;
-    StageHdr h;
+    StageView h;
     while (true) {
       const int s = n % p.NS;
       bool got = mbar_wait(sm.full(s, p), (n / p.NS) & 1);
@@ -1074,44 +1223,72 @@ struct Consumer {
         }
         break;
       }
-      h = *sm.hdr(s, p);
-      if (h.kind != 0) break;
-      if (h.flags & kSegFirst) begin_segment(h);
+      const uint32_t ha = sm.hdr_u32(s, p);
+      const int4 h0 = lds128i(ha);
+      if (h0.x & kEnd) break;
+      const int4 h1 = lds128i(ha + 16);
+      h.flags = h0.x;
+      h.tbase = h0.y;
+      h.t0 = h0.z;
+      h.t1 = h0.w;
+      h.L = h1.x;
+      h.unit = h1.y;
+      h.b = h1.z;
+      h.g = h1.w;
+      h.m0 = h.m1 = h.m2 = h.m3 = 0u;
+      if (p.topk > 0) {
+        const int4 h2 = lds128i(ha + 32);
+        h.m0 = (unsigned)h2.x;
+        h.m1 = (unsigned)h2.y;
+        h.m2 = (unsigned)h2.z;
+        h.m3 = (unsigned)h2.w;
+      }
+      int slot = 0;
+      MergeDesc md{1, 0, 0, 0};
+      if (h.flags & kSegLast) {
+        const int4 h3 = lds128i(ha + 48);
+        const int sstride = lds128i(ha + 64).x;
+        slot = h3.x;
+        md = MergeDesc{h3.y, h3.z, h3.w, sstride};
+      }
+      if (h.flags & kSegFirst) begin_segment(h.b, h.g, h.L);
       const uint32_t kst = sm.stage(s, p);
       const uint32_t vst = kst + (uint32_t)p.TT * 128u * NCH;
       const uint32_t sst = kst + p.off_scale;
-      for (int tau = wt; tau < p.TT / 16; tau += p.Wt) tile(h, kst, vst, sst, tau);
+      const int steps = p.TT / (16 * TW);
+      for (int j = wt; j < steps; j += p.Wt) step(h, kst, vst, sst, j * TW);
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.empty(s, p));
-      if (h.flags & kSegLast) end_segment(h);
+      if (h.flags & kSegLast) end_segment(h, slot, md);
       ++n;
     }
   }
 
-  // Cluster merge: CTA `rank` of the cluster merges its share of the rows of
-  // all partitions' partials, read over distributed shared memory.
-  __device__ void cluster_merge(int unit) {
+  // Cluster merge: CTA `rank` merges its share of the unit's output elements
+  // from the per-warp partials of all P CTAs, read over distributed shared memory.
+  __device__ void cluster_merge(int unit, int tid, int nthr) {
     const int b = unit / p.Hkv, g = unit % p.Hkv;
     uint32_t rank;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
     const int E = p.R * (D / 4);
     const int e0 = (int)((long long)rank * E / p.P), e1 = (int)((long long)(rank + 1) * E / p.P);
     const uint32_t cp_local = sm.base_u32 + p.off_cpart;
-    const uint32_t ml_off = (uint32_t)p.Rpad * D * 4u;
+    const uint32_t ml_off = (uint32_t)p.Wt * p.Rpad * D * 4u;
+    const int Wt = p.Wt;
     merge_elems<D>(
-        p, vscale, p.P, b, g, threadIdx.x, p.NCW * 32, e0, e1,
-        [&](int k, int r) {
+        p, vscale, p.P * Wt, b, g, tid, nthr, e0, e1,
+        [&](int q, int r) {
           uint32_t remote;
-          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(cp_local + ml_off + 8u * r), "r"(k));
+          const uint32_t local = cp_local + ml_off + 8u * (uint32_t)((q % Wt) * p.Rpad + r);
+          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(q / Wt));
           float2 v;
           asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(remote));
           return v;
         },
-        [&](int k, int r, int d) {
+        [&](int q, int r, int d) {
           uint32_t remote;
-          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-                       : "=r"(remote)
-                       : "r"(cp_local + (uint32_t)(r * D + d) * 4u), "r"(k));
+          const uint32_t local = cp_local + 4u * (uint32_t)(((q % Wt) * p.Rpad + r) * D + d);
+          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(q / Wt));
           float4 v;
           asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
                        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
@@ -1126,10 +1303,10 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-template <bool FP8, int D, int NT, bool VTOK>
-__global__ void __launch_bounds__(D == 256 ? 288 : 160) pa_tile_kernel(const __grid_constant__ PaParams p,
-                                                      const __grid_constant__ CUtensorMap tmK,
-                                                      const __grid_constant__ CUtensorMap tmV) {
+template <bool FP8, int D, int NT, bool VTOK, int TW>
+__global__ void __launch_bounds__(160, (D == 128 && NT == 1) ? 2 : 1) pa_tile_kernel(const __grid_constant__ PaParams p,
+                                                                      const __grid_constant__ CUtensorMap tmK,
+                                                                      const __grid_constant__ CUtensorMap tmV) {
   extern __shared__ uint8_t smem_raw[];
   Smem sm;
   {
@@ -1146,6 +1323,7 @@ __global__ void __launch_bounds__(D == 256 ? 288 : 160) pa_tile_kernel(const __g
     }
     sm.misc(p)[0] = 0;
     sm.misc(p)[1] = 0;
+    sm.misc(p)[2] = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -1154,23 +1332,23 @@ __global__ void __launch_bounds__(D == 256 ? 288 : 160) pa_tile_kernel(const __g
   if (warp == p.NCW) {
     Producer<ELT, NCH> prod(p, &tmK, &tmV, sm);
     prod.run();
-  } else {
-    Consumer<FP8, D, NT, VTOK> cons(p, sm);
-    cons.run();
     if (p.merge == kMergeCluster) {
       cluster_sync_all();
-      cons.cluster_merge(blockIdx.x / p.P);
       cluster_sync_all();
-      return;
     }
-  }
-  if (p.merge == kMergeCluster && warp == p.NCW) {
-    cluster_sync_all();
-    cluster_sync_all();
+  } else {
+    Consumer<FP8, D, NT, VTOK, TW> cons(p, sm);
+    cons.run();
+    if (p.merge == kMergeLastArriver) cons.run_pending();
+    if (p.merge == kMergeCluster) {
+      cluster_sync_all();
+      cons.cluster_merge(blockIdx.x / p.P, threadIdx.x, p.NCW * 32);
+      cluster_sync_all();
+    }
   }
 }
 
-// Standalone reducer: one CTA per unit merges the unit's partials in order.
+// Standalone reducer: one CTA per unit merges all of the unit's partials in order.
 template <int D>
 __device__ void reduce_unit(const PaParams& p) {
   const int unit = blockIdx.x;
@@ -1178,16 +1356,16 @@ __device__ void reduce_unit(const PaParams& p) {
   if (threadIdx.x == 0) desc_s = p.unit_desc[unit];
   __syncthreads();
   const int4 desc = desc_s;
-  if (desc.x < 2) return;
+  if (desc.x < 1) return;
   const MergeDesc md{desc.x, desc.y, desc.z, desc.w};
   const int b = unit / p.Hkv, g = unit % p.Hkv;
   merge_elems<D>(
-      p, per_tensor_vscale(p), md.nseg, b, g, threadIdx.x, blockDim.x, 0, p.R * (D / 4),
-      [&](int k, int r) {
-        return __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((size_t)merge_slot(md, k) * p.Rpad + r) * 2));
+      p, per_tensor_vscale(p), md.nseg * p.Wt, b, g, threadIdx.x, blockDim.x, 0, p.R * (D / 4),
+      [&](int q, int r) {
+        return __ldcg(reinterpret_cast<const float2*>(p.part_ml + (partial_index(md, p.Wt, q) * p.Rpad + r) * 2));
       },
-      [&](int k, int r, int d) {
-        return __ldcg(reinterpret_cast<const float4*>(p.part_o + ((size_t)merge_slot(md, k) * p.Rpad + r) * D + d));
+      [&](int q, int r, int d) {
+        return __ldcg(reinterpret_cast<const float4*>(p.part_o + (partial_index(md, p.Wt, q) * p.Rpad + r) * D + d));
       });
   __syncthreads();
   if (threadIdx.x == 0) p.unit_desc[unit].x = 0;

@@ -2,9 +2,9 @@
 #include "pa_tile.cuh"
 
 namespace pa {
-const void* tile_kernel_fp8_d256(int nt, int vtok) {
-  if (nt == 1 && !vtok) return reinterpret_cast<const void*>(&dev::pa_tile_kernel<true, 256, 1, false>);
-  if (nt == 1 && vtok) return reinterpret_cast<const void*>(&dev::pa_tile_kernel<true, 256, 1, true>);
-  return nullptr;
+const void* tile_kernel_fp8_d256(int nt, int vtok, int tw) {
+  if (tw != 1 || nt != 1) return nullptr;
+  if (!vtok) return reinterpret_cast<const void*>(&dev::pa_tile_kernel<true, 256, 1, false, 1>);
+  return reinterpret_cast<const void*>(&dev::pa_tile_kernel<true, 256, 1, true, 1>);
 }
 }  // namespace pa

@@ -24,31 +24,33 @@ def kernel_shape(d):
     wt = 1 if wr >= 4 else 4 // wr
     elt = 1 if d["kv_dtype"] == 0 else 2
     rb = d["head_dim"] * elt
-    tt = min(64, max(16, 16384 // (2 * rb)))
+    tt = min(128, max(16, 32768 // (2 * rb)))
+    tw = 2 if (d["kv_dtype"] == 0 and d["head_dim"] == 128) else 1
     return dict(R=R, G=G, nt=nt, rw=rw, wr=wr, wt=wt, ncw=wr * wt, rpad=wr * rw, elt=elt, rb=rb,
-                tt=tt, bh=min(d["page_size"], tt))
+                tt=tt, tw=tw, bh=min(d["page_size"], tt))
 
 
 def smem_total(d, k, ns, cluster):
     stage = 2 * k["tt"] * k["rb"] + (1024 if d["scale_mode"] == 2 else 0)
     off = ns * stage
-    off += align(k["wt"] * k["rpad"] * d["head_dim"] * 4 + k["wt"] * k["rpad"] * 8, 128)
     if cluster:
-        off += align(k["rpad"] * d["head_dim"] * 4 + k["rpad"] * 8, 128)
-    off += ns * 64 + ns * 16 + 64
+        off += align(k["wt"] * k["rpad"] * d["head_dim"] * 4 + k["wt"] * k["rpad"] * 8, 128)
+    off += ns * 128 + ns * 16 + 64 + 32 * 32
     return stage, off + 1024
 
 
 def plan(d):
     """Expected pa_plan_info fields for a descriptor dict with overrides set."""
     k = kernel_shape(d)
+    two = d["head_dim"] == 128 and k["nt"] == 1
     ns, budget = 0, SMEM_TWO
-    for attempt in range(2):
+    cl0 = d.get("sparse_topk", 0) > 0 or d.get("merge_mode", 0) == 2
+    for attempt in range(0 if two else 1, 2):
         if ns >= 3:
             break
         budget = SMEM_TWO if attempt == 0 else SMEM_ONE
-        stage, total0 = smem_total(d, k, 0, True)
-        ns = min(8, (budget - total0) // (stage + 80))
+        stage, total0 = smem_total(d, k, 0, cl0)
+        ns = min(8, (budget - total0) // (stage + 144))
     assert ns >= 2
     sm, cps = d["sm_count_override"], d["ctas_per_sm_override"]
     units = d["batch"] * d["num_kv_heads"]
@@ -81,15 +83,16 @@ def plan(d):
     if units == 0:
         grid = 0
     if sched == 1:
-        slots = 2 * grid
-    elif P > 1 and not cluster:
+        slots = 2 * grid + units if units > 0 else 0
+    elif (P > 1 and not cluster) or (P == 1 and k["wt"] > 1):
         slots = units * P
     else:
         slots = 0
-    off = align(slots * k["rpad"] * d["head_dim"] * 4, 256)
-    off = align(off + slots * k["rpad"] * 8, 256)
-    if merge == 3:
-        off = align(off + units * COUNTER_STRIDE * 4, 256)
+    kmerge = 3 if merge == 1 else merge
+    off = align(slots * k["wt"] * k["rpad"] * d["head_dim"] * 4, 256)
+    off = align(off + slots * k["wt"] * k["rpad"] * 8, 256)
+    if kmerge == 3 and slots > 0:
+        off = align(off + units * k["wr"] * COUNTER_STRIDE * 4, 256)
     if merge == 4:
         off = align(off + units * 16, 256)
     status = off
@@ -99,4 +102,4 @@ def plan(d):
                 row_warps=k["wr"], token_warps=k["wt"], block_threads=(k["ncw"] + 1) * 32,
                 grid=grid, cluster=P if cluster else 1, ctas_per_sm=cps, sm_count=sm,
                 launches_per_call=2 if merge == 4 else 1, units=units, smem_bytes=smem,
-                workspace_bytes=off, partial_slots=slots, status_offset=status)
+                workspace_bytes=off, partial_slots=slots * k["wt"], status_offset=status)

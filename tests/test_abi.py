@@ -113,6 +113,7 @@ BAD = [
     (dict(batch=-1), pa.PA_ERR_INVALID_ARG),
     (dict(num_pages=2 ** 30), pa.PA_ERR_UNSUPPORTED),
     (dict(max_partitions=300), pa.PA_ERR_INVALID_ARG),
+    (dict(head_dim=256, num_q_heads=64, num_kv_heads=1), pa.PA_ERR_UNSUPPORTED),
 ]
 
 
