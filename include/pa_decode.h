@@ -184,6 +184,24 @@ PA_API pa_status pa_decode_sparse(void* out, const void* q, const void* k_cache,
                            const int32_t* topk_idx, const float* k_scale, const float* v_scale,
                            const float* sinks, const pa_plan_t* plan, void* stream);
 
+/* Dense decode exactly like pa_decode, but on a scratch buffer built into the
+ * library instead of the plan's workspace, so it needs no device allocation
+ * from the caller (for code that cannot call cudaMalloc: plugins inside a
+ * framework that owns all device memory, or latency-critical paths where an
+ * allocation may synchronise the device). The reference pages have no
+ * counterpart to this entry point. The scratch is 32 MiB per GPU that loads
+ * the library, held until the process exits; plans whose
+ * pa_plan_workspace_bytes exceed it get PA_ERR_WORKSPACE. No workspace needs
+ * to be bound to the plan. The first call on a device looks up the scratch
+ * address (cudaGetSymbolAddress); make that first call before any stream
+ * capture. Every call shares the one buffer: calls that can overlap on the
+ * GPU race, so serialise them. Each call zeroes the scratch's counters and
+ * status word on `stream` before its kernel. */
+PA_API pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_table, const int32_t* ctx_lens, const float* k_scale,
+                                   const float* v_scale, int window, const float* sinks, const pa_plan_t* plan,
+                                   void* stream);
+
 PA_API const char* pa_strerror(pa_status status);
 
 /* Message of the last failure on this thread ("" if none). */

@@ -24,8 +24,8 @@ __all__ = [
     "PA_MERGE_LAST_ARRIVER", "PA_MERGE_REDUCER", "PA_SCHED_AUTO", "PA_SCHED_BALANCED",
     "PA_SCHED_PER_UNIT", "PaError", "PlanDesc", "PlanInfo", "Plan", "library", "library_path",
     "pa_plan_create", "pa_plan_workspace_bytes", "pa_plan_set_workspace", "pa_plan_get_info",
-    "pa_plan_destroy", "pa_decode", "pa_decode_sparse", "pa_strerror", "pa_last_error",
-    "EXPORTED_SYMBOLS",
+    "pa_plan_destroy", "pa_decode", "pa_decode_sparse", "pa_decode_noalloc", "pa_strerror",
+    "pa_last_error", "EXPORTED_SYMBOLS",
 ]
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA, PA_ERR_DEVICE_STATUS = range(6)
@@ -36,7 +36,8 @@ PA_SCHED_AUTO, PA_SCHED_BALANCED, PA_SCHED_PER_UNIT = 0, 1, 2
 
 EXPORTED_SYMBOLS = [
     "pa_plan_create", "pa_plan_workspace_bytes", "pa_plan_set_workspace", "pa_plan_get_info",
-    "pa_plan_destroy", "pa_decode", "pa_decode_sparse", "pa_strerror", "pa_last_error",
+    "pa_plan_destroy", "pa_decode", "pa_decode_sparse", "pa_decode_noalloc", "pa_strerror",
+    "pa_last_error",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -98,6 +99,8 @@ def library():
         lib.pa_decode.restype = st
         lib.pa_decode_sparse.argtypes = [vp] * 12
         lib.pa_decode_sparse.restype = st
+        lib.pa_decode_noalloc.argtypes = [vp] * 8 + [i, vp, vp, vp]
+        lib.pa_decode_noalloc.restype = st
         lib.pa_strerror.argtypes = [st]
         lib.pa_strerror.restype = ctypes.c_char_p
         lib.pa_last_error.argtypes = []
@@ -172,6 +175,16 @@ def pa_decode(out, q, k_cache, v_cache, block_table, ctx_lens, k_scale, v_scale,
     _check(library().pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
                                _ptr(ctx_lens), _ptr(k_scale), _ptr(v_scale), int(window), _ptr(sinks),
                                plan, _stream(stream)))
+
+
+def pa_decode_noalloc(out, q, k_cache, v_cache, block_table, ctx_lens, k_scale, v_scale, window,
+                      sinks, plan, stream=None):
+    """Dense decode on the library's built-in scratch: for callers that cannot
+    allocate device memory (no workspace has to be bound to `plan`)."""
+    _check(library().pa_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                       _ptr(block_table), _ptr(ctx_lens), _ptr(k_scale),
+                                       _ptr(v_scale), int(window), _ptr(sinks), plan,
+                                       _stream(stream)))
 
 
 def pa_decode_sparse(out, q, k_cache, v_cache, block_table, ctx_lens, topk_idx, k_scale, v_scale,

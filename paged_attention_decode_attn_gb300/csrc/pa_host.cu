@@ -465,6 +465,35 @@ pa_status launch(const pa_plan* cpl, void* out, const void* q, const void* k_cac
 
 }  // namespace
 
+namespace pa {
+
+// Decode with an explicit workspace in place of the plan's bound one. The
+// plan itself is not modified (a stack copy carries the workspace pointer).
+pa_status launch_on_workspace(const pa_plan* plan, void* ws, size_t ws_bytes, void* out, const void* q,
+                              const void* k_cache, const void* v_cache, const int32_t* block_table,
+                              const int32_t* ctx_lens, const float* k_scale, const float* v_scale, int window,
+                              const float* sinks, void* stream) {
+  pa_plan local = *plan;
+  local.ws = ws;
+  local.ws_bytes = ws_bytes;
+  return launch(&local, out, q, k_cache, v_cache, block_table, ctx_lens, nullptr, k_scale, v_scale, window, sinks,
+                stream);
+}
+
+// Record a failure message for pa_last_error() and return the status.
+pa_status set_error(pa_status status, const char* message) { return fail(status, "%s", message); }
+
+// Workspace bytes of a plan, the offset from which its workspace must start
+// zero-filled (arrival counters, reducer descriptors, status word), and its device.
+size_t plan_workspace_layout(const pa_plan* plan, size_t* zero_from, int* device, int* sparse) {
+  *zero_from = plan->off_counters;
+  *device = plan->desc.device;
+  *sparse = plan->desc.sparse_topk > 0;
+  return plan->info.workspace_bytes;
+}
+
+}  // namespace pa
+
 extern "C" {
 
 pa_status pa_plan_create(const pa_plan_desc* desc, pa_plan_t** out) {

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "pa_decode.h"
+
 namespace pa {
 
 enum : int { kSchedBalanced = 1, kSchedPerUnit = 2 };
@@ -68,5 +70,18 @@ const void* tile_kernel_fp8_d256(int nt, int vtok, int tw);
 const void* tile_kernel_bf16(int d, int nt, int tw);
 const void* reduce_kernel(int d);
 
+}  // namespace pa
+
+struct pa_plan;
+
+namespace pa {
+
+// Host helpers shared with the no-allocation entry point (pa_noalloc.cu).
+pa_status launch_on_workspace(const pa_plan* plan, void* ws, size_t ws_bytes, void* out, const void* q,
+                              const void* k_cache, const void* v_cache, const int32_t* block_table,
+                              const int32_t* ctx_lens, const float* k_scale, const float* v_scale, int window,
+                              const float* sinks, void* stream);
+size_t plan_workspace_layout(const pa_plan* plan, size_t* zero_from, int* device, int* sparse);
+pa_status set_error(pa_status status, const char* message);
 
 }  // namespace pa

@@ -1,0 +1,77 @@
+"""pa_decode_noalloc, the decode entry point for callers that cannot allocate
+device memory: a plugin inside a framework that owns every device
+allocation, or a latency-critical path where cudaMalloc may synchronise the
+device. It decodes on a scratch buffer built into the library, so no
+workspace is bound to its plan. Checked against pa_decode through the C ABI
+on two calls in a row (the second reuses the scratch the first left behind).
+"""
+
+import numpy as np
+import pytest
+
+import paged_attention_decode_attn_gb300 as pa
+import pa_workloads as pw
+from paged_attention_decode_attn_gb300 import _build
+
+ATOL = RTOL = 5e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    _build.build()
+
+
+def test_rejects_plans_larger_than_the_scratch():
+    # 16,000 CTAs x 2 partial slots x 64 rows x 128 dims of f32 is far above
+    # the 32 MiB scratch: refused before any device work.
+    h = pa.pa_plan_create(batch=4, num_q_heads=64, num_kv_heads=1, head_dim=128, query_len=1,
+                          page_size=64, max_pages_per_seq=64, num_pages=1024, kv_dtype=0,
+                          scale_mode=1, causal=1, sm_count_override=8000, ctas_per_sm_override=2)
+    try:
+        assert pa.pa_plan_workspace_bytes(h) > (32 << 20)
+        with pytest.raises(pa.PaError) as ei:
+            pa.pa_decode_noalloc(0x100, 0x100, 0x100, 0x100, 0x100, 0x100, 0x100, 0x100, 0, None, h,
+                                 stream=0)
+        assert ei.value.status == pa.PA_ERR_WORKSPACE
+        assert "32 MiB" in pa.pa_last_error()
+    finally:
+        pa.pa_plan_destroy(h)
+
+
+@pytest.mark.gpu
+def test_matches_pa_decode_on_two_calls():
+    torch = pytest.importorskip("torch")
+    w = pw.make_dense("noalloc", batch=7, hkv=2, group=8, head_dim=128, query_len=2, page_size=16,
+                      ctx_lens=[0, 3, 90, 600, 1300, 2222, 4001], kv_dtype=pw.KV_FP8,
+                      scale_mode=pw.SCALE_PER_TENSOR, seed=21, causal=1, with_sinks=True)
+    dev = torch.device("cuda", 0)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    q = t(w.q.view(np.int16)).view(torch.bfloat16)
+    k, v = t(w.k_cache), t(w.v_cache)
+    bt, ctx = t(w.block_table), t(w.ctx_lens)
+    ks, vs, sinks = t(w.k_scale), t(w.v_scale), t(w.sinks)
+    fields = dict(batch=w.batch, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                  head_dim=w.head_dim, query_len=w.query_len, page_size=w.page_size,
+                  max_pages_per_seq=w.max_pages_per_seq, num_pages=w.num_pages,
+                  max_context_len=int(w.ctx_lens.max()), kv_dtype=w.kv_dtype, scale_mode=w.scale_mode,
+                  causal=1, has_sinks=1, sm_count_override=5, ctas_per_sm_override=2)
+    # the existing entry point, with a caller-allocated workspace
+    plan = pa.Plan(device=dev, **fields)
+    ref = torch.full_like(q, float("nan"))
+    plan.decode(ref, q, k, v, bt, ctx, ks, vs, 0, sinks)
+    torch.cuda.synchronize()
+    ref = ref.float().cpu().numpy()
+    assert np.all(np.isfinite(ref))
+    # the no-allocation entry point: a plan with no workspace bound
+    h = pa.pa_plan_create(device=0, **fields)
+    try:
+        assert pa.pa_plan_get_info(h)["merge_mode"] == pa.PA_MERGE_LAST_ARRIVER
+        for _ in range(2):
+            out = torch.full_like(q, float("nan"))
+            pa.pa_decode_noalloc(out, q, k, v, bt, ctx, ks, vs, 0, sinks, h)
+            torch.cuda.synchronize()
+            got = out.float().cpu().numpy()
+            assert np.all(np.isfinite(got))
+            assert np.all(np.abs(got - ref) <= ATOL + RTOL * np.abs(ref))
+    finally:
+        pa.pa_plan_destroy(h)
