@@ -96,16 +96,20 @@ pa::SmemLayout smem_layout(const pa_plan_desc& d, const KernelShape& k, int ns, 
   L.off_stage = 0;
   size_t off = (size_t)ns * L.stage_bytes;
   L.off_merge = (int)off;
-  L.off_cpart = (int)off;  // cluster merge: per-warp partials of this CTA
-  if (cluster) off += align_up((size_t)k.wt * k.rpad * d.head_dim * 4 + (size_t)k.wt * k.rpad * 8, 128);
+  L.off_cpart = (int)off;  // cluster merge: this CTA's partial (O, then max/sum)
+  if (cluster) off += align_up((size_t)k.rpad * d.head_dim * 4 + (size_t)k.rpad * 8, 128);
   L.off_hdr = (int)off;
   off += (size_t)ns * 128;
   L.off_bar = (int)off;
   off += (size_t)ns * 16;
   L.off_misc = (int)off;
   off += 64;
-  L.off_pend = (int)off;  // queued last-arriver merges: 32 entries of 32 bytes
-  off += 32 * 32;
+  L.off_pend = (int)off;  // queued last-arriver merges: 8 entries of 32 bytes
+  off += 8 * 32;
+  L.off_arr = (int)off;  // recorded arrivals of split units: 4 entries of 32 bytes
+  off += 4 * 32;
+  L.off_mml = (int)off;  // (max, sum) of the token-group warps at a segment end
+  off += align_up((size_t)k.wt * k.rpad * 8, 16);
   L.total = (int)(off + 1024);  // slack for aligning the base to 1024 bytes
   return L;
 }
@@ -237,6 +241,9 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
     if (ns > 8) ns = 8;
   }
   if (ns < 2) return fail(PA_ERR_UNSUPPORTED, "shared memory too small for two ring stages");
+  // the token-group warps merge their partial states inside one stage buffer
+  if (k.wt > 1 && (size_t)k.wt * k.rpad * d.head_dim * 4 > (size_t)2 * k.tt * k.rb)
+    return fail(PA_ERR_UNSUPPORTED, "token-group merge does not fit a ring stage");
 
   int ctas_per_sm = ctas_override;
   if (ctas_per_sm == 0) ctas_per_sm = budget == kSmemTwoPerSm ? 2 : 1;  // refined by the occupancy query
@@ -252,26 +259,26 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   const int R = G * d.query_len;
   long long grid = sched == PA_SCHED_BALANCED ? (long long)sm_count * ctas_per_sm : (long long)units * P;
   if (units == 0) grid = 0;
-  // Partials are per (segment slot, token-group warp). A unit needs merging
-  // unless one warp group saw all of it (per-unit, one partition, Wt == 1).
+  // One partial per segment of a split unit: balanced CTAs keep two slots
+  // (the unit they start with, the unit they end with); per-unit plans one
+  // per partition. Units one CTA covers alone are written directly.
   size_t slots = 0;
   if (sched == PA_SCHED_BALANCED)
-    slots = units > 0 ? 2 * (size_t)grid + units : 0;
-  else if ((P > 1 && !cluster) || (P == 1 && k.wt > 1))
+    slots = 2 * (size_t)grid;
+  else if (P > 1 && !cluster)
     slots = (size_t)units * P;
-  // Direct output with several token groups merges them like a last arriver.
-  const int kernel_merge = (merge == PA_MERGE_DIRECT) ? PA_MERGE_LAST_ARRIVER : merge;
-  const bool counters = kernel_merge == PA_MERGE_LAST_ARRIVER && slots > 0;
+  const int kernel_merge = merge;
+  const bool counters = merge == PA_MERGE_LAST_ARRIVER && slots > 0;
 
-  // workspace: partial O, partial (max, sum), arrival counters (one line per
-  // unit and row slice), reducer descriptors, status word
+  // workspace: partial O, partial (max, sum), arrival counters (one 128-byte
+  // line per unit), reducer descriptors, status word
   size_t off = 0;
   pl->off_part_o = off;
-  off = align_up(off + slots * k.wt * k.rpad * d.head_dim * 4, 256);
+  off = align_up(off + slots * k.rpad * d.head_dim * 4, 256);
   pl->off_part_ml = off;
-  off = align_up(off + slots * k.wt * k.rpad * 8, 256);
+  off = align_up(off + slots * k.rpad * 8, 256);
   pl->off_counters = off;
-  if (counters) off = align_up(off + (size_t)units * k.wr * pa::kCounterStride * 4, 256);
+  if (counters) off = align_up(off + (size_t)units * pa::kCounterStride * 4, 256);
   pl->off_desc = off;
   if (merge == PA_MERGE_REDUCER) off = align_up(off + (size_t)units * 16, 256);
   pl->off_status = off;
@@ -295,7 +302,7 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   in.units = units;
   in.smem_bytes = (size_t)L.total;
   in.workspace_bytes = off;
-  in.partial_slots = slots * k.wt;
+  in.partial_slots = slots;
   in.status_offset = pl->off_status;
 
   pa::PaParams& p = pl->base;
@@ -337,6 +344,8 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   p.off_cpart = L.off_cpart;
   p.off_misc = L.off_misc;
   p.off_pend = L.off_pend;
+  p.off_arr = L.off_arr;
+  p.off_mml = L.off_mml;
   return PA_OK;
 }
 

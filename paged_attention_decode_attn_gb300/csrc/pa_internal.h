@@ -14,7 +14,7 @@ enum : int { kMergeDirect = 1, kMergeCluster = 2, kMergeLastArriver = 3, kMergeR
 enum : int { kScaleNone = 0, kScalePerTensor = 1, kScalePerToken = 2 };
 
 // Device status bits (int32 in the workspace).
-enum : int { kStatusTimeout = 1, kStatusBadPage = 2 };
+enum : int { kStatusTimeout = 1, kStatusBadPage = 2, kStatusInternal = 4 };
 
 // Stage header flags.
 enum : int { kSegFirst = 1, kSegLast = 2, kSegWhole = 4 };
@@ -53,12 +53,12 @@ struct PaParams {
   int swz;          // XOR mask of the 128-byte swizzle (7) or 0 (linear rows)
   // dynamic shared memory layout (byte offsets from a 1024-aligned base)
   int off_stage, stage_bytes, off_scale;  // off_scale: within a stage
-  int off_hdr, off_bar, off_merge, off_cpart, off_misc, off_pend;
+  int off_hdr, off_bar, off_merge, off_cpart, off_misc, off_pend, off_arr, off_mml;
 };
 
 // Host-visible shared-memory sizing for a kernel configuration.
 struct SmemLayout {
-  int stage_bytes, off_stage, off_scale, off_hdr, off_bar, off_merge, off_cpart, off_misc, off_pend, total;
+  int stage_bytes, off_stage, off_scale, off_hdr, off_bar, off_merge, off_cpart, off_misc, off_pend, off_arr, off_mml, total;
 };
 
 using KernelFn = void (*)(PaParams, CUtensorMap, CUtensorMap);

@@ -53,7 +53,8 @@ struct alignas(16) StageHdr {
 };
 static_assert(sizeof(StageHdr) == 128, "header size");
 constexpr int kEnd = 1 << 8;
-constexpr int kPendingMax = 32;  // queued last-arriver merges per CTA
+constexpr int kArrivalsMax = 4;    // split units recorded per CTA (at most 2 in schedule order)
+constexpr int kScanRegs = 8;       // schedule scan in registers for batch <= 256
 
 // ---------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -331,53 +332,54 @@ __device__ __forceinline__ void finalize_store(const PaParams& p, float vscale, 
 template <int D, class LoadML, class LoadO>
 __device__ __forceinline__ void merge_elems(const PaParams& p, float vscale, int n, int b, int g, int tid, int nthr,
                                             int e0, int e1, LoadML load_ml, LoadO load_o) {
-  constexpr int kStaged = 16;  // partials whose (max, sum) are loaded up front
+  // Partials are read in chunks of kChunk whose loads are all issued before
+  // any is used (one memory round trip per chunk); chunks fold into a running
+  // (max, sum, O) in partition order. An empty partial (max = -inf, sum = 0,
+  // O = 0) contributes exact zeros.
+  constexpr int kChunk = 8;
   for (int e = e0 + tid; e < e1; e += nthr) {
     const int r = e / (D / 4);
     const int d = (e % (D / 4)) * 4;
-    float M = -INFINITY;
-    float2 ml[kStaged];
-#pragma unroll
-    for (int q = 0; q < kStaged; ++q)
-      if (q < n) ml[q] = load_ml(q, r);
-#pragma unroll
-    for (int q = 0; q < kStaged; ++q)
-      if (q < n) M = fmaxf(M, ml[q].x);
-    for (int q = kStaged; q < n; ++q) M = fmaxf(M, load_ml(q, r).x);
-    float L = 0.f;
+    float M = -INFINITY, L = 0.f;
     float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q0 = 0; q0 < n; q0 += kChunk) {
+      float2 ml[kChunk];
+      float4 ov[kChunk];
 #pragma unroll
-    for (int q = 0; q < kStaged; ++q) {
-      if (q < n && ml[q].x != -INFINITY) {
-        const float a = ex2(ml[q].x - M);
-        const float4 oq = load_o(q, r, d);
-        L = fmaf(ml[q].y, a, L);
-        O.x = fmaf(oq.x, a, O.x);
-        O.y = fmaf(oq.y, a, O.y);
-        O.z = fmaf(oq.z, a, O.z);
-        O.w = fmaf(oq.w, a, O.w);
+      for (int q = 0; q < kChunk; ++q) {
+        if (q0 + q < n) {
+          ml[q] = load_ml(q0 + q, r);
+          ov[q] = load_o(q0 + q, r, d);
+        } else {
+          ml[q] = make_float2(-INFINITY, 0.f);
+          ov[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
-    }
-    for (int q = kStaged; q < n; ++q) {
-      const float2 m2 = load_ml(q, r);
-      if (m2.x == -INFINITY) continue;
-      const float a = ex2(m2.x - M);
-      const float4 oq = load_o(q, r, d);
-      L = fmaf(m2.y, a, L);
-      O.x = fmaf(oq.x, a, O.x);
-      O.y = fmaf(oq.y, a, O.y);
-      O.z = fmaf(oq.z, a, O.z);
-      O.w = fmaf(oq.w, a, O.w);
+      float Mc = M;
+#pragma unroll
+      for (int q = 0; q < kChunk; ++q) Mc = fmaxf(Mc, ml[q].x);
+      if (Mc == -INFINITY) continue;
+      const float c = ex2(M - Mc);  // rescale what the earlier chunks summed (0 if none)
+      L *= c;
+      O.x *= c;
+      O.y *= c;
+      O.z *= c;
+      O.w *= c;
+#pragma unroll
+      for (int q = 0; q < kChunk; ++q) {
+        const float a = ex2(ml[q].x - Mc);
+        L = fmaf(ml[q].y, a, L);
+        O.x = fmaf(ov[q].x, a, O.x);
+        O.y = fmaf(ov[q].y, a, O.y);
+        O.z = fmaf(ov[q].z, a, O.z);
+        O.w = fmaf(ov[q].w, a, O.w);
+      }
+      M = Mc;
     }
     finalize_store<D>(p, vscale, O, M, L, b, g, r, d);
   }
 }
 
-// Storage index of the q-th partial of a unit: segment k = q / Wt (in
-// schedule order), token group w = q % Wt.
-__device__ __forceinline__ size_t partial_index(const MergeDesc& md, int Wt, int q) {
-  return (size_t)merge_slot(md, q / Wt) * Wt + (q % Wt);
-}
 
 __device__ __forceinline__ float per_tensor_vscale(const PaParams& p) {
   return p.scale_mode == kScalePerTensor ? __ldg(p.v_scale) : 1.f;
@@ -620,7 +622,25 @@ struct Producer {
     } else {
       // With fewer chunks than CTAs only the first N CTAs take work, so every
       // CTA between a unit's first and last owner holds part of that unit.
-      const long long N = balanced_total(p, lane);
+      long long N;
+      long long cnt_reg[kScanRegs];
+      const bool in_regs = p.B <= 32 * kScanRegs;
+      if (in_regs) {
+        // chunk counts of sequences lane, lane + 32, ... loaded in one round trip
+#pragma unroll
+        for (int i = 0; i < kScanRegs; ++i) {
+          const int b = i * 32 + lane;
+          cnt_reg[i] = b < p.B ? (long long)p.Hkv * max(1, unit_range(p, b).n) : 0;
+        }
+        long long t = 0;
+#pragma unroll
+        for (int i = 0; i < kScanRegs; ++i) t += cnt_reg[i];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+        N = t;
+      } else {
+        N = balanced_total(p, lane);
+      }
       const long long C = min((long long)p.C, N);
       const long long c = blockIdx.x;
       long long x = c < C ? sched_start(c, N, C) : 0;
@@ -628,7 +648,30 @@ struct Producer {
       if (x < x1) {
         int b;
         long long excl;
-        balanced_find(p, lane, x, b, excl);
+        if (in_regs) {
+          long long base = 0;
+          b = p.B;
+          excl = 0;
+#pragma unroll
+          for (int i = 0; i < kScanRegs; ++i) {
+            long long incl = cnt_reg[i];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+              const long long v = __shfl_up_sync(0xffffffffu, incl, off);
+              if (lane >= off) incl += v;
+            }
+            const long long total = __shfl_sync(0xffffffffu, incl, 31);
+            const unsigned hit = __ballot_sync(0xffffffffu, base + incl > x);
+            if (hit && b == p.B) {
+              const int first = __ffs(hit) - 1;
+              b = i * 32 + first;
+              excl = base + __shfl_sync(0xffffffffu, incl - cnt_reg[i], first);
+            }
+            base += total;
+          }
+        } else {
+          balanced_find(p, lane, x, b, excl);
+        }
         UnitRange r = unit_range(p, b);
         long long nb = max(1, r.n);
         int g = (int)((x - excl) / nb);
@@ -636,17 +679,11 @@ struct Producer {
           const long long Pu = excl + g * nb;
           const long long kin = x - Pu;
           const long long take = min(nb - kin, x1 - x);
-          // Slots: a unit that one CTA covers alone owns slot 2*grid + unit; a
-          // split unit uses its CTAs' continuation slots (2c: the unit CTA c
-          // starts with, 2c + 1: the unit CTA c ends with).
-          MergeDesc md = balanced_desc(Pu, nb, N, C);
-          int slot;
-          if (md.nseg == 1) {
-            slot = 2 * p.C + b * p.Hkv + g;
-            md.s0 = md.sbase = slot;
-          } else {
-            slot = (int)(2 * c + ((c == sched_owner(Pu, N, C) && sched_start(c, N, C) < Pu) ? 1 : 0));
-          }
+          // A unit split over CTAs c1..c2 writes one partial per CTA: slot 2c
+          // for the unit CTA c starts with, 2c + 1 for the one it ends with (a
+          // unit one CTA covers alone is written as output directly).
+          const MergeDesc md = balanced_desc(Pu, nb, N, C);
+          const int slot = (int)(2 * c + ((c == sched_owner(Pu, N, C) && sched_start(c, N, C) < Pu) ? 1 : 0));
           if (r.n > 0)
             segment(b, g, r, (int)kin, (int)(kin + take), md.nseg == 1, slot, md);
           else
@@ -1087,12 +1124,18 @@ struct Consumer {
   }
 
   // ---------------------------------------------------------------- epilogue
-  // Segment end for this warp: either the output rows directly (a whole unit
-  // seen by one token group), or a per-warp partial that the last arriver,
-  // the cluster or the reducer merges.
-  __device__ void end_segment(const StageView& h, int slot, const MergeDesc& md) {
+  // Segment end. The token-group warps hold partial states of the same rows;
+  // they merge them through the segment's last stage buffer (free once every
+  // warp has read it) in a fixed order, then write the BF16 output (a unit the
+  // CTA covers alone), a global partial (a split unit) or the cluster partial.
+  // Only then is the stage handed back to the producer.
+  __device__ void end_segment(const StageView& h, int slot, const MergeDesc& md, int s) {
     const bool whole = (h.flags & kSegWhole) != 0;
+    const bool cluster = p.merge == kMergeCluster;
     const float ounit = VTOK ? __uint_as_float((uint32_t)(max(vexp, -126) + 127) << 23) : 1.f;
+    const int nthr = p.NCW * 32;
+    float* cp_o = reinterpret_cast<float*>(sm.base + p.off_cpart);
+    float* cp_ml = cp_o + (size_t)p.Rpad * D;
     float lsum[NT][2];
 #pragma unroll
     for (int j = 0; j < NT; ++j)
@@ -1104,109 +1147,186 @@ struct Consumer {
         l += __shfl_xor_sync(0xffffffffu, l, 16);
         lsum[j][rho] = l;
       }
-    const bool direct = whole && p.Wt == 1;
-    const bool cluster = p.merge == kMergeCluster;
-    const size_t pi = (size_t)slot * p.Wt + wt;
-    float* cp_o = reinterpret_cast<float*>(sm.base + p.off_cpart);
-    float* cp_ml = cp_o + (size_t)p.Wt * p.Rpad * D;
+    if (p.Wt == 1) {
+      // one token group: this warp's rows are complete in registers
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.empty(s, p));
 #pragma unroll
-    for (int j = 0; j < NT; ++j)
+      for (int j = 0; j < NT; ++j)
 #pragma unroll
-      for (int rho = 0; rho < 2; ++rho) {
-        const int r = row_of(j, rho);
-        if (r >= p.R) continue;
+        for (int rho = 0; rho < 2; ++rho) {
+          const int r = row_of(j, rho);
+          if (r >= p.R) continue;
 #pragma unroll
-        for (int cb = 0; cb < NCH; ++cb) {
-          // this thread holds d = cb*DPB + (DPB/8)*g4 + {0 .. DPB/8 - 1} of row r
-          float v[DPB / 8];
+          for (int cb = 0; cb < NCH; ++cb) {
+            float v[DPB / 8];
 #pragma unroll
-          for (int mt = 0; mt < MT_BLK; ++mt) {
-            v[2 * mt] = o[cb * MT_BLK + mt][j][rho] * ounit;
-            v[2 * mt + 1] = o[cb * MT_BLK + mt][j][rho + 2] * ounit;
+            for (int mt = 0; mt < MT_BLK; ++mt) {
+              v[2 * mt] = o[cb * MT_BLK + mt][j][rho] * ounit;
+              v[2 * mt + 1] = o[cb * MT_BLK + mt][j][rho + 2] * ounit;
+            }
+            const int d0 = cb * DPB + (DPB / 8) * g4;
+#pragma unroll
+            for (int q4 = 0; q4 < DPB / 32; ++q4) {
+              const float4 f = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+              if (whole)
+                finalize_store<D>(p, vscale, f, mrun[j][rho], lsum[j][rho], h.b, h.g, r, d0 + 4 * q4);
+              else if (cluster)
+                *reinterpret_cast<float4*>(cp_o + (size_t)r * D + d0 + 4 * q4) = f;
+              else
+                *reinterpret_cast<float4*>(p.part_o + ((size_t)slot * p.Rpad + r) * D + d0 + 4 * q4) = f;
+            }
           }
-          const int d0 = cb * DPB + (DPB / 8) * g4;
-#pragma unroll
-          for (int q4 = 0; q4 < DPB / 32; ++q4) {
-            const float4 f = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
-            if (direct)
-              finalize_store<D>(p, vscale, f, mrun[j][rho], lsum[j][rho], h.b, h.g, r, d0 + 4 * q4);
-            else if (cluster)
-              *reinterpret_cast<float4*>(cp_o + ((size_t)wt * p.Rpad + r) * D + d0 + 4 * q4) = f;
+          if (g4 == 0 && !whole) {
+            const float2 ml = make_float2(mrun[j][rho], lsum[j][rho]);
+            if (cluster)
+              *reinterpret_cast<float2*>(cp_ml + 2 * r) = ml;
             else
-              *reinterpret_cast<float4*>(p.part_o + (pi * p.Rpad + r) * D + d0 + 4 * q4) = f;
+              *reinterpret_cast<float2*>(p.part_ml + ((size_t)slot * p.Rpad + r) * 2) = ml;
           }
         }
-        if (g4 == 0 && !direct) {
-          const float2 ml = make_float2(mrun[j][rho], lsum[j][rho]);
-          if (cluster)
-            *reinterpret_cast<float2*>(cp_ml + ((size_t)wt * p.Rpad + r) * 2) = ml;
-          else
-            *reinterpret_cast<float2*>(p.part_ml + (pi * p.Rpad + r) * 2) = ml;
+    } else {
+      // several token groups: merge through the stage buffer
+      float* mb_o = reinterpret_cast<float*>(sm.base + (sm.stage(s, p) - sm.base_u32));
+      float* mb_ml = reinterpret_cast<float*>(sm.base + p.off_mml);
+      named_bar(1, nthr);  // every warp is done reading stage s
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int rho = 0; rho < 2; ++rho) {
+          const int r = row_of(j, rho);
+          if (g4 == 0) {
+            mb_ml[((size_t)wt * p.Rpad + r) * 2 + 0] = mrun[j][rho];
+            mb_ml[((size_t)wt * p.Rpad + r) * 2 + 1] = lsum[j][rho];
+          }
+#pragma unroll
+          for (int cb = 0; cb < NCH; ++cb) {
+            float v[DPB / 8];
+#pragma unroll
+            for (int mt = 0; mt < MT_BLK; ++mt) {
+              v[2 * mt] = o[cb * MT_BLK + mt][j][rho] * ounit;
+              v[2 * mt + 1] = o[cb * MT_BLK + mt][j][rho + 2] * ounit;
+            }
+            float4* dst = reinterpret_cast<float4*>(mb_o + ((size_t)wt * p.Rpad + r) * D + cb * DPB + (DPB / 8) * g4);
+#pragma unroll
+            for (int q4 = 0; q4 < DPB / 32; ++q4)
+              dst[q4] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+          }
+        }
+      named_bar(1, nthr);
+      const int E = p.R * (D / 4);
+      for (int e = threadIdx.x; e < E; e += nthr) {
+        const int r = e / (D / 4);
+        const int d = (e % (D / 4)) * 4;
+        float M = -INFINITY;
+        for (int w = 0; w < p.Wt; ++w) M = fmaxf(M, mb_ml[((size_t)w * p.Rpad + r) * 2]);
+        float L = 0.f;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY) {
+          for (int w = 0; w < p.Wt; ++w) {
+            const float a = ex2(mb_ml[((size_t)w * p.Rpad + r) * 2] - M);
+            const float4 ow = *reinterpret_cast<const float4*>(mb_o + ((size_t)w * p.Rpad + r) * D + d);
+            L = fmaf(mb_ml[((size_t)w * p.Rpad + r) * 2 + 1], a, L);
+            O.x = fmaf(ow.x, a, O.x);
+            O.y = fmaf(ow.y, a, O.y);
+            O.z = fmaf(ow.z, a, O.z);
+            O.w = fmaf(ow.w, a, O.w);
+          }
+        }
+        if (whole) {
+          finalize_store<D>(p, vscale, O, M, L, h.b, h.g, r, d);
+        } else if (cluster) {
+          *reinterpret_cast<float4*>(cp_o + (size_t)r * D + d) = O;
+          if (d == 0) *reinterpret_cast<float2*>(cp_ml + 2 * r) = make_float2(M, L);
+        } else {
+          *reinterpret_cast<float4*>(p.part_o + ((size_t)slot * p.Rpad + r) * D + d) = O;
+          if (d == 0) *reinterpret_cast<float2*>(p.part_ml + ((size_t)slot * p.Rpad + r) * 2) = make_float2(M, L);
         }
       }
-    if (direct || cluster) return;
-    __threadfence();
-    __syncwarp();
-    const int npart = md.nseg * p.Wt;
-    if (p.merge == kMergeReducer) {
-      if (lane == 0 && wt == 0 && wr == 0 && slot == md.s0)
-        p.unit_desc[h.unit] = make_int4(md.nseg, md.s0, md.sbase, md.sstride);
-      return;
+      // the stage buffer was written through the generic proxy; order that
+      // before the producer's next TMA write into it
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      named_bar(1, nthr);  // the stage buffer and the (max, sum) area are read
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.empty(s, p));
     }
-    // last arriver among the unit's partials of this row slice merges the slice
-    int last = 0;
-    if (lane == 0) {
-      int* cnt = p.counters + ((size_t)h.unit * p.Wr + wr) * kCounterStride;
-      const int prev = atomicAdd(cnt, 1);
-      last = (prev == npart - 1);
-      if (last) atomicExch(cnt, 0);
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) return;
-    // Queue the merge of this row slice; the CTA's consumer warps run the
-    // queue together once the stream is done (a merge here would hold up the
-    // shared stage ring). A full queue merges on the spot with this warp.
-    int idx = 0;
-    if (lane == 0) idx = atomicAdd(reinterpret_cast<int*>(sm.base + p.off_misc) + 2, 1);
-    idx = __shfl_sync(0xffffffffu, idx, 0);
-    if (idx < kPendingMax) {
-      if (lane == 0) {
-        int4* q = reinterpret_cast<int4*>(sm.base + p.off_pend) + 2 * idx;
-        q[0] = make_int4(h.b, h.g, wr, md.nseg);
-        q[1] = make_int4(md.s0, md.sbase, md.sstride, 0);
+    if (whole || cluster) return;
+    if (threadIdx.x == 0) {
+      if (p.merge == kMergeReducer) {
+        if (slot == md.s0) p.unit_desc[h.unit] = make_int4(md.nseg, md.s0, md.sbase, md.sstride);
+      } else if (p.merge == kMergeLastArriver) {
+        // arrivals are made after the stream, behind one fence for all partials
+        volatile int* nrec = sm.misc(p) + 3;
+        const int k = *nrec;
+        // A CTA splits at most its first and last unit (one segment per CTA
+        // in the per-unit schedule), so the record list cannot overflow.
+        if (k < kArrivalsMax) {
+          int4* e = reinterpret_cast<int4*>(sm.base + p.off_arr) + 2 * k;
+          e[0] = make_int4(h.b, h.g, h.unit, md.nseg);
+          e[1] = make_int4(md.s0, md.sbase, md.sstride, 0);
+          *nrec = k + 1;
+        } else {
+          flag_status(p, kStatusInternal);
+        }
       }
-      return;
     }
-    __threadfence();
-    merge_slice(h.b, h.g, wr, md, lane, 32);
   }
 
-  // Merge one row slice of a unit from its global partials.
-  __device__ void merge_slice(int b, int g, int slice, const MergeDesc& md, int tid, int nthr) const {
-    const int e0 = slice * RW * (D / 4);
-    const int e1 = min(p.R, (slice + 1) * RW) * (D / 4);
-    merge_elems<D>(
-        p, vscale, md.nseg * p.Wt, b, g, tid, nthr, e0, e1,
-        [&](int q, int r) {
-          return __ldcg(reinterpret_cast<const float2*>(p.part_ml + (partial_index(md, p.Wt, q) * p.Rpad + r) * 2));
-        },
-        [&](int q, int r, int d) {
-          return __ldcg(reinterpret_cast<const float4*>(p.part_o + (partial_index(md, p.Wt, q) * p.Rpad + r) * D + d));
-        });
+  // Count one partial of a split unit; the last of its nseg partials queues
+  // the unit's merge for this CTA (thread 0 only).
+  __device__ void arrive(int b, int g, int unit, const MergeDesc& md) {
+    int* cnt = p.counters + (size_t)unit * kCounterStride;
+    const int prev = atomicAdd(cnt, 1);
+    if (prev != md.nseg - 1) return;
+    atomicExch(cnt, 0);
+    volatile int* npend = sm.misc(p) + 2;
+    const int idx = *npend;
+    int4* q = reinterpret_cast<int4*>(sm.base + p.off_pend) + 2 * idx;
+    q[0] = make_int4(b, g, unit, md.nseg);
+    q[1] = make_int4(md.s0, md.sbase, md.sstride, 0);
+    *npend = idx + 1;
   }
 
-  // After the stream: all consumer warps run the queued merges together.
-  __device__ void run_pending() {
-    const int nthr = p.NCW * 32;
-    named_bar(1, nthr);
-    const int cnt = min(*(reinterpret_cast<volatile int*>(sm.base + p.off_misc) + 2), kPendingMax);
+  // Run and clear the queued merges with all consumer threads.
+  __device__ void run_queue(int nthr) {
+    const int cnt = *(sm.misc(p) + 2);
     if (cnt == 0) return;
     __threadfence();
     for (int i = 0; i < cnt; ++i) {
       const int4* q = reinterpret_cast<const int4*>(sm.base + p.off_pend) + 2 * i;
       const int4 a = q[0], c = q[1];
-      merge_slice(a.x, a.y, a.z, MergeDesc{a.w, c.x, c.y, c.z}, threadIdx.x, nthr);
+      const MergeDesc md{a.w, c.x, c.y, c.z};
+      merge_elems<D>(
+          p, vscale, md.nseg, a.x, a.y, threadIdx.x, nthr, 0, p.R * (D / 4),
+          [&](int k, int r) {
+            return __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((size_t)merge_slot(md, k) * p.Rpad + r) * 2));
+          },
+          [&](int k, int r, int d) {
+            return __ldcg(
+                reinterpret_cast<const float4*>(p.part_o + ((size_t)merge_slot(md, k) * p.Rpad + r) * D + d));
+          });
     }
+    named_bar(1, nthr);
+    if (threadIdx.x == 0) *(sm.misc(p) + 2) = 0;
+    named_bar(1, nthr);
+  }
+
+  // After the stream: one fence for this CTA's partials, the recorded
+  // arrivals, then the merges this CTA turned out to be last for.
+  __device__ void finish_last_arriver() {
+    const int nthr = p.NCW * 32;
+    __threadfence();
+    named_bar(1, nthr);
+    if (threadIdx.x == 0) {
+      const int n = *(sm.misc(p) + 3);
+      for (int k = 0; k < n; ++k) {
+        const int4* e = reinterpret_cast<const int4*>(sm.base + p.off_arr) + 2 * k;
+        const int4 a = e[0], c = e[1];
+        arrive(a.x, a.y, a.z, MergeDesc{a.w, c.x, c.y, c.z});
+      }
+    }
+    named_bar(1, nthr);
+    run_queue(nthr);
   }
 
   __device__ void run() {
@@ -1219,7 +1339,7 @@ struct Consumer {
       if (!got) {
         if (lane == 0) {
           flag_status(p, kStatusTimeout);
-          sm.misc(p)[0] = 1;
+          sm.misc(p)[0] |= 1;
         }
         break;
       }
@@ -1257,15 +1377,19 @@ struct Consumer {
       const uint32_t sst = kst + p.off_scale;
       const int steps = p.TT / (16 * TW);
       for (int j = wt; j < steps; j += p.Wt) step(h, kst, vst, sst, j * TW);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sm.empty(s, p));
-      if (h.flags & kSegLast) end_segment(h, slot, md);
+      if (h.flags & kSegLast) {
+        end_segment(h, slot, md, s);  // hands stage s back itself
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.empty(s, p));
+      }
       ++n;
     }
   }
 
   // Cluster merge: CTA `rank` merges its share of the unit's output elements
-  // from the per-warp partials of all P CTAs, read over distributed shared memory.
+  // from the partials of all P CTAs (partition order), read over distributed
+  // shared memory.
   __device__ void cluster_merge(int unit, int tid, int nthr) {
     const int b = unit / p.Hkv, g = unit % p.Hkv;
     uint32_t rank;
@@ -1273,22 +1397,21 @@ struct Consumer {
     const int E = p.R * (D / 4);
     const int e0 = (int)((long long)rank * E / p.P), e1 = (int)((long long)(rank + 1) * E / p.P);
     const uint32_t cp_local = sm.base_u32 + p.off_cpart;
-    const uint32_t ml_off = (uint32_t)p.Wt * p.Rpad * D * 4u;
-    const int Wt = p.Wt;
+    const uint32_t ml_off = (uint32_t)p.Rpad * D * 4u;
     merge_elems<D>(
-        p, vscale, p.P * Wt, b, g, tid, nthr, e0, e1,
-        [&](int q, int r) {
+        p, vscale, p.P, b, g, tid, nthr, e0, e1,
+        [&](int k, int r) {
           uint32_t remote;
-          const uint32_t local = cp_local + ml_off + 8u * (uint32_t)((q % Wt) * p.Rpad + r);
-          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(q / Wt));
+          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(cp_local + ml_off + 8u * r), "r"(k));
           float2 v;
           asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(remote));
           return v;
         },
-        [&](int q, int r, int d) {
+        [&](int k, int r, int d) {
           uint32_t remote;
-          const uint32_t local = cp_local + 4u * (uint32_t)(((q % Wt) * p.Rpad + r) * D + d);
-          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(q / Wt));
+          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                       : "=r"(remote)
+                       : "r"(cp_local + 4u * (uint32_t)(r * D + d)), "r"(k));
           float4 v;
           asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
                        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
@@ -1321,9 +1444,7 @@ __global__ void __launch_bounds__(160, (D == 128 && NT == 1) ? 2 : 1) pa_tile_ke
       mbar_init(sm.full(s, p), 1);
       mbar_init(sm.empty(s, p), p.NCW);
     }
-    sm.misc(p)[0] = 0;
-    sm.misc(p)[1] = 0;
-    sm.misc(p)[2] = 0;
+    for (int i = 0; i < 16; ++i) sm.misc(p)[i] = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -1339,7 +1460,7 @@ __global__ void __launch_bounds__(160, (D == 128 && NT == 1) ? 2 : 1) pa_tile_ke
   } else {
     Consumer<FP8, D, NT, VTOK, TW> cons(p, sm);
     cons.run();
-    if (p.merge == kMergeLastArriver) cons.run_pending();
+    if (p.merge == kMergeLastArriver) cons.finish_last_arriver();
     if (p.merge == kMergeCluster) {
       cluster_sync_all();
       cons.cluster_merge(blockIdx.x / p.P, threadIdx.x, p.NCW * 32);
@@ -1348,7 +1469,7 @@ __global__ void __launch_bounds__(160, (D == 128 && NT == 1) ? 2 : 1) pa_tile_ke
   }
 }
 
-// Standalone reducer: one CTA per unit merges all of the unit's partials in order.
+// Standalone reducer: one CTA per split unit merges its partials in order.
 template <int D>
 __device__ void reduce_unit(const PaParams& p) {
   const int unit = blockIdx.x;
@@ -1356,16 +1477,16 @@ __device__ void reduce_unit(const PaParams& p) {
   if (threadIdx.x == 0) desc_s = p.unit_desc[unit];
   __syncthreads();
   const int4 desc = desc_s;
-  if (desc.x < 1) return;
+  if (desc.x < 2) return;
   const MergeDesc md{desc.x, desc.y, desc.z, desc.w};
   const int b = unit / p.Hkv, g = unit % p.Hkv;
   merge_elems<D>(
-      p, per_tensor_vscale(p), md.nseg * p.Wt, b, g, threadIdx.x, blockDim.x, 0, p.R * (D / 4),
-      [&](int q, int r) {
-        return __ldcg(reinterpret_cast<const float2*>(p.part_ml + (partial_index(md, p.Wt, q) * p.Rpad + r) * 2));
+      p, per_tensor_vscale(p), md.nseg, b, g, threadIdx.x, blockDim.x, 0, p.R * (D / 4),
+      [&](int k, int r) {
+        return __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((size_t)merge_slot(md, k) * p.Rpad + r) * 2));
       },
-      [&](int q, int r, int d) {
-        return __ldcg(reinterpret_cast<const float4*>(p.part_o + (partial_index(md, p.Wt, q) * p.Rpad + r) * D + d));
+      [&](int k, int r, int d) {
+        return __ldcg(reinterpret_cast<const float4*>(p.part_o + ((size_t)merge_slot(md, k) * p.Rpad + r) * D + d));
       });
   __syncthreads();
   if (threadIdx.x == 0) p.unit_desc[unit].x = 0;

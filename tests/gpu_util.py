@@ -92,10 +92,10 @@ def unit_rows_mask(w: pw.Workload, unit_mask: np.ndarray) -> np.ndarray:
 
 def arrival_counters(plan, head_dim: int):
     """View of a last-arriver plan's arrival counters (one 128-byte line per
-    unit and row slice) inside its workspace."""
+    unit) inside its workspace."""
     info = plan.info
     rpad = info["row_warps"] * info["rows_per_warp"]
     a = lambda x: (x + 255) // 256 * 256  # noqa: E731
     off = a(info["partial_slots"] * rpad * head_dim * 4)
     off = a(off + info["partial_slots"] * rpad * 8)
-    return plan.workspace[off:off + info["units"] * info["row_warps"] * 32 * 4].view(torch.int32)
+    return plan.workspace[off:off + info["units"] * 32 * 4].view(torch.int32)

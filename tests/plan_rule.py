@@ -34,8 +34,8 @@ def smem_total(d, k, ns, cluster):
     stage = 2 * k["tt"] * k["rb"] + (1024 if d["scale_mode"] == 2 else 0)
     off = ns * stage
     if cluster:
-        off += align(k["wt"] * k["rpad"] * d["head_dim"] * 4 + k["wt"] * k["rpad"] * 8, 128)
-    off += ns * 128 + ns * 16 + 64 + 32 * 32
+        off += align(k["rpad"] * d["head_dim"] * 4 + k["rpad"] * 8, 128)
+    off += ns * 128 + ns * 16 + 64 + 8 * 32 + 4 * 32 + align(k["wt"] * k["rpad"] * 8, 16)
     return stage, off + 1024
 
 
@@ -83,16 +83,15 @@ def plan(d):
     if units == 0:
         grid = 0
     if sched == 1:
-        slots = 2 * grid + units if units > 0 else 0
-    elif (P > 1 and not cluster) or (P == 1 and k["wt"] > 1):
+        slots = 2 * grid
+    elif P > 1 and not cluster:
         slots = units * P
     else:
         slots = 0
-    kmerge = 3 if merge == 1 else merge
-    off = align(slots * k["wt"] * k["rpad"] * d["head_dim"] * 4, 256)
-    off = align(off + slots * k["wt"] * k["rpad"] * 8, 256)
-    if kmerge == 3 and slots > 0:
-        off = align(off + units * k["wr"] * COUNTER_STRIDE * 4, 256)
+    off = align(slots * k["rpad"] * d["head_dim"] * 4, 256)
+    off = align(off + slots * k["rpad"] * 8, 256)
+    if merge == 3 and slots > 0:
+        off = align(off + units * COUNTER_STRIDE * 4, 256)
     if merge == 4:
         off = align(off + units * 16, 256)
     status = off
@@ -102,4 +101,4 @@ def plan(d):
                 row_warps=k["wr"], token_warps=k["wt"], block_threads=(k["ncw"] + 1) * 32,
                 grid=grid, cluster=P if cluster else 1, ctas_per_sm=cps, sm_count=sm,
                 launches_per_call=2 if merge == 4 else 1, units=units, smem_bytes=smem,
-                workspace_bytes=off, partial_slots=slots * k["wt"], status_offset=status)
+                workspace_bytes=off, partial_slots=slots, status_offset=status)
