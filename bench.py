@@ -72,10 +72,10 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", "pa_tile_dense_fp8_b64.md")
+def profiled_traffic(workload: str = "dense"):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    if it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"pa_tile_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -190,6 +190,38 @@ def cpu_baseline(w, units=CPU_SAMPLE_UNITS, seed=0):
             "seconds": dt}
 
 
+WORKLOADS = {
+    "dense": WORKLOAD,
+    "tiny": "tiny paged decode: batch 2, 1 KV head, GQA8, head_dim 128, page 16, contexts {37, 100}, FP8 per-tensor",
+    "d256": ("packed D256 long-context decode: batch 16, 2 KV heads, GQA8, head_dim 256, page 64, contexts "
+             "{8K, 128K} + ragged tails and one empty sequence, FP8 per-token scales"),
+    "sparse": ("sparse top-k decode: 64 rows, 16 query heads, 1 KV head, head_dim 128, page 16, 2048 of 131072 "
+               "tokens per row, 4096-page pool"),
+    "mtp4": ("dense MTP4 verify: batch 32, 4 KV heads, GQA16, head_dim 128, query length 4 causal, page 128, "
+             "contexts U[4096, 65536]"),
+}
+
+
+SEQ_LEN = {"dense": "U[1024,8192]", "tiny": "{37,100}", "d256": "{0, 8K+tail, 128K+tail}",
+           "sparse": "2048 of 131072", "mtp4": "U[4096,65536]"}
+MERGES = {"auto": 0, "direct": 1, "cluster": 2, "last-arriver": 3, "reducer": 4}
+
+
+def make_workload(args, rank):
+    kv = pw.KV_BF16 if args.kv == "bf16" else pw.KV_FP8
+    if args.workload == "dense":
+        return pw.dense(seed=1002 + rank)
+    if args.workload == "tiny":
+        return pw.tiny()
+    if args.workload == "d256":
+        return pw.d256(query_len=args.ql, window=args.window, with_sinks=args.sinks)
+    if args.workload == "sparse":
+        return pw.sparse(kv_dtype=kv)
+    if args.workload == "mtp4":
+        return pw.mtp4(kv_dtype=kv)
+    raise ValueError(args.workload)
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -224,6 +256,14 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="dense", choices=sorted(WORKLOADS),
+                    help="the headline line uses the default dense workload; the others are for profiling")
+    ap.add_argument("--kv", default="fp8", choices=["fp8", "bf16"], help="sparse and mtp4 cache format")
+    ap.add_argument("--ql", type=int, default=1, help="d256: query length (MTP rows)")
+    ap.add_argument("--window", type=int, default=0, help="d256: sliding window (0 = off)")
+    ap.add_argument("--sinks", action="store_true", help="d256: per-head sink logits")
+    ap.add_argument("--partitions", type=int, default=0, help="plan max_partitions (per-unit schedule)")
+    ap.add_argument("--merge", default="auto", choices=sorted(MERGES), help="plan merge mode")
     args = ap.parse_args()
     args.steps_ref = max(1, min(args.steps, 5))
     args.warmup_ref = 1 if args.warmup > 0 else 0
@@ -242,24 +282,29 @@ def main():
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
 
-    w = pw.dense(seed=1002 + rank)
+    w = make_workload(args, rank)
     alg = pw.algorithmic_bytes(w)
-    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
-    host = {
-        "q": torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).pin_memory(),
-        "k": torch.from_numpy(w.k_cache).pin_memory(),
-        "v": torch.from_numpy(w.v_cache).pin_memory(),
-        "bt": torch.from_numpy(w.block_table).pin_memory(),
-        "ctx": torch.from_numpy(w.ctx_lens).pin_memory(),
-        "ks": torch.from_numpy(w.k_scale).pin_memory(),
-        "vs": torch.from_numpy(w.v_scale).pin_memory(),
-    }
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    host = {"q": pin(w.q.view(np.int16)).view(torch.bfloat16), "bt": pin(w.block_table), "ctx": pin(w.ctx_lens)}
+    if w.kv_dtype == pw.KV_BF16:
+        host["k"] = pin(w.k_cache.view(np.int16)).view(torch.bfloat16)
+        host["v"] = pin(w.v_cache.view(np.int16)).view(torch.bfloat16)
+    else:
+        host["k"], host["v"] = pin(w.k_cache), pin(w.v_cache)
+    for name, arr in (("ks", w.k_scale), ("vs", w.v_scale), ("sinks", w.sinks), ("idx", w.topk_idx)):
+        if arr is not None:
+            host[name] = pin(arr)
     d = {k: v.to(dev) for k, v in host.items()}
     out = torch.empty_like(d["q"])
-    plan = pa.Plan(device=dev, batch=w.batch, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
-                   head_dim=w.head_dim, query_len=w.query_len, page_size=w.page_size,
-                   max_pages_per_seq=w.max_pages_per_seq, num_pages=w.num_pages,
-                   max_context_len=8192, kv_dtype=w.kv_dtype, scale_mode=w.scale_mode, causal=1)
+    fields = dict(batch=w.batch, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                  head_dim=w.head_dim, query_len=w.query_len, page_size=w.page_size,
+                  max_pages_per_seq=w.max_pages_per_seq, num_pages=w.num_pages,
+                  max_context_len=int(w.ctx_lens.max()), kv_dtype=w.kv_dtype, scale_mode=w.scale_mode,
+                  causal=int(w.causal), has_sinks=int(w.sinks is not None), sparse_topk=int(w.topk))
+    if args.partitions:
+        fields.update(schedule=pa.PA_SCHED_PER_UNIT, max_partitions=args.partitions)
+    fields["merge_mode"] = MERGES[args.merge]
+    plan = pa.Plan(device=dev, **fields)
     stream = torch.cuda.current_stream(dev)
     flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
 
@@ -267,7 +312,12 @@ def main():
         return flush.sum(dtype=torch.int64)
 
     def step():
-        plan.decode(out, d["q"], d["k"], d["v"], d["bt"], d["ctx"], d["ks"], d["vs"], 0, None, stream=stream)
+        if w.topk:
+            plan.decode_sparse(out, d["q"], d["k"], d["v"], d["bt"], d["ctx"], d["idx"], d.get("ks"), d.get("vs"),
+                               d.get("sinks"), stream=stream)
+        else:
+            plan.decode(out, d["q"], d["k"], d["v"], d["bt"], d["ctx"], d.get("ks"), d.get("vs"), w.window,
+                        d.get("sinks"), stream=stream)
 
     for _ in range(args.warmup):
         flush_l2()
@@ -324,23 +374,27 @@ def main():
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": float(np.mean(per_call_ms)),
             "us_per_call": per_launch_us, "us_per_call_median": float(np.median(per_call_ms)) * 1000.0,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 (KV), bf16 (Q/O), f32 accumulate",
-            "data": "synthetic (seeded pa_workloads.dense)",
-            "config": {"workload": WORKLOAD, "global_batch": 64 * world, "seq_len": "U[1024,8192]",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": ("fp8-e4m3" if w.kv_dtype == pw.KV_FP8 else "bf16") + " (KV), bf16 (Q/O), f32 accumulate",
+            "data": f"synthetic (seeded pa_workloads.{args.workload})",
+            "config": {"workload": WORKLOADS[args.workload], "global_batch": w.batch * world,
+                       "seq_len": SEQ_LEN[args.workload], "query_len": w.query_len,
+                       "window": int(w.window), "sinks": w.sinks is not None,
                        "parallelism": "replicas" if world > 1 else "single GPU",
-                       "l2": "inputs larger than L2 (604 MB KV); 512 MiB read-only pass before every timed call",
-                       "plan": {k: plan.info[k] for k in ("schedule", "merge_mode", "grid", "block_threads",
-                                                         "num_stages", "stage_tokens", "ctas_per_sm")}},
+                       "l2": "512 MiB read-only pass before every timed call (dense: inputs also larger than L2)",
+                       "plan": {k: plan.info[k] for k in ("schedule", "merge_mode", "num_partitions", "grid",
+                                                         "block_threads", "num_stages", "stage_tokens",
+                                                         "ctas_per_sm", "launches_per_call")}},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_kind": peak_kind, "traffic": profiled_traffic(),
-                         "algorithmic_bytes_per_launch": alg, "kernel": "pa_tile_kernel<fp8,128,1>"},
+                         "frac": achieved / peak, "peak_kind": peak_kind, "traffic": profiled_traffic(args.workload),
+                         "algorithmic_bytes_per_launch": alg, "kernel": "pa_tile_kernel"},
             "e2e": {"value": e2e_bytes / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "steps": e2e_steps},
             "gpu_launches": int(K * plan.info["launches_per_call"]),
             "clocks": clk.summary(),
             "device_status": status,
         }
-        if world == 1 and not args.no_cpu_baseline:
+        if world == 1 and not args.no_cpu_baseline and args.workload == "dense":
             cb = cpu_baseline(w)
             cb.pop("seconds")
             line["cpu_baseline"] = cb

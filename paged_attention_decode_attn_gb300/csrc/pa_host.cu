@@ -69,7 +69,9 @@ KernelShape kernel_shape(const pa_plan_desc& d) {
   KernelShape k;
   const int G = d.num_q_heads / d.num_kv_heads;
   const int R = G * d.query_len;
-  k.nt = (d.head_dim == 128 && R > 8) ? 2 : 1;
+  // Each consumer warp owns 8 query rows (one MMA N tile); groups of more
+  // rows take more row-slice warps (up to 8 for 64 rows).
+  k.nt = 1;
   k.rw = 8 * k.nt;
   k.wr = (R + k.rw - 1) / k.rw;
   k.wt = k.wr >= 4 ? 1 : 4 / k.wr;
@@ -116,10 +118,10 @@ pa::SmemLayout smem_layout(const pa_plan_desc& d, const KernelShape& k, int ns, 
 
 const void* pick_tile_kernel(const pa_plan_desc& d, const KernelShape& k) {
   if (d.kv_dtype == PA_KV_FP8_E4M3) {
-    if (d.head_dim == 128) return pa::tile_kernel_fp8_d128(k.nt, k.vtok, k.tw);
-    return pa::tile_kernel_fp8_d256(k.nt, k.vtok, k.tw);
+    if (d.head_dim == 128) return pa::tile_kernel_fp8_d128(k.vtok, k.ncw > 4);
+    return k.ncw > 4 ? nullptr : pa::tile_kernel_fp8_d256(k.vtok);
   }
-  return pa::tile_kernel_bf16(d.head_dim, k.nt, k.tw);
+  return pa::tile_kernel_bf16(d.head_dim, k.ncw > 4);
 }
 
 pa_status validate_desc(const pa_plan_desc& d) {
@@ -230,7 +232,7 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   // 8-row warp tiles: at most 168 registers, so three warps share an SM
   // sub-partition's register file) get as many stages as fit 112 KiB (at
   // least 3); the others one CTA per SM and up to 226 KiB.
-  const bool two_per_sm = d.head_dim == 128 && k.nt == 1;
+  const bool two_per_sm = d.head_dim == 128 && k.ncw <= 4;
   int ns = 0;
   int budget = kSmemTwoPerSm;
   for (int attempt = two_per_sm ? 0 : 1; attempt < 2 && ns < 3; ++attempt) {

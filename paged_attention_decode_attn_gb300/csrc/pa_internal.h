@@ -65,9 +65,9 @@ using KernelFn = void (*)(PaParams, CUtensorMap, CUtensorMap);
 
 // Tile-kernel instantiations (defined in the pa_tile_*.cu files).
 // Returns null when the combination is not instantiated.
-const void* tile_kernel_fp8_d128(int nt, int vtok, int tw);
-const void* tile_kernel_fp8_d256(int nt, int vtok, int tw);
-const void* tile_kernel_bf16(int d, int nt, int tw);
+const void* tile_kernel_fp8_d128(int vtok, int wide);
+const void* tile_kernel_fp8_d256(int vtok);
+const void* tile_kernel_bf16(int d, int wide);
 const void* reduce_kernel(int d);
 
 }  // namespace pa

@@ -493,6 +493,22 @@ struct Producer {
     }
   }
 
+  // Sparse stages: row r of stage k holds index position tbase + r. The index
+  // loads of a stage are issued together (and for the next stage while this
+  // one's gathers are in flight), then the block-table loads together, so a
+  // stage costs one dependent round trip on the producer's path.
+  int pf_b = -1, pf_pos = -1;
+  int pf_idx[4];
+
+  __device__ __forceinline__ void load_indices(int b, int pos0, int pos_end, int* idx) const {
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int row = rr * 32 + lane;
+      const int pos = pos0 + row;
+      idx[rr] = (row < p.TT && pos < pos_end) ? __ldg(p.topk_idx + (size_t)b * p.topk + pos) : -1;
+    }
+  }
+
   __device__ void emit_sparse(StageHdr h) {
     int s;
     if (!acquire_stage(s)) return;
@@ -501,24 +517,35 @@ struct Producer {
     const uint32_t vst = kst + (uint32_t)TT * 128u * NCH;
     const bool ktok = p.scale_mode == kScalePerToken;
     const bool empty = !(h.t1 > h.t0);
+    int idx[4];
+    if (!empty) {
+      if (pf_b == h.b && pf_pos == h.tbase) {
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) idx[rr] = pf_idx[rr];
+      } else {
+        load_indices(h.b, h.tbase, h.t1, idx);
+      }
+    }
+    int phys[4];
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int t = empty ? -1 : idx[rr];
+      phys[rr] = (t >= 0 && t < h.L) ? __ldg(p.block_table + (size_t)h.b * p.maxp + t / p.S) : -1;
+    }
     int yv[4];
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) {
       const int row = rr * 32 + lane;
-      const int pos = h.tbase + row;
-      bool valid = false;
+      const int t = empty ? -1 : idx[rr];
+      const bool valid = t >= 0 && t < h.L;
       int y = 0;
-      if (!empty && row < TT && pos < h.t1) {
-        const int t = __ldg(p.topk_idx + (size_t)h.b * p.topk + pos);
-        if (t >= 0 && t < h.L) {
-          int phys = __ldg(p.block_table + (size_t)h.b * p.maxp + t / p.S);
-          if (phys < 0 || phys >= p.num_pages) {
-            flag_status(p, kStatusBadPage);
-            phys = 0;
-          }
-          y = (phys * p.Hkv + h.g) * p.S + t % p.S;
-          valid = true;
+      if (valid) {
+        int ph = phys[rr];
+        if (ph < 0 || ph >= p.num_pages) {
+          flag_status(p, kStatusBadPage);
+          ph = 0;
         }
+        y = (ph * p.Hkv + h.g) * p.S + t % p.S;
       }
       yv[rr] = y;
       h.mask[rr] = __ballot_sync(0xffffffffu, valid);
@@ -560,6 +587,15 @@ struct Producer {
           tma_gather4(vst + (uint32_t)(cb * TT + 4 * lane) * 128u, tmV, cb * (128 / ELT), y4[0], y4[1], y4[2], y4[3], bar);
         }
       }
+    }
+    // prefetch the next stage's indices of this segment
+    const int next = h.tbase + TT;
+    if (!empty && next < h.t1 + TT && next < p.topk) {
+      load_indices(h.b, next, p.topk, pf_idx);
+      pf_b = h.b;
+      pf_pos = next;
+    } else {
+      pf_b = -1;
     }
   }
 
@@ -1426,8 +1462,10 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-template <bool FP8, int D, int NT, bool VTOK, int TW>
-__global__ void __launch_bounds__(160, (D == 128 && NT == 1) ? 2 : 1) pa_tile_kernel(const __grid_constant__ PaParams p,
+// MAXW: warps per CTA the instantiation is built for (5: up to 4 consumer
+// warps, two CTAs per SM at head_dim 128; 9: up to 8 row-slice warps).
+template <bool FP8, int D, int NT, bool VTOK, int TW, int MAXW>
+__global__ void __launch_bounds__(MAXW * 32, (D == 128 && MAXW == 5) ? 2 : 1) pa_tile_kernel(const __grid_constant__ PaParams p,
                                                                       const __grid_constant__ CUtensorMap tmK,
                                                                       const __grid_constant__ CUtensorMap tmV) {
   extern __shared__ uint8_t smem_raw[];

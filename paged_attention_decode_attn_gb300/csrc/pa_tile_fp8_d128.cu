@@ -2,12 +2,10 @@
 #include "pa_tile.cuh"
 
 namespace pa {
-const void* tile_kernel_fp8_d128(int nt, int vtok, int tw) {
-  if (tw != 2) return nullptr;
-  if (nt == 1 && !vtok) return reinterpret_cast<const void*>(&dev::pa_tile_kernel<true, 128, 1, false, 2>);
-  if (nt == 1 && vtok) return reinterpret_cast<const void*>(&dev::pa_tile_kernel<true, 128, 1, true, 2>);
-  if (nt == 2 && !vtok) return reinterpret_cast<const void*>(&dev::pa_tile_kernel<true, 128, 2, false, 2>);
-  if (nt == 2 && vtok) return reinterpret_cast<const void*>(&dev::pa_tile_kernel<true, 128, 2, true, 2>);
-  return nullptr;
+const void* tile_kernel_fp8_d128(int vtok, int wide) {
+  if (!vtok && !wide) return reinterpret_cast<const void*>(&dev::pa_tile_kernel<true, 128, 1, false, 2, 5>);
+  if (vtok && !wide) return reinterpret_cast<const void*>(&dev::pa_tile_kernel<true, 128, 1, true, 2, 5>);
+  if (!vtok && wide) return reinterpret_cast<const void*>(&dev::pa_tile_kernel<true, 128, 1, false, 2, 9>);
+  return reinterpret_cast<const void*>(&dev::pa_tile_kernel<true, 128, 1, true, 2, 9>);
 }
 }  // namespace pa

@@ -18,7 +18,7 @@ def align(x, a):
 def kernel_shape(d):
     G = d["num_q_heads"] // d["num_kv_heads"]
     R = G * d["query_len"]
-    nt = 2 if (d["head_dim"] == 128 and R > 8) else 1
+    nt = 1
     rw = 8 * nt
     wr = -(-R // rw)
     wt = 1 if wr >= 4 else 4 // wr
@@ -42,7 +42,7 @@ def smem_total(d, k, ns, cluster):
 def plan(d):
     """Expected pa_plan_info fields for a descriptor dict with overrides set."""
     k = kernel_shape(d)
-    two = d["head_dim"] == 128 and k["nt"] == 1
+    two = d["head_dim"] == 128 and k["ncw"] <= 4
     ns, budget = 0, SMEM_TWO
     cl0 = d.get("sparse_topk", 0) > 0 or d.get("merge_mode", 0) == 2
     for attempt in range(0 if two else 1, 2):
