@@ -57,6 +57,10 @@ struct pa_plan {
 namespace {
 
 // Largest dynamic shared memory a CTA may use while two CTAs share an SM.
+// A segment's fixed cost (query rows, token-group merge, output or partial
+// write) is about one stage of streaming; the balanced schedule charges it as
+// one virtual chunk per unit.
+constexpr int kSegCostChunks = 1;
 constexpr int kSmemTwoPerSm = 112 * 1024;
 constexpr int kSmemOnePerSm = 226 * 1024;
 
@@ -91,7 +95,7 @@ KernelShape kernel_shape(const pa_plan_desc& d) {
 }
 
 // Shared-memory layout for `ns` ring stages.
-pa::SmemLayout smem_layout(const pa_plan_desc& d, const KernelShape& k, int ns, bool cluster) {
+pa::SmemLayout smem_layout(const pa_plan_desc& d, const KernelShape& k, int ns, bool cluster, int nq) {
   pa::SmemLayout L;
   L.stage_bytes = 2 * k.tt * k.rb + (d.scale_mode == PA_SCALE_PER_TOKEN ? 1024 : 0);
   L.off_scale = 2 * k.tt * k.rb;
@@ -103,15 +107,17 @@ pa::SmemLayout smem_layout(const pa_plan_desc& d, const KernelShape& k, int ns, 
   L.off_hdr = (int)off;
   off += (size_t)ns * 128;
   L.off_bar = (int)off;
-  off += (size_t)ns * 16;
+  off += (size_t)ns * 16 + 32;  // full/empty per stage, then full/empty per Q slot
   L.off_misc = (int)off;
   off += 64;
   L.off_pend = (int)off;  // queued last-arriver merges: 8 entries of 32 bytes
   off += 8 * 32;
-  L.off_arr = (int)off;  // recorded arrivals of split units: 4 entries of 32 bytes
-  off += 4 * 32;
   L.off_mml = (int)off;  // (max, sum) of the token-group warps at a segment end
-  off += align_up((size_t)k.wt * k.rpad * 8, 16);
+  off += align_up((size_t)k.wt * k.rpad * 8, 128);
+  L.q_slot_bytes = k.rpad * d.head_dim * 2;  // a unit's BF16 query rows
+  L.nq = nq;
+  L.off_q = (int)off;
+  off += (size_t)nq * L.q_slot_bytes;
   L.total = (int)(off + 1024);  // slack for aligning the base to 1024 bytes
   return L;
 }
@@ -232,15 +238,21 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   // 8-row warp tiles: at most 168 registers, so three warps share an SM
   // sub-partition's register file) get as many stages as fit 112 KiB (at
   // least 3); the others one CTA per SM and up to 226 KiB.
+  // The Q ring has two slots (the next segment's rows load while the current
+  // one streams) unless that costs the third stage; one slot then.
   const bool two_per_sm = d.head_dim == 128 && k.ncw <= 4;
-  int ns = 0;
+  int ns = 0, nq = 2;
   int budget = kSmemTwoPerSm;
   for (int attempt = two_per_sm ? 0 : 1; attempt < 2 && ns < 3; ++attempt) {
     budget = attempt == 0 ? kSmemTwoPerSm : kSmemOnePerSm;
-    const pa::SmemLayout l0 = smem_layout(d, k, 0, d.sparse_topk > 0 || d.merge_mode == PA_MERGE_CLUSTER);
-    const int stage = l0.stage_bytes + 128 + 16;
-    ns = (budget - l0.total) / stage;
-    if (ns > 8) ns = 8;
+    for (nq = 2; nq >= 1; --nq) {
+      const pa::SmemLayout l0 = smem_layout(d, k, 0, d.sparse_topk > 0 || d.merge_mode == PA_MERGE_CLUSTER, nq);
+      const int stage = l0.stage_bytes + 128 + 16;
+      ns = (budget - l0.total) / stage;
+      if (ns > 8) ns = 8;
+      if (ns >= 3) break;
+    }
+    if (nq < 1) nq = 1;
   }
   if (ns < 2) return fail(PA_ERR_UNSUPPORTED, "shared memory too small for two ring stages");
   // the token-group warps merge their partial states inside one stage buffer
@@ -254,7 +266,7 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   pa_status st = resolve_schedule(d, k, sm_count, ctas_per_sm, sched, merge, P);
   if (st != PA_OK) return st;
   const bool cluster = merge == PA_MERGE_CLUSTER;
-  const pa::SmemLayout L = smem_layout(d, k, ns, cluster);
+  const pa::SmemLayout L = smem_layout(d, k, ns, cluster, nq);
 
   const int units = d.batch * d.num_kv_heads;
   const int G = d.num_q_heads / d.num_kv_heads;
@@ -329,6 +341,7 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   p.sched = sched;
   p.merge = kernel_merge;
   p.C = sched == PA_SCHED_BALANCED ? (int)grid : 0;
+  p.seg_cost = sched == PA_SCHED_BALANCED ? kSegCostChunks : 0;
   p.P = sched == PA_SCHED_PER_UNIT ? P : 0;
   p.TT = k.tt;
   p.NS = ns;
@@ -346,8 +359,10 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   p.off_cpart = L.off_cpart;
   p.off_misc = L.off_misc;
   p.off_pend = L.off_pend;
-  p.off_arr = L.off_arr;
   p.off_mml = L.off_mml;
+  p.off_q = L.off_q;
+  p.q_slot_bytes = L.q_slot_bytes;
+  p.NQ = L.nq;
   return PA_OK;
 }
 

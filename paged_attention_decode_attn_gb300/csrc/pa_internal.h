@@ -45,6 +45,7 @@ struct PaParams {
   // schedule
   int sched, merge;
   int C;   // balanced: CTAs in the grid
+  int seg_cost;  // balanced: virtual chunks charged per unit for its segment overhead
   int P;   // per-unit: partitions per unit
   int TT;  // tokens per stage (= chunk)
   int NS;  // ring stages
@@ -53,12 +54,14 @@ struct PaParams {
   int swz;          // XOR mask of the 128-byte swizzle (7) or 0 (linear rows)
   // dynamic shared memory layout (byte offsets from a 1024-aligned base)
   int off_stage, stage_bytes, off_scale;  // off_scale: within a stage
-  int off_hdr, off_bar, off_merge, off_cpart, off_misc, off_pend, off_arr, off_mml;
+  int off_hdr, off_bar, off_merge, off_cpart, off_misc, off_pend, off_mml;
+  int off_q, q_slot_bytes, NQ;  // Q ring: NQ (1 or 2) slots of Rpad rows x D BF16 values
 };
 
 // Host-visible shared-memory sizing for a kernel configuration.
 struct SmemLayout {
-  int stage_bytes, off_stage, off_scale, off_hdr, off_bar, off_merge, off_cpart, off_misc, off_pend, off_arr, off_mml, total;
+  int stage_bytes, off_stage, off_scale, off_hdr, off_bar, off_merge, off_cpart, off_misc, off_pend, off_mml;
+  int off_q, q_slot_bytes, nq, total;
 };
 
 using KernelFn = void (*)(PaParams, CUtensorMap, CUtensorMap);

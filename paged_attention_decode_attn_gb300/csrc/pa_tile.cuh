@@ -53,8 +53,8 @@ struct alignas(16) StageHdr {
 };
 static_assert(sizeof(StageHdr) == 128, "header size");
 constexpr int kEnd = 1 << 8;
-constexpr int kArrivalsMax = 4;    // split units recorded per CTA (at most 2 in schedule order)
 constexpr int kScanRegs = 8;       // schedule scan in registers for batch <= 256
+constexpr int kMaxTokenWarps = 4;  // token groups per CTA (the plan never makes more)
 
 // ---------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -219,13 +219,21 @@ __device__ __forceinline__ long long sched_start(long long c, long long N, long 
 __device__ __forceinline__ long long sched_owner(long long x, long long N, long long C) {
   return ((x + 1) * C - 1) / N;
 }
-// Total chunk count of the balanced schedule (warp-collective).
+// Weight of sequence b in the balanced schedule: each of its units counts its
+// chunks (at least one) plus seg_cost virtual chunks that stand for the fixed
+// cost of a segment. The virtual chunks come first in the unit's range and
+// carry no work, so a CTA whose range holds many short units gets fewer real
+// chunks.
+__device__ __forceinline__ long long seq_weight(const PaParams& p, int b) {
+  return (long long)p.Hkv * (max(1, unit_range(p, b).n) + p.seg_cost);
+}
+// Total weight of the balanced schedule (warp-collective).
 __device__ __forceinline__ long long balanced_total(const PaParams& p, int lane) {
   long long tot = 0;
   for (int b0 = 0; b0 < p.B; b0 += 32) {
     int b = b0 + lane;
     long long cnt = 0;
-    if (b < p.B) cnt = (long long)p.Hkv * max(1, unit_range(p, b).n);
+    if (b < p.B) cnt = seq_weight(p, b);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
     tot += cnt;
@@ -240,7 +248,7 @@ __device__ __forceinline__ void balanced_find(const PaParams& p, int lane, long 
   for (int b0 = 0; b0 < p.B; b0 += 32) {
     int b = b0 + lane;
     long long cnt = 0;
-    if (b < p.B) cnt = (long long)p.Hkv * max(1, unit_range(p, b).n);
+    if (b < p.B) cnt = seq_weight(p, b);
     long long incl = cnt;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -259,13 +267,16 @@ __device__ __forceinline__ void balanced_find(const PaParams& p, int lane, long 
     base += total;
   }
 }
-// Merge descriptor of a unit in the balanced schedule.
+// Merge descriptor of a unit whose weight range starts at Pu and whose nu real
+// chunks start at Pu + A. CTAs c1..c2 own the real chunks; c1 writes slot
+// 2*c1 + 1 if its range began before Pu (it then holds the previous unit's
+// last chunk), else 2*c1; the others write 2*c.
 struct MergeDesc {
   int nseg, s0, sbase, sstride;
 };
-__device__ __forceinline__ MergeDesc balanced_desc(long long Pu, long long nu, long long N, long long C) {
+__device__ __forceinline__ MergeDesc balanced_desc(long long Pu, long long nu, long long A, long long N, long long C) {
   MergeDesc d;
-  long long c1 = sched_owner(Pu, N, C), c2 = sched_owner(Pu + nu - 1, N, C);
+  long long c1 = sched_owner(Pu + A, N, C), c2 = sched_owner(Pu + A + nu - 1, N, C);
   d.nseg = (int)(c2 - c1 + 1);
   d.s0 = (int)(2 * c1 + (sched_start(c1, N, C) < Pu ? 1 : 0));
   d.sbase = (int)(2 * c1);
@@ -290,6 +301,17 @@ struct Smem {
   __device__ __forceinline__ uint32_t full(int s, const PaParams& p) const { return base_u32 + p.off_bar + 8 * s; }
   __device__ __forceinline__ uint32_t empty(int s, const PaParams& p) const {
     return base_u32 + p.off_bar + 8 * (p.NS + s);
+  }
+  // Q ring: slot i's rows arrive on qfull(i); qempty(i) collects one arrival
+  // per consumer warp once the rows are in registers.
+  __device__ __forceinline__ uint32_t qfull(int i, const PaParams& p) const {
+    return base_u32 + p.off_bar + 16 * p.NS + 8 * i;
+  }
+  __device__ __forceinline__ uint32_t qempty(int i, const PaParams& p) const {
+    return base_u32 + p.off_bar + 16 * p.NS + 16 + 8 * i;
+  }
+  __device__ __forceinline__ uint32_t qbuf(int i, const PaParams& p) const {
+    return base_u32 + p.off_q + i * p.q_slot_bytes;
   }
   __device__ __forceinline__ volatile int* misc(const PaParams& p) const {
     return reinterpret_cast<volatile int*>(base + p.off_misc);
@@ -397,6 +419,9 @@ struct Producer {
   bool ok = true;
   // page-id staging: lane l holds the physical page of logical page pbase + l
   int pid_b = -1, pbase = 0, pid_cur = -1, pid_next = -1, npages_b = 0;
+  // the window a unit's walk began at, kept for the next KV head of the same
+  // sequence (same block-table row, same start)
+  int first_base = 0, first_cur = -1, first_next = -1;
 
   __device__ Producer(const PaParams& p_, const CUtensorMap* k, const CUtensorMap* v, Smem s)
       : p(p_), tmK(k), tmV(v), sm(s), lane(threadIdx.x & 31) {}
@@ -405,24 +430,38 @@ struct Producer {
     if (lp < 0 || lp >= npages_b) return -1;
     return __ldg(p.block_table + (size_t)b * p.maxp + lp);
   }
-  // Physical page of logical page lp0 + lane (lanes < pages in the stage; the
-  // stage's pages lie inside one aligned batch of 32).
-  __device__ __forceinline__ int staged_pages(int b, int L, int lp0, int align) {
+  // Make the batch of 32 page ids holding logical page lp0 current (loads
+  // are issued here and waited for at first use).
+  __device__ __forceinline__ void stage_window(int b, int L, int lp0, int align) {
     if (b != pid_b) {
       pid_b = b;
       npages_b = (L + p.S - 1) / p.S;
       pbase = -(1 << 30);
+      first_base = -(1 << 30);
     }
     if (lp0 < pbase || lp0 >= pbase + 32) {
       if (lp0 >= pbase + 32 && lp0 < pbase + 64) {
         pid_cur = pid_next;
         pbase += 32;
+        pid_next = load_pid(b, pbase + 32 + lane);
+      } else if (lp0 - lp0 % align == first_base) {
+        pbase = first_base;
+        pid_cur = first_cur;
+        pid_next = first_next;
       } else {
         pbase = lp0 - lp0 % align;
         pid_cur = load_pid(b, pbase + lane);
+        pid_next = load_pid(b, pbase + 32 + lane);
+        first_base = pbase;
+        first_cur = pid_cur;
+        first_next = pid_next;
       }
-      pid_next = load_pid(b, pbase + 32 + lane);
     }
+  }
+  // Physical page of logical page lp0 + lane (lanes < pages in the stage; the
+  // stage's pages lie inside one aligned batch of 32).
+  __device__ __forceinline__ int staged_pages(int b, int L, int lp0, int align) {
+    stage_window(b, L, lp0, align);
     return __shfl_sync(0xffffffffu, pid_cur, (lp0 - pbase + lane) & 31);
   }
 
@@ -599,6 +638,31 @@ struct Producer {
     }
   }
 
+  // Query rows of unit (b, g) into Q ring slot nq % NQ: one bulk copy per
+  // query position, since the G heads that share KV head g are contiguous.
+  int nq = 0;
+  __device__ bool load_q(int b, int g) {
+    const int qs = nq % p.NQ;
+    bool got = mbar_wait(sm.qempty(qs, p), ((nq / p.NQ) & 1) ^ 1);
+    got = __all_sync(0xffffffffu, got);
+    if (!got) {
+      ok = false;
+      if (lane == 0) {
+        flag_status(p, kStatusTimeout);
+        sm.misc(p)[0] = 1;
+      }
+      return false;
+    }
+    const uint32_t rowb = (uint32_t)p.G * (uint32_t)p.D * 2u;
+    if (lane == 0) mbar_arrive_tx(sm.qfull(qs, p), rowb * (uint32_t)p.QL);
+    __syncwarp();
+    for (int i = lane; i < p.QL; i += 32)
+      bulk_load(sm.qbuf(qs, p) + (uint32_t)i * rowb, p.q + ((size_t)(b * p.QL + i) * p.Hq + (size_t)g * p.G) * p.D,
+                rowb, sm.qfull(qs, p));
+    ++nq;
+    return true;
+  }
+
   __device__ void emit_end() {
     int s;
     if (!acquire_stage(s)) return;
@@ -624,6 +688,13 @@ struct Producer {
     h.sbase = md.sbase;
     h.sstride = md.sstride;
     const int kend = (k1 > k0) ? k1 : k0 + 1;
+    if (p.topk == 0 && k1 > k0) {
+      // start the first stage's page-id load before the query copy
+      const int tbase = (r.c_lo + k0) * p.TT;
+      const int lp0 = p.S >= p.TT ? tbase / p.S : max(tbase, r.lo) / p.S;
+      stage_window(b, r.L, lp0, p.S < p.TT ? p.TT / p.S : 1);
+    }
+    if (!load_q(b, g)) return;
     for (int k = k0; k < kend && ok; ++k) {
       h.kind_flags = (k == k0 ? kSegFirst : 0) | (k == kend - 1 ? kSegLast : 0) | (whole ? kSegWhole : 0);
       if (k1 > k0) {
@@ -666,7 +737,7 @@ struct Producer {
 #pragma unroll
         for (int i = 0; i < kScanRegs; ++i) {
           const int b = i * 32 + lane;
-          cnt_reg[i] = b < p.B ? (long long)p.Hkv * max(1, unit_range(p, b).n) : 0;
+          cnt_reg[i] = b < p.B ? seq_weight(p, b) : 0;
         }
         long long t = 0;
 #pragma unroll
@@ -681,15 +752,15 @@ struct Producer {
       const long long c = blockIdx.x;
       long long x = c < C ? sched_start(c, N, C) : 0;
       const long long x1 = c < C ? sched_start(c + 1, N, C) : 0;
-      if (x < x1) {
-        int b;
-        long long excl;
+      // sequence holding global chunk xx and the chunk count before it
+      auto locate = [&](long long xx, int& b, long long& excl) {
         if (in_regs) {
           long long base = 0;
           b = p.B;
           excl = 0;
 #pragma unroll
           for (int i = 0; i < kScanRegs; ++i) {
+            if (i * 32 >= p.B) break;
             long long incl = cnt_reg[i];
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -697,7 +768,7 @@ struct Producer {
               if (lane >= off) incl += v;
             }
             const long long total = __shfl_sync(0xffffffffu, incl, 31);
-            const unsigned hit = __ballot_sync(0xffffffffu, base + incl > x);
+            const unsigned hit = __ballot_sync(0xffffffffu, base + incl > xx);
             if (hit && b == p.B) {
               const int first = __ffs(hit) - 1;
               b = i * 32 + first;
@@ -706,32 +777,39 @@ struct Producer {
             base += total;
           }
         } else {
-          balanced_find(p, lane, x, b, excl);
+          balanced_find(p, lane, xx, b, excl);
         }
+      };
+      if (x < x1) {
+        int b;
+        long long excl;
+        locate(x, b, excl);
         UnitRange r = unit_range(p, b);
-        long long nb = max(1, r.n);
-        int g = (int)((x - excl) / nb);
+        long long nb = max(1, r.n), wu = nb + p.seg_cost;
+        int g = (int)((x - excl) / wu);
         while (x < x1 && ok) {
-          const long long Pu = excl + g * nb;
-          const long long kin = x - Pu;
-          const long long take = min(nb - kin, x1 - x);
-          // A unit split over CTAs c1..c2 writes one partial per CTA: slot 2c
-          // for the unit CTA c starts with, 2c + 1 for the one it ends with (a
-          // unit one CTA covers alone is written as output directly).
-          const MergeDesc md = balanced_desc(Pu, nb, N, C);
-          const int slot = (int)(2 * c + ((c == sched_owner(Pu, N, C) && sched_start(c, N, C) < Pu) ? 1 : 0));
-          if (r.n > 0)
-            segment(b, g, r, (int)kin, (int)(kin + take), md.nseg == 1, slot, md);
-          else
-            segment(b, g, r, 0, 0, md.nseg == 1, slot, md);
-          x += take;
+          const long long Pu = excl + g * wu, R0 = Pu + p.seg_cost;
+          const long long lo = max(x, R0), hi = min(x1, R0 + nb);
+          if (lo < hi) {
+            // A unit split over CTAs c1..c2 writes one partial per CTA: slot
+            // 2c for the unit CTA c starts with, 2c + 1 for the one it ends
+            // with (a unit one CTA covers alone is written as output directly).
+            const MergeDesc md = balanced_desc(Pu, nb, p.seg_cost, N, C);
+            const int slot = (int)(2 * c + ((c == sched_owner(R0, N, C) && sched_start(c, N, C) < Pu) ? 1 : 0));
+            if (r.n > 0)
+              segment(b, g, r, (int)(lo - R0), (int)(hi - R0), md.nseg == 1, slot, md);
+            else
+              segment(b, g, r, 0, 0, md.nseg == 1, slot, md);
+          }
+          x = Pu + wu;
           if (++g == p.Hkv) {
             g = 0;
-            excl += (long long)p.Hkv * nb;
+            excl += (long long)p.Hkv * wu;
             ++b;
             if (b < p.B) {
               r = unit_range(p, b);
               nb = max(1, r.n);
+              wu = nb + p.seg_cost;
             }
           }
         }
@@ -742,6 +820,7 @@ struct Producer {
       // Wait (bounded) for copies this warp issued that may still be in flight.
       const int first = max(0, n - p.NS);
       for (int m = first; m < n; ++m) (void)mbar_wait(sm.full(m % p.NS, p), (m / p.NS) & 1);
+      for (int m = max(0, nq - p.NQ); m < nq; ++m) (void)mbar_wait(sm.qfull(m % p.NQ, p), (m / p.NQ) & 1);
     }
   }
 };
@@ -815,16 +894,34 @@ struct Consumer {
 
   __device__ __forceinline__ int row_of(int j, int rho) const { return wr * RW + 8 * j + 2 * t4 + rho; }
 
-  __device__ void begin_segment(int b, int g, int L) {
+  // XOR on the float4 column of row r in the token-group merge buffer. One
+  // 128-bit store instruction covers lanes t4 = 0..3 (rows 2*t4 + rho) and two
+  // g4 values; the XOR sends those eight lanes to eight different 16-byte
+  // bank groups. Readers walk a row's columns in order, so they stay
+  // conflict-free under any XOR below 8.
+  __device__ __forceinline__ static int merge_swz(int r) {
+    const int t = (r >> 1) & 3;
+    return ELT == 1 ? t : ((t & 1) | ((t & 2) << 1));
+  }
+
+  int nq = 0;  // segments begun (Q ring position)
+
+  // Start a segment of unit (b, g): take its query rows from the Q ring.
+  // Returns false if the rows did not arrive in time.
+  __device__ bool begin_segment(int L) {
+    const int qs = nq % p.NQ;
+    bool got = mbar_wait(sm.qfull(qs, p), (nq / p.NQ) & 1);
+    got = __all_sync(0xffffffffu, got);
+    if (!got) return false;
+    ++nq;
     // Q rows of this warp's slice as MMA B fragments (row n = g4), with the
     // head-dim permutation that matches how K rows are read from shared memory.
+    // Slot rows are laid out like the unit's rows of q: row r = i * G + head.
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       const int r = wr * RW + 8 * j + g4;
       const bool valid = r < p.R;
-      const int i = valid ? r / p.G : 0;
-      const int head = g * p.G + (valid ? r % p.G : 0);
-      const uint16_t* qrow = p.q + ((size_t)(b * p.QL + i) * p.Hq + head) * D;
+      const uint32_t qrow = sm.qbuf(qs, p) + (uint32_t)(valid ? r : 0) * (uint32_t)(D * 2);
       float crow_n = 0.f;
       if constexpr (FP8) {
         // 32 values per block: d in [cb*128 + 32*t4, +32)
@@ -834,7 +931,7 @@ struct Consumer {
         for (int cb = 0; cb < NCH; ++cb)
 #pragma unroll
           for (int v = 0; v < 4; ++v)
-            raw[cb][v] = valid ? __ldg(reinterpret_cast<const uint4*>(qrow + cb * 128 + 32 * t4) + v) : make_uint4(0, 0, 0, 0);
+            raw[cb][v] = valid ? lds128(qrow + (uint32_t)(cb * 128 + 32 * t4) * 2u + 16u * v) : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int cb = 0; cb < NCH; ++cb)
 #pragma unroll
@@ -878,7 +975,7 @@ struct Consumer {
         for (int cb = 0; cb < NCH; ++cb)
 #pragma unroll
           for (int v = 0; v < 2; ++v) {
-            const uint4 w = valid ? __ldg(reinterpret_cast<const uint4*>(qrow + cb * 64 + 16 * t4) + v) : make_uint4(0, 0, 0, 0);
+            const uint4 w = valid ? lds128(qrow + (uint32_t)(cb * 64 + 16 * t4) * 2u + 16u * v) : make_uint4(0, 0, 0, 0);
             const int s0 = cb * KS_BLK + 2 * v;
             qf[j][s0][0] = w.x;
             qf[j][s0][1] = w.y;
@@ -903,6 +1000,9 @@ struct Consumer {
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[mt][j][e] = 0.f;
     vexp = -127;
+    __syncwarp();  // every lane has read its rows
+    if (lane == 0) mbar_arrive(sm.qempty(qs, p));
+    return true;
   }
 
   // Does stage row `row` carry a real token (one that some query row may see)?
@@ -1243,30 +1343,49 @@ struct Consumer {
               v[2 * mt] = o[cb * MT_BLK + mt][j][rho] * ounit;
               v[2 * mt + 1] = o[cb * MT_BLK + mt][j][rho + 2] * ounit;
             }
-            float4* dst = reinterpret_cast<float4*>(mb_o + ((size_t)wt * p.Rpad + r) * D + cb * DPB + (DPB / 8) * g4);
+            float4* dst = reinterpret_cast<float4*>(mb_o + ((size_t)wt * p.Rpad + r) * D);
+            const int c0 = (cb * DPB + (DPB / 8) * g4) / 4;
 #pragma unroll
             for (int q4 = 0; q4 < DPB / 32; ++q4)
-              dst[q4] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+              dst[(c0 + q4) ^ merge_swz(r)] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
           }
         }
       named_bar(1, nthr);
       const int E = p.R * (D / 4);
+      // per element, the token groups' shared loads are issued before any is
+      // used; at most kMaxTokenWarps token groups
       for (int e = threadIdx.x; e < E; e += nthr) {
         const int r = e / (D / 4);
         const int d = (e % (D / 4)) * 4;
+        const int c = (e % (D / 4)) ^ merge_swz(r);
+        float2 mlw[kMaxTokenWarps];
+        float4 ow[kMaxTokenWarps];
+#pragma unroll
+        for (int w = 0; w < kMaxTokenWarps; ++w) {
+          if (w < p.Wt) {
+            mlw[w] = *reinterpret_cast<const float2*>(mb_ml + ((size_t)w * p.Rpad + r) * 2);
+            ow[w] = reinterpret_cast<const float4*>(mb_o + ((size_t)w * p.Rpad + r) * D)[c];
+          } else {
+            mlw[w] = make_float2(-INFINITY, 0.f);
+            ow[w] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
         float M = -INFINITY;
-        for (int w = 0; w < p.Wt; ++w) M = fmaxf(M, mb_ml[((size_t)w * p.Rpad + r) * 2]);
+#pragma unroll
+        for (int w = 0; w < kMaxTokenWarps; ++w) M = fmaxf(M, mlw[w].x);
         float L = 0.f;
         float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
         if (M != -INFINITY) {
-          for (int w = 0; w < p.Wt; ++w) {
-            const float a = ex2(mb_ml[((size_t)w * p.Rpad + r) * 2] - M);
-            const float4 ow = *reinterpret_cast<const float4*>(mb_o + ((size_t)w * p.Rpad + r) * D + d);
-            L = fmaf(mb_ml[((size_t)w * p.Rpad + r) * 2 + 1], a, L);
-            O.x = fmaf(ow.x, a, O.x);
-            O.y = fmaf(ow.y, a, O.y);
-            O.z = fmaf(ow.z, a, O.z);
-            O.w = fmaf(ow.w, a, O.w);
+#pragma unroll
+          for (int w = 0; w < kMaxTokenWarps; ++w) {
+            if (w < p.Wt) {
+              const float a = ex2(mlw[w].x - M);
+              L = fmaf(mlw[w].y, a, L);
+              O.x = fmaf(ow[w].x, a, O.x);
+              O.y = fmaf(ow[w].y, a, O.y);
+              O.z = fmaf(ow[w].z, a, O.z);
+              O.w = fmaf(ow[w].w, a, O.w);
+            }
           }
         }
         if (whole) {
@@ -1287,24 +1406,18 @@ struct Consumer {
       if (lane == 0) mbar_arrive(sm.empty(s, p));
     }
     if (whole || cluster) return;
-    if (threadIdx.x == 0) {
-      if (p.merge == kMergeReducer) {
-        if (slot == md.s0) p.unit_desc[h.unit] = make_int4(md.nseg, md.s0, md.sbase, md.sstride);
-      } else if (p.merge == kMergeLastArriver) {
-        // arrivals are made after the stream, behind one fence for all partials
-        volatile int* nrec = sm.misc(p) + 3;
-        const int k = *nrec;
-        // A CTA splits at most its first and last unit (one segment per CTA
-        // in the per-unit schedule), so the record list cannot overflow.
-        if (k < kArrivalsMax) {
-          int4* e = reinterpret_cast<int4*>(sm.base + p.off_arr) + 2 * k;
-          e[0] = make_int4(h.b, h.g, h.unit, md.nseg);
-          e[1] = make_int4(md.s0, md.sbase, md.sstride, 0);
-          *nrec = k + 1;
-        } else {
-          flag_status(p, kStatusInternal);
-        }
-      }
+    if (p.merge == kMergeReducer) {
+      if (threadIdx.x == 0 && slot == md.s0) p.unit_desc[h.unit] = make_int4(md.nseg, md.s0, md.sbase, md.sstride);
+    } else if (p.merge == kMergeLastArriver) {
+      // Publish the partial, count it, and merge the unit here if this was
+      // its last partial. A CTA has at most two split segments: its first
+      // (the end of a unit others began) and its last (the start of a unit
+      // others finish), so it runs at most one merge in mid-stream.
+      __threadfence();
+      named_bar(1, nthr);
+      if (threadIdx.x == 0) arrive(h.b, h.g, h.unit, md);
+      named_bar(1, nthr);
+      run_queue(nthr);
     }
   }
 
@@ -1345,24 +1458,6 @@ struct Consumer {
     named_bar(1, nthr);
     if (threadIdx.x == 0) *(sm.misc(p) + 2) = 0;
     named_bar(1, nthr);
-  }
-
-  // After the stream: one fence for this CTA's partials, the recorded
-  // arrivals, then the merges this CTA turned out to be last for.
-  __device__ void finish_last_arriver() {
-    const int nthr = p.NCW * 32;
-    __threadfence();
-    named_bar(1, nthr);
-    if (threadIdx.x == 0) {
-      const int n = *(sm.misc(p) + 3);
-      for (int k = 0; k < n; ++k) {
-        const int4* e = reinterpret_cast<const int4*>(sm.base + p.off_arr) + 2 * k;
-        const int4 a = e[0], c = e[1];
-        arrive(a.x, a.y, a.z, MergeDesc{a.w, c.x, c.y, c.z});
-      }
-    }
-    named_bar(1, nthr);
-    run_queue(nthr);
   }
 
   __device__ void run() {
@@ -1407,7 +1502,13 @@ struct Consumer {
         slot = h3.x;
         md = MergeDesc{h3.y, h3.z, h3.w, sstride};
       }
-      if (h.flags & kSegFirst) begin_segment(h.b, h.g, h.L);
+      if ((h.flags & kSegFirst) && !begin_segment(h.L)) {
+        if (lane == 0) {
+          flag_status(p, kStatusTimeout);
+          sm.misc(p)[0] |= 1;
+        }
+        break;
+      }
       const uint32_t kst = sm.stage(s, p);
       const uint32_t vst = kst + (uint32_t)p.TT * 128u * NCH;
       const uint32_t sst = kst + p.off_scale;
@@ -1482,6 +1583,10 @@ __global__ void __launch_bounds__(MAXW * 32, (D == 128 && MAXW == 5) ? 2 : 1) pa
       mbar_init(sm.full(s, p), 1);
       mbar_init(sm.empty(s, p), p.NCW);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(sm.qfull(i, p), 1);
+      mbar_init(sm.qempty(i, p), p.NCW);
+    }
     for (int i = 0; i < 16; ++i) sm.misc(p)[i] = 0;
     fence_barrier_init();
   }
@@ -1498,7 +1603,6 @@ __global__ void __launch_bounds__(MAXW * 32, (D == 128 && MAXW == 5) ? 2 : 1) pa
   } else {
     Consumer<FP8, D, NT, VTOK, TW> cons(p, sm);
     cons.run();
-    if (p.merge == kMergeLastArriver) cons.finish_last_arriver();
     if (p.merge == kMergeCluster) {
       cluster_sync_all();
       cons.cluster_merge(blockIdx.x / p.P, threadIdx.x, p.NCW * 32);

@@ -30,12 +30,13 @@ def kernel_shape(d):
                 tt=tt, tw=tw, bh=min(d["page_size"], tt))
 
 
-def smem_total(d, k, ns, cluster):
+def smem_total(d, k, ns, cluster, nq):
     stage = 2 * k["tt"] * k["rb"] + (1024 if d["scale_mode"] == 2 else 0)
     off = ns * stage
     if cluster:
         off += align(k["rpad"] * d["head_dim"] * 4 + k["rpad"] * 8, 128)
-    off += ns * 128 + ns * 16 + 64 + 8 * 32 + 4 * 32 + align(k["wt"] * k["rpad"] * 8, 16)
+    off += ns * 128 + ns * 16 + 32 + 64 + 8 * 32 + align(k["wt"] * k["rpad"] * 8, 128)
+    off += nq * k["rpad"] * d["head_dim"] * 2  # Q ring: nq slots of BF16 query rows
     return stage, off + 1024
 
 
@@ -49,8 +50,11 @@ def plan(d):
         if ns >= 3:
             break
         budget = SMEM_TWO if attempt == 0 else SMEM_ONE
-        stage, total0 = smem_total(d, k, 0, cl0)
-        ns = min(8, (budget - total0) // (stage + 144))
+        for nq in (2, 1):
+            stage, total0 = smem_total(d, k, 0, cl0, nq)
+            ns = min(8, (budget - total0) // (stage + 144))
+            if ns >= 3:
+                break
     assert ns >= 2
     sm, cps = d["sm_count_override"], d["ctas_per_sm_override"]
     units = d["batch"] * d["num_kv_heads"]
@@ -78,7 +82,7 @@ def plan(d):
     if sched == 2 and P == 1:
         merge = 1
     cluster = merge == 2
-    _, smem = smem_total(d, k, ns, cluster)
+    _, smem = smem_total(d, k, ns, cluster, nq)
     grid = sm * cps if sched == 1 else units * P
     if units == 0:
         grid = 0
