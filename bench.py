@@ -205,6 +205,7 @@ WORKLOADS = {
 SEQ_LEN = {"dense": "U[1024,8192]", "tiny": "{37,100}", "d256": "{0, 8K+tail, 128K+tail}",
            "sparse": "2048 of 131072", "mtp4": "U[4096,65536]"}
 MERGES = {"auto": 0, "direct": 1, "cluster": 2, "last-arriver": 3, "reducer": 4}
+CONSUMERS = {"auto": 0, "tile": 1, "tmem": 2}
 
 
 def make_workload(args, rank):
@@ -264,6 +265,8 @@ def main():
     ap.add_argument("--sinks", action="store_true", help="d256: per-head sink logits")
     ap.add_argument("--partitions", type=int, default=0, help="plan max_partitions (per-unit schedule)")
     ap.add_argument("--merge", default="auto", choices=sorted(MERGES), help="plan merge mode")
+    ap.add_argument("--consumer", default="auto", choices=sorted(CONSUMERS),
+                    help="stage consumer: auto, tile (mma.sync) or tmem (tcgen05, 17..64 rows)")
     args = ap.parse_args()
     args.steps_ref = max(1, min(args.steps, 5))
     args.warmup_ref = 1 if args.warmup > 0 else 0
@@ -304,6 +307,7 @@ def main():
     if args.partitions:
         fields.update(schedule=pa.PA_SCHED_PER_UNIT, max_partitions=args.partitions)
     fields["merge_mode"] = MERGES[args.merge]
+    fields["consumer"] = CONSUMERS[args.consumer]
     plan = pa.Plan(device=dev, **fields)
     stream = torch.cuda.current_stream(dev)
     flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
@@ -382,7 +386,7 @@ def main():
                        "window": int(w.window), "sinks": w.sinks is not None,
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "l2": "512 MiB read-only pass before every timed call (dense: inputs also larger than L2)",
-                       "plan": {k: plan.info[k] for k in ("schedule", "merge_mode", "num_partitions", "grid",
+                       "plan": {k: plan.info[k] for k in ("schedule", "merge_mode", "consumer", "num_partitions", "grid",
                                                          "block_threads", "num_stages", "stage_tokens",
                                                          "ctas_per_sm", "launches_per_call")}},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

@@ -97,6 +97,13 @@ enum {
   PA_MERGE_REDUCER = 4       /* a second kernel merges the partials */
 };
 
+/* How a stage is consumed. The tile consumer runs mma.sync per 8-row warp
+ * (any shape); the tensor-memory consumer runs tcgen05.mma with accumulators
+ * in TMEM on one 64-row block (dense decode with 17..64 rows per KV head,
+ * FP8 head_dim 128/256 or BF16 head_dim 128). AUTO picks the faster one for
+ * the shape. */
+enum { PA_CONSUMER_AUTO = 0, PA_CONSUMER_TILE = 1, PA_CONSUMER_TMEM = 2 };
+
 /* How KV chunks are assigned to CTAs. */
 enum {
   PA_SCHED_AUTO = 0,
@@ -126,6 +133,7 @@ typedef struct pa_plan_desc {
   int sm_count_override; /* 0 => device attribute (tests: simulated SM counts) */
   int ctas_per_sm_override; /* 0 => occupancy query */
   int device;            /* CUDA device ordinal the plan is for */
+  int consumer;          /* PA_CONSUMER_*; TMEM on an unsupported shape is PA_ERR_UNSUPPORTED */
 } pa_plan_desc;
 
 typedef struct pa_plan_info {
@@ -145,6 +153,7 @@ typedef struct pa_plan_info {
   int sm_count;
   int launches_per_call;
   int units;           /* batch * num_kv_heads */
+  int consumer;        /* resolved PA_CONSUMER_* */
   size_t smem_bytes;   /* dynamic shared memory of the tile kernel */
   size_t workspace_bytes;
   size_t partial_slots;

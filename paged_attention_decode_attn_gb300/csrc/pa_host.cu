@@ -66,8 +66,23 @@ constexpr int kSmemOnePerSm = 226 * 1024;
 
 struct KernelShape {
   int nt, rw, wr, wt, ncw, rpad, elt, rb, nch, tt, tw, bh;
-  bool vtok;
+  bool vtok, umma;
 };
+
+// Groups of more than 16 query rows per KV head (MTP verify, wide GQA) on
+// dense decode run the tensor-memory (tcgen05) consumer: four warps, one
+// 64-row MMA block.
+bool umma_supported(const pa_plan_desc& d, int R) {
+  if (d.sparse_topk > 0 || R <= 16) return false;
+  if (d.kv_dtype == PA_KV_FP8_E4M3) return d.head_dim == 128 || d.head_dim == 256;
+  return d.head_dim == 128;
+}
+// AUTO keeps the tile consumer: on the measured shapes (GQA16 x MTP4, D256 x
+// MTP3-4) it is still the faster of the two.
+bool use_umma(const pa_plan_desc& d, int R) {
+  return d.consumer == PA_CONSUMER_TMEM && umma_supported(d, R);
+}
+constexpr int kUmmaRows = 64;
 
 KernelShape kernel_shape(const pa_plan_desc& d) {
   KernelShape k;
@@ -91,6 +106,16 @@ KernelShape kernel_shape(const pa_plan_desc& d) {
   k.tw = (d.kv_dtype == PA_KV_FP8_E4M3 && d.head_dim == 128) ? 2 : 1;
   k.bh = d.page_size < k.tt ? d.page_size : k.tt;
   k.vtok = d.kv_dtype == PA_KV_FP8_E4M3 && d.scale_mode == PA_SCALE_PER_TOKEN;
+  k.umma = use_umma(d, R);
+  if (k.umma) {
+    // rows 16*w .. 16*w + 15 belong to consumer warp w (M = 64 TMEM layout)
+    k.nt = 2;
+    k.rw = 16;
+    k.wr = 4;
+    k.wt = 1;
+    k.ncw = 4;
+    k.rpad = (R + 7) / 8 * 8;
+  }
   return k;
 }
 
@@ -101,6 +126,22 @@ pa::SmemLayout smem_layout(const pa_plan_desc& d, const KernelShape& k, int ns, 
   L.off_scale = 2 * k.tt * k.rb;
   L.off_stage = 0;
   size_t off = (size_t)ns * L.stage_bytes;
+  L.off_k16 = L.off_v16 = L.off_q16 = L.off_p16 = 0;
+  if (k.umma) {
+    // 1024-aligned 16-bit operands (stage_bytes is a multiple of 1024)
+    if (d.kv_dtype == PA_KV_FP8_E4M3) {
+      L.off_k16 = (int)off;
+      off += (size_t)k.tt * d.head_dim * 2;
+      L.off_v16 = (int)off;
+      off += (size_t)k.tt * d.head_dim * 2;
+    }
+    L.off_q16 = (int)off;
+    off += (size_t)kUmmaRows * d.head_dim * 2;
+    // P^T ([tokens][64 rows]), its unscaled copy under per-token V scales,
+    // then a 16 x tokens operand of ones for the row sums
+    L.off_p16 = (int)off;
+    off += (size_t)(k.vtok ? 2 : 1) * k.tt * kUmmaRows * 2 + (size_t)16 * k.tt * 2;
+  }
   L.off_merge = (int)off;
   L.off_cpart = (int)off;  // cluster merge: this CTA's partial (O, then max/sum)
   if (cluster) off += align_up((size_t)k.rpad * d.head_dim * 4 + (size_t)k.rpad * 8, 128);
@@ -108,6 +149,13 @@ pa::SmemLayout smem_layout(const pa_plan_desc& d, const KernelShape& k, int ns, 
   off += (size_t)ns * 128;
   L.off_bar = (int)off;
   off += (size_t)ns * 16 + 32;  // full/empty per stage, then full/empty per Q slot
+  L.off_ubar = (int)off;  // tcgen05 commit barriers (S, O)
+  off += 16;
+  L.off_tslot = (int)off;  // tensor-memory address written by tcgen05.alloc
+  off += 16;
+  L.off_rows = (int)off;  // tcgen05 consumer: per-row state (8 x 64 words) and 4 flags
+  off += k.umma ? (size_t)(8 * kUmmaRows + 4) * 4 : 0;
+  off = align_up(off, 16);
   L.off_misc = (int)off;
   off += 64;
   L.off_pend = (int)off;  // queued last-arriver merges: 8 entries of 32 bytes
@@ -123,6 +171,7 @@ pa::SmemLayout smem_layout(const pa_plan_desc& d, const KernelShape& k, int ns, 
 }
 
 const void* pick_tile_kernel(const pa_plan_desc& d, const KernelShape& k) {
+  if (k.umma) return pa::umma_kernel(d.kv_dtype == PA_KV_FP8_E4M3, d.head_dim, k.vtok);
   if (d.kv_dtype == PA_KV_FP8_E4M3) {
     if (d.head_dim == 128) return pa::tile_kernel_fp8_d128(k.vtok, k.ncw > 4);
     return k.ncw > 4 ? nullptr : pa::tile_kernel_fp8_d256(k.vtok);
@@ -170,6 +219,13 @@ pa_status validate_desc(const pa_plan_desc& d) {
     return fail(PA_ERR_INVALID_ARG, "unknown merge_mode %d", d.merge_mode);
   if (d.schedule < PA_SCHED_AUTO || d.schedule > PA_SCHED_PER_UNIT)
     return fail(PA_ERR_INVALID_ARG, "unknown schedule %d", d.schedule);
+  if (d.consumer < PA_CONSUMER_AUTO || d.consumer > PA_CONSUMER_TMEM)
+    return fail(PA_ERR_INVALID_ARG, "consumer must be PA_CONSUMER_* (got %d)", d.consumer);
+  if (d.consumer == PA_CONSUMER_TMEM &&
+      !umma_supported(d, d.query_len * (d.num_kv_heads > 0 ? d.num_q_heads / d.num_kv_heads : 0)))
+    return fail(PA_ERR_UNSUPPORTED,
+                "the tensor-memory consumer needs dense decode, 17..64 rows per KV head, FP8 head_dim 128/256 or "
+                "BF16 head_dim 128");
   if (d.sm_count_override < 0 || d.ctas_per_sm_override < 0)
     return fail(PA_ERR_INVALID_ARG, "overrides must be >= 0");
   return PA_OK;
@@ -240,7 +296,7 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   // least 3); the others one CTA per SM and up to 226 KiB.
   // The Q ring has two slots (the next segment's rows load while the current
   // one streams) unless that costs the third stage; one slot then.
-  const bool two_per_sm = d.head_dim == 128 && k.ncw <= 4;
+  const bool two_per_sm = !k.umma && d.head_dim == 128 && k.ncw <= 4;
   int ns = 0, nq = 2;
   int budget = kSmemTwoPerSm;
   for (int attempt = two_per_sm ? 0 : 1; attempt < 2 && ns < 3; ++attempt) {
@@ -314,6 +370,7 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   in.sm_count = sm_count;
   in.launches_per_call = merge == PA_MERGE_REDUCER ? 2 : 1;
   in.units = units;
+  in.consumer = k.umma ? PA_CONSUMER_TMEM : PA_CONSUMER_TILE;
   in.smem_bytes = (size_t)L.total;
   in.workspace_bytes = off;
   in.partial_slots = slots;
@@ -361,6 +418,13 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   p.off_pend = L.off_pend;
   p.off_mml = L.off_mml;
   p.off_q = L.off_q;
+  p.off_k16 = L.off_k16;
+  p.off_v16 = L.off_v16;
+  p.off_q16 = L.off_q16;
+  p.off_p16 = L.off_p16;
+  p.off_ubar = L.off_ubar;
+  p.off_tslot = L.off_tslot;
+  p.off_rows = L.off_rows;
   p.q_slot_bytes = L.q_slot_bytes;
   p.NQ = L.nq;
   return PA_OK;

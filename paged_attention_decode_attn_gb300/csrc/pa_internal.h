@@ -56,12 +56,15 @@ struct PaParams {
   int off_stage, stage_bytes, off_scale;  // off_scale: within a stage
   int off_hdr, off_bar, off_merge, off_cpart, off_misc, off_pend, off_mml;
   int off_q, q_slot_bytes, NQ;  // Q ring: NQ (1 or 2) slots of Rpad rows x D BF16 values
+  // tcgen05 consumer: 16-bit K and V operands (FP8 caches), Q and P operands,
+  // the two MMA commit barriers, and the tensor-memory address slot
+  int off_k16, off_v16, off_q16, off_p16, off_ubar, off_tslot, off_rows;
 };
 
 // Host-visible shared-memory sizing for a kernel configuration.
 struct SmemLayout {
   int stage_bytes, off_stage, off_scale, off_hdr, off_bar, off_merge, off_cpart, off_misc, off_pend, off_mml;
-  int off_q, q_slot_bytes, nq, total;
+  int off_q, q_slot_bytes, nq, off_k16, off_v16, off_q16, off_p16, off_ubar, off_tslot, off_rows, total;
 };
 
 using KernelFn = void (*)(PaParams, CUtensorMap, CUtensorMap);
@@ -72,6 +75,8 @@ const void* tile_kernel_fp8_d128(int vtok, int wide);
 const void* tile_kernel_fp8_d256(int vtok);
 const void* tile_kernel_bf16(int d, int wide);
 const void* reduce_kernel(int d);
+// tcgen05 consumer instantiations (FP8 head_dim 128/256, BF16 head_dim 128).
+const void* umma_kernel(int fp8, int d, int vtok);
 
 }  // namespace pa
 

@@ -825,6 +825,82 @@ struct Producer {
   }
 };
 
+// ------------------------------------------------------------ unit merges
+// Count one partial of a split unit; the last of its nseg partials queues
+// the unit's merge for this CTA (thread 0 only).
+__device__ __forceinline__ void la_arrive(const PaParams& p, Smem sm, int b, int g, int unit, const MergeDesc& md) {
+  int* cnt = p.counters + (size_t)unit * kCounterStride;
+  const int prev = atomicAdd(cnt, 1);
+  if (prev != md.nseg - 1) return;
+  atomicExch(cnt, 0);
+  volatile int* npend = sm.misc(p) + 2;
+  const int idx = *npend;
+  int4* q = reinterpret_cast<int4*>(sm.base + p.off_pend) + 2 * idx;
+  q[0] = make_int4(b, g, unit, md.nseg);
+  q[1] = make_int4(md.s0, md.sbase, md.sstride, 0);
+  *npend = idx + 1;
+}
+
+// Run and clear the queued merges with the nthr consumer threads (named
+// barrier 1).
+template <int D>
+__device__ void la_run_queue(const PaParams& p, Smem sm, float vscale, int nthr) {
+  const int cnt = *(sm.misc(p) + 2);
+  if (cnt == 0) return;
+  __threadfence();
+  for (int i = 0; i < cnt; ++i) {
+    const int4* q = reinterpret_cast<const int4*>(sm.base + p.off_pend) + 2 * i;
+    const int4 a = q[0], c = q[1];
+    const MergeDesc md{a.w, c.x, c.y, c.z};
+    merge_elems<D>(
+        p, vscale, md.nseg, a.x, a.y, threadIdx.x, nthr, 0, p.R * (D / 4),
+        [&](int k, int r) {
+          return __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((size_t)merge_slot(md, k) * p.Rpad + r) * 2));
+        },
+        [&](int k, int r, int d) {
+          return __ldcg(
+              reinterpret_cast<const float4*>(p.part_o + ((size_t)merge_slot(md, k) * p.Rpad + r) * D + d));
+        });
+  }
+  named_bar(1, nthr);
+  if (threadIdx.x == 0) *(sm.misc(p) + 2) = 0;
+  named_bar(1, nthr);
+}
+
+// Cluster merge: CTA `rank` merges its share of the unit's output elements
+// from the partials of all P CTAs (partition order), read over distributed
+// shared memory.
+template <int D>
+__device__ void cluster_merge_unit(const PaParams& p, Smem sm, float vscale, int unit, int tid, int nthr) {
+  const int b = unit / p.Hkv, g = unit % p.Hkv;
+  uint32_t rank;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  const int E = p.R * (D / 4);
+  const int e0 = (int)((long long)rank * E / p.P), e1 = (int)((long long)(rank + 1) * E / p.P);
+  const uint32_t cp_local = sm.base_u32 + p.off_cpart;
+  const uint32_t ml_off = (uint32_t)p.Rpad * D * 4u;
+  merge_elems<D>(
+      p, vscale, p.P, b, g, tid, nthr, e0, e1,
+      [&](int k, int r) {
+        uint32_t remote;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(cp_local + ml_off + 8u * r), "r"(k));
+        float2 v;
+        asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(remote));
+        return v;
+      },
+      [&](int k, int r, int d) {
+        uint32_t remote;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                     : "=r"(remote)
+                     : "r"(cp_local + 4u * (uint32_t)(r * D + d)), "r"(k));
+        float4 v;
+        asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                     : "r"(remote));
+        return v;
+      });
+}
+
 // ================================================================ consumers
 // Per-stage header fields every consumer warp needs. The sparse validity
 // words are separate scalars (selected by comparison, never indexed with a
@@ -1421,44 +1497,9 @@ struct Consumer {
     }
   }
 
-  // Count one partial of a split unit; the last of its nseg partials queues
-  // the unit's merge for this CTA (thread 0 only).
-  __device__ void arrive(int b, int g, int unit, const MergeDesc& md) {
-    int* cnt = p.counters + (size_t)unit * kCounterStride;
-    const int prev = atomicAdd(cnt, 1);
-    if (prev != md.nseg - 1) return;
-    atomicExch(cnt, 0);
-    volatile int* npend = sm.misc(p) + 2;
-    const int idx = *npend;
-    int4* q = reinterpret_cast<int4*>(sm.base + p.off_pend) + 2 * idx;
-    q[0] = make_int4(b, g, unit, md.nseg);
-    q[1] = make_int4(md.s0, md.sbase, md.sstride, 0);
-    *npend = idx + 1;
-  }
-
-  // Run and clear the queued merges with all consumer threads.
-  __device__ void run_queue(int nthr) {
-    const int cnt = *(sm.misc(p) + 2);
-    if (cnt == 0) return;
-    __threadfence();
-    for (int i = 0; i < cnt; ++i) {
-      const int4* q = reinterpret_cast<const int4*>(sm.base + p.off_pend) + 2 * i;
-      const int4 a = q[0], c = q[1];
-      const MergeDesc md{a.w, c.x, c.y, c.z};
-      merge_elems<D>(
-          p, vscale, md.nseg, a.x, a.y, threadIdx.x, nthr, 0, p.R * (D / 4),
-          [&](int k, int r) {
-            return __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((size_t)merge_slot(md, k) * p.Rpad + r) * 2));
-          },
-          [&](int k, int r, int d) {
-            return __ldcg(
-                reinterpret_cast<const float4*>(p.part_o + ((size_t)merge_slot(md, k) * p.Rpad + r) * D + d));
-          });
-    }
-    named_bar(1, nthr);
-    if (threadIdx.x == 0) *(sm.misc(p) + 2) = 0;
-    named_bar(1, nthr);
-  }
+  __device__ void arrive(int b, int g, int unit, const MergeDesc& md) { la_arrive(p, sm, b, g, unit, md); }
+  __device__ void run_queue(int nthr) { la_run_queue<D>(p, sm, vscale, nthr); }
+  __device__ void cluster_merge(int unit, int tid, int nthr) { cluster_merge_unit<D>(p, sm, vscale, unit, tid, nthr); }
 
   __device__ void run() {
     int n = 0;
@@ -1524,38 +1565,6 @@ struct Consumer {
     }
   }
 
-  // Cluster merge: CTA `rank` merges its share of the unit's output elements
-  // from the partials of all P CTAs (partition order), read over distributed
-  // shared memory.
-  __device__ void cluster_merge(int unit, int tid, int nthr) {
-    const int b = unit / p.Hkv, g = unit % p.Hkv;
-    uint32_t rank;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
-    const int E = p.R * (D / 4);
-    const int e0 = (int)((long long)rank * E / p.P), e1 = (int)((long long)(rank + 1) * E / p.P);
-    const uint32_t cp_local = sm.base_u32 + p.off_cpart;
-    const uint32_t ml_off = (uint32_t)p.Rpad * D * 4u;
-    merge_elems<D>(
-        p, vscale, p.P, b, g, tid, nthr, e0, e1,
-        [&](int k, int r) {
-          uint32_t remote;
-          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(cp_local + ml_off + 8u * r), "r"(k));
-          float2 v;
-          asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(remote));
-          return v;
-        },
-        [&](int k, int r, int d) {
-          uint32_t remote;
-          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-                       : "=r"(remote)
-                       : "r"(cp_local + 4u * (uint32_t)(r * D + d)), "r"(k));
-          float4 v;
-          asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                       : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                       : "r"(remote));
-          return v;
-        });
-  }
 };
 
 __device__ __forceinline__ void cluster_sync_all() {

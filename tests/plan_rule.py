@@ -26,16 +26,30 @@ def kernel_shape(d):
     rb = d["head_dim"] * elt
     tt = min(128, max(16, 32768 // (2 * rb)))
     tw = 2 if (d["kv_dtype"] == 0 and d["head_dim"] == 128) else 1
-    return dict(R=R, G=G, nt=nt, rw=rw, wr=wr, wt=wt, ncw=wr * wt, rpad=wr * rw, elt=elt, rb=rb,
-                tt=tt, tw=tw, bh=min(d["page_size"], tt))
+    k = dict(R=R, G=G, nt=nt, rw=rw, wr=wr, wt=wt, ncw=wr * wt, rpad=wr * rw, elt=elt, rb=rb,
+             tt=tt, tw=tw, bh=min(d["page_size"], tt), umma=False)
+    # more than 16 rows on dense decode: the tcgen05 consumer (4 warps of 16 rows)
+    if d.get("consumer", 0) == 2 and d.get("sparse_topk", 0) == 0 and R > 16 and (
+            d["head_dim"] == 128 or (d["kv_dtype"] == 0 and d["head_dim"] == 256)):
+        k.update(umma=True, nt=2, rw=16, wr=4, wt=1, ncw=4, rpad=-(-R // 8) * 8)
+    return k
 
 
 def smem_total(d, k, ns, cluster, nq):
     stage = 2 * k["tt"] * k["rb"] + (1024 if d["scale_mode"] == 2 else 0)
     off = ns * stage
+    if k["umma"]:
+        if d["kv_dtype"] == 0:
+            off += 2 * k["tt"] * d["head_dim"] * 2  # 16-bit K and V operands
+        off += 64 * d["head_dim"] * 2  # Q operand (64 rows)
+        vtok = d["kv_dtype"] == 0 and d["scale_mode"] == 2
+        off += (2 if vtok else 1) * k["tt"] * 64 * 2 + 16 * k["tt"] * 2  # P^T (+ unscaled), ones
     if cluster:
         off += align(k["rpad"] * d["head_dim"] * 4 + k["rpad"] * 8, 128)
-    off += ns * 128 + ns * 16 + 32 + 64 + 8 * 32 + align(k["wt"] * k["rpad"] * 8, 128)
+    off += ns * 128 + ns * 16 + 32 + 32
+    if k["umma"]:
+        off = align(off + (8 * 64 + 4) * 4, 16)  # per-row state
+    off += 64 + 8 * 32 + align(k["wt"] * k["rpad"] * 8, 128)
     off += nq * k["rpad"] * d["head_dim"] * 2  # Q ring: nq slots of BF16 query rows
     return stage, off + 1024
 
@@ -43,7 +57,7 @@ def smem_total(d, k, ns, cluster, nq):
 def plan(d):
     """Expected pa_plan_info fields for a descriptor dict with overrides set."""
     k = kernel_shape(d)
-    two = d["head_dim"] == 128 and k["ncw"] <= 4
+    two = not k["umma"] and d["head_dim"] == 128 and k["ncw"] <= 4
     ns, budget = 0, SMEM_TWO
     cl0 = d.get("sparse_topk", 0) > 0 or d.get("merge_mode", 0) == 2
     for attempt in range(0 if two else 1, 2):
@@ -104,5 +118,6 @@ def plan(d):
                 stage_tokens=k["tt"], num_stages=ns, rows=k["R"], rows_per_warp=k["rw"],
                 row_warps=k["wr"], token_warps=k["wt"], block_threads=(k["ncw"] + 1) * 32,
                 grid=grid, cluster=P if cluster else 1, ctas_per_sm=cps, sm_count=sm,
-                launches_per_call=2 if merge == 4 else 1, units=units, smem_bytes=smem,
+                launches_per_call=2 if merge == 4 else 1, units=units, consumer=2 if k["umma"] else 1,
+                smem_bytes=smem,
                 workspace_bytes=off, partial_slots=slots, status_offset=status)

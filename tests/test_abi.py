@@ -81,6 +81,16 @@ PLAN_CASES = [
     desc(batch=5, num_q_heads=12, num_kv_heads=1, query_len=5, schedule=pa.PA_SCHED_PER_UNIT,
          max_partitions=3, merge_mode=pa.PA_MERGE_LAST_ARRIVER),
     desc(batch=241, num_q_heads=16, num_kv_heads=1, sparse_topk=2048, sm_count_override=256),
+    desc(batch=4, num_q_heads=64, num_kv_heads=4, query_len=4, page_size=128, schedule=pa.PA_SCHED_PER_UNIT,
+         max_partitions=4, merge_mode=pa.PA_MERGE_CLUSTER, consumer=pa.PA_CONSUMER_TMEM),
+    desc(batch=16, num_q_heads=16, num_kv_heads=2, head_dim=256, page_size=64, scale_mode=2, query_len=4,
+         merge_mode=pa.PA_MERGE_REDUCER, consumer=pa.PA_CONSUMER_TMEM),
+    desc(batch=16, num_q_heads=16, num_kv_heads=2, head_dim=256, page_size=64, scale_mode=2, query_len=3,
+         consumer=pa.PA_CONSUMER_TMEM),
+    desc(batch=32, num_q_heads=64, num_kv_heads=4, query_len=4, page_size=128, consumer=pa.PA_CONSUMER_TMEM),
+    desc(batch=32, num_q_heads=64, num_kv_heads=4, query_len=4, page_size=128, kv_dtype=1, scale_mode=0,
+         consumer=pa.PA_CONSUMER_TMEM),
+    desc(num_q_heads=24, num_kv_heads=8, query_len=4, kv_dtype=1, scale_mode=0, consumer=pa.PA_CONSUMER_TILE),
 ]
 
 
@@ -114,6 +124,9 @@ BAD = [
     (dict(num_pages=2 ** 30), pa.PA_ERR_UNSUPPORTED),
     (dict(max_partitions=300), pa.PA_ERR_INVALID_ARG),
     (dict(head_dim=256, num_q_heads=64, num_kv_heads=1), pa.PA_ERR_UNSUPPORTED),
+    (dict(consumer=3), pa.PA_ERR_INVALID_ARG),
+    (dict(consumer=pa.PA_CONSUMER_TMEM), pa.PA_ERR_UNSUPPORTED),  # 8 rows: tile consumer only
+    (dict(consumer=pa.PA_CONSUMER_TMEM, num_q_heads=64, num_kv_heads=4, sparse_topk=64), pa.PA_ERR_UNSUPPORTED),
 ]
 
 

@@ -58,11 +58,12 @@ def test_dense_full(orc):
     check(orc, w, gpu, 40, include=(0, 511))
 
 
-@pytest.mark.parametrize("ql,window,sinks", [(1, 0, False), (4, 0, True), (3, 8193, False), (2, 257, True),
-                                             (4, 17, False), (1, 1, True)])
-def test_d256_full(orc, ql, window, sinks):
+@pytest.mark.parametrize("ql,window,sinks,consumer", [
+    (1, 0, False, 0), (4, 0, True, 1), (3, 8193, False, 1), (2, 257, True, 0), (4, 17, False, 1), (1, 1, True, 0),
+    (4, 0, True, 2), (3, 8193, False, 2), (4, 17, False, 2)])
+def test_d256_full(orc, ql, window, sinks, consumer):
     w = pw.d256(query_len=ql, window=window, with_sinks=sinks)
-    gpu, plan = decode(DeviceWorkload(w), max_context_len=131135)
+    gpu, plan = decode(DeviceWorkload(w), max_context_len=131135, consumer=consumer)
     # seq 0 is empty; odd seqs 8K, even seqs 128K; always include the empty one
     check(orc, w, gpu, 3 if window == 0 else 8, seed=ql, include=(0, 1, 2 * 3 + 1))
 
@@ -77,8 +78,9 @@ def test_sparse_full(orc, kv):
         assert_parity(gpu, ref, what=f"sparse {m}")
 
 
+@pytest.mark.parametrize("consumer", [pa.PA_CONSUMER_AUTO, pa.PA_CONSUMER_TMEM], ids=["auto", "tmem"])
 @pytest.mark.parametrize("kv", [pw.KV_FP8, pw.KV_BF16], ids=["fp8", "bf16"])
-def test_mtp4_full(orc, kv):
+def test_mtp4_full(orc, kv, consumer):
     w = pw.mtp4(kv_dtype=kv)
-    gpu, plan = decode(DeviceWorkload(w), max_context_len=65536)
+    gpu, plan = decode(DeviceWorkload(w), max_context_len=65536, consumer=consumer)
     check(orc, w, gpu, 6, seed=kv)

@@ -48,6 +48,25 @@ def test_merge_paths_bit_identical_balanced():
     assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("kv", [pw.KV_FP8, pw.KV_BF16], ids=["fp8", "bf16"])
+def test_tmem_merge_paths_bit_identical(kv):
+    """The tensor-memory consumer feeds the same three merges: one schedule,
+    bit-identical outputs."""
+    w = pw.make_dense("tmem", batch=5, hkv=2, group=16, head_dim=128, query_len=2, page_size=16,
+                      ctx_lens=[0, 70, 600, 1300, 2500], kv_dtype=kv,
+                      scale_mode=pw.SCALE_PER_TENSOR if kv == pw.KV_FP8 else pw.SCALE_NONE, seed=14, causal=1)
+    dw = DeviceWorkload(w)
+    outs = [decode(dw, schedule=pa.PA_SCHED_PER_UNIT, max_partitions=5, merge_mode=m, consumer=pa.PA_CONSUMER_TMEM)[0]
+            for m in (pa.PA_MERGE_CLUSTER, pa.PA_MERGE_LAST_ARRIVER, pa.PA_MERGE_REDUCER)]
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+    b1, _ = decode(dw, sm_count_override=7, ctas_per_sm_override=1, merge_mode=pa.PA_MERGE_LAST_ARRIVER,
+                   consumer=pa.PA_CONSUMER_TMEM)
+    b2, _ = decode(dw, sm_count_override=7, ctas_per_sm_override=1, merge_mode=pa.PA_MERGE_REDUCER,
+                   consumer=pa.PA_CONSUMER_TMEM)
+    assert np.array_equal(b1, b2)
+    assert_parity(b1, oracle.get().decode(w), what="tmem balanced")
+
+
 def test_sparse_merge_paths_bit_identical():
     dw = DeviceWorkload(pw.small_sparse(rows=4, topk=512, context=3000))
     outs = [decode(dw, schedule=pa.PA_SCHED_PER_UNIT, max_partitions=8, merge_mode=m)[0]

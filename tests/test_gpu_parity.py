@@ -78,21 +78,27 @@ def test_d256_per_token_mtp_windows(orc, ql, window):
                       seed=100 + ql, causal=1, window=window, with_sinks=(window % 2 == 1))
     ref = orc.decode(w)
     dw = DeviceWorkload(w)
-    for m in (dict(), dict(sm_count_override=4, ctas_per_sm_override=1)):
+    modes = [dict(), dict(sm_count_override=4, ctas_per_sm_override=1)]
+    if 8 * ql > 16:  # tensor-memory consumer
+        modes += [dict(consumer=pa.PA_CONSUMER_TMEM),
+                  dict(consumer=pa.PA_CONSUMER_TMEM, sm_count_override=4, ctas_per_sm_override=1)]
+    for m in modes:
         gpu, _ = decode(dw, **m)
         assert_parity(gpu, ref, what=f"d256 ql{ql} w{window} {m}")
 
 
+@pytest.mark.parametrize("consumer", [pa.PA_CONSUMER_TILE, pa.PA_CONSUMER_TMEM], ids=["tile", "tmem"])
 @pytest.mark.parametrize("kv", [pw.KV_FP8, pw.KV_BF16], ids=["fp8", "bf16"])
-@pytest.mark.parametrize("mode", MODES[:2] + MODES[4:6], ids=MODE_IDS[:2] + MODE_IDS[4:6])
-def test_mtp4_gqa16(orc, kv, mode):
+@pytest.mark.parametrize("mode", MODES[:2] + MODES[4:6] + [MODES[2]], ids=MODE_IDS[:2] + MODE_IDS[4:6] + [MODE_IDS[2]])
+def test_mtp4_gqa16(orc, kv, mode, consumer):
     lens = [3, 4, 5, 128, 129, 1000, 2600]
     w = pw.make_dense("mtp4s", batch=len(lens), hkv=2, group=16, head_dim=128, query_len=4,
                       page_size=128, ctx_lens=lens, kv_dtype=kv,
                       scale_mode=pw.SCALE_PER_TENSOR if kv == pw.KV_FP8 else pw.SCALE_NONE,
                       seed=30, causal=1)
-    gpu, _ = decode(DeviceWorkload(w), **mode)
-    assert_parity(gpu, orc.decode(w), what=f"mtp4 {mode}")
+    gpu, plan = decode(DeviceWorkload(w), consumer=consumer, **mode)
+    assert plan.info["consumer"] == consumer
+    assert_parity(gpu, orc.decode(w), what=f"mtp4 {mode} consumer {consumer}")
 
 
 @pytest.mark.parametrize("page", [16, 32, 64, 128, 256])
@@ -109,16 +115,22 @@ def test_group_shapes(orc, group, ql):
     w = pw.make_dense("groups", batch=3, hkv=2, group=group, head_dim=128, query_len=ql,
                       page_size=16, ctx_lens=[ql, 90, 700], kv_dtype=pw.KV_BF16,
                       scale_mode=pw.SCALE_NONE, seed=50 + group, causal=1, with_sinks=True)
-    gpu, _ = decode(DeviceWorkload(w))
-    assert_parity(gpu, orc.decode(w), what=f"group {group} ql {ql}")
+    dw = DeviceWorkload(w)
+    ref = orc.decode(w)
+    for consumer in ([pa.PA_CONSUMER_TILE, pa.PA_CONSUMER_TMEM] if group * ql > 16 else [pa.PA_CONSUMER_TILE]):
+        gpu, _ = decode(dw, consumer=consumer)
+        assert_parity(gpu, ref, what=f"group {group} ql {ql} consumer {consumer}")
 
 
 def test_noncausal_mtp(orc):
     w = pw.make_dense("nc", batch=3, hkv=1, group=8, head_dim=128, query_len=3, page_size=16,
                       ctx_lens=[2, 40, 300], kv_dtype=pw.KV_FP8, scale_mode=pw.SCALE_PER_TENSOR,
                       seed=60, causal=0)
-    gpu, _ = decode(DeviceWorkload(w))
-    assert_parity(gpu, orc.decode(w), what="non-causal")
+    dw = DeviceWorkload(w)
+    ref = orc.decode(w)
+    for consumer in (pa.PA_CONSUMER_TILE, pa.PA_CONSUMER_TMEM):
+        gpu, _ = decode(dw, consumer=consumer)
+        assert_parity(gpu, ref, what=f"non-causal consumer {consumer}")
 
 
 SPARSE_MODES = [dict()] + [dict(schedule=pa.PA_SCHED_PER_UNIT, max_partitions=p,
