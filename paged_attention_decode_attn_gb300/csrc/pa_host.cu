@@ -70,17 +70,20 @@ struct KernelShape {
 };
 
 // Groups of more than 16 query rows per KV head (MTP verify, wide GQA) on
-// dense decode run the tensor-memory (tcgen05) consumer: four warps, one
-// 64-row MMA block.
+// dense decode can run the tensor-memory (tcgen05) consumer: eight warps,
+// one 64-row MMA block.
 bool umma_supported(const pa_plan_desc& d, int R) {
   if (d.sparse_topk > 0 || R <= 16) return false;
   if (d.kv_dtype == PA_KV_FP8_E4M3) return d.head_dim == 128 || d.head_dim == 256;
   return d.head_dim == 128;
 }
-// AUTO keeps the tile consumer: on the measured shapes (GQA16 x MTP4, D256 x
-// MTP3-4) it is still the faster of the two.
+// AUTO takes the tensor-memory consumer where it measured faster: FP8 caches
+// at head_dim 128 (GQA16 x MTP4: 0.88 ms against 1.09 ms per call). At head_dim
+// 256 and on BF16 caches the tile consumer is still as fast or faster.
 bool use_umma(const pa_plan_desc& d, int R) {
-  return d.consumer == PA_CONSUMER_TMEM && umma_supported(d, R);
+  if (d.consumer == PA_CONSUMER_TILE || !umma_supported(d, R)) return false;
+  if (d.consumer == PA_CONSUMER_TMEM) return true;
+  return d.kv_dtype == PA_KV_FP8_E4M3 && d.head_dim == 128;
 }
 constexpr int kUmmaRows = 64;
 
@@ -112,8 +115,8 @@ KernelShape kernel_shape(const pa_plan_desc& d) {
     k.nt = 2;
     k.rw = 16;
     k.wr = 4;
-    k.wt = 1;
-    k.ncw = 4;
+    k.wt = 2;  // warps w and w + 4 split each token's row scores
+    k.ncw = 8;
     k.rpad = (R + 7) / 8 * 8;
   }
   return k;
@@ -312,7 +315,7 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   }
   if (ns < 2) return fail(PA_ERR_UNSUPPORTED, "shared memory too small for two ring stages");
   // the token-group warps merge their partial states inside one stage buffer
-  if (k.wt > 1 && (size_t)k.wt * k.rpad * d.head_dim * 4 > (size_t)2 * k.tt * k.rb)
+  if (!k.umma && k.wt > 1 && (size_t)k.wt * k.rpad * d.head_dim * 4 > (size_t)2 * k.tt * k.rb)
     return fail(PA_ERR_UNSUPPORTED, "token-group merge does not fit a ring stage");
 
   int ctas_per_sm = ctas_override;

@@ -109,13 +109,25 @@ __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity) {
     if (global_timer() - t0 > kWaitLimitNs) return false;
   }
 }
+// Named barrier that also ORs a predicate over the participating threads.
+__device__ __forceinline__ bool named_bar_or(int id, int nthr, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %2, 0;\n barrier.cta.red.or.pred po, %1, %3, pi;\n"
+      " selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(r)
+      : "r"(id), "r"((uint32_t)v), "r"(nthr)
+      : "memory");
+  return r != 0;
+}
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
 
 constexpr int kUmmaRows = 64;      // query rows of the MMA block (N of S^T, M of O)
-constexpr int kUmmaThreads = 128;  // four consumer warps
+constexpr int kUmmaThreads = 256;  // eight consumer warps: warps w and w + 4 share TMEM lane quarter w
+constexpr int kHalfRows = 32;      // score rows per thread (warps 0-3: rows 0-31, warps 4-7: rows 32-63)
 constexpr uint32_t kUmmaOCol = 64;  // TMEM columns: S^T [0, 64), O [64, 64 + D), L [64 + D, +16)
 
 template <bool FP8, int D, bool VTOK>
@@ -139,6 +151,7 @@ struct UmmaConsumer {
   int r;          // O row owned by this thread (M = 64 layout: lane < 16 of warp w -> row 16w + lane)
   bool row_own;   // r < R
   int tok;        // S^T row (stage token) held by this thread, -1 if none
+  int half;       // which 32 of the 64 rows this thread's softmax covers
   uint32_t tmem = 0, lane_base = 0;
   float kscale = 1.f, vscale = 1.f;
   bool o_valid = false, pv_pending = false;
@@ -151,11 +164,13 @@ struct UmmaConsumer {
   __device__ UmmaConsumer(const PaParams& p_, Smem s) : p(p_), sm(s) {
     warp = threadIdx.x >> 5;
     lane = threadIdx.x & 31;
-    r = 16 * warp + lane;
-    row_own = lane < 16 && r < p.R;
-    // M = 128: token = thread; M = 64: token 16w + lane for lane < 16
-    tok = TT == 128 ? (int)threadIdx.x : (lane < 16 ? 16 * warp + lane : -1);
-    lane_base = (uint32_t)(32 * warp) << 16;
+    const int quarter = warp & 3;
+    half = warp >> 2;
+    r = 16 * quarter + lane;
+    row_own = half == 0 && lane < 16 && r < p.R;
+    // M = 128: token 32q + lane; M = 64: token 16q + lane for lane < 16
+    tok = TT == 128 ? 32 * quarter + lane : (lane < 16 ? 16 * quarter + lane : -1);
+    lane_base = (uint32_t)(32 * quarter) << 16;
     if (FP8 && p.scale_mode == kScalePerTensor) kscale = __ldg(p.k_scale);
     vscale = per_tensor_vscale(p);
   }
@@ -283,29 +298,28 @@ struct UmmaConsumer {
     return true;
   }
 
-  // FP8 stage -> FP16 K and V operands ([chunks of 64 dims][TT rows][128 B],
-  // swizzled); V rows outside the stage's token range become zeros so that
-  // poisoned slots never reach the MMA. Four units per pass, loads first.
-  __device__ void convert_stage(uint32_t kst, uint32_t vst, const StageView& h) {
-    const uint32_t k16 = sm.base_u32 + p.off_k16, v16 = sm.base_u32 + p.off_v16;
+  // One FP8 tensor of a stage -> FP16 operand ([chunks of 64 dims][TT rows]
+  // [128 B], swizzled); V rows outside the stage's token range become zeros so
+  // that poisoned slots never reach the MMA. Four units per pass, loads first.
+  template <bool IS_V>
+  __device__ void convert_tensor(uint32_t src_base, const StageView& h) {
+    const uint32_t dst_base = sm.base_u32 + (IS_V ? p.off_v16 : p.off_k16);
     constexpr int UPR = NCH * 8;     // 16-byte FP8 units per token row
-    constexpr int UNITS = TT * UPR;  // per tensor
-    static_assert((2 * UNITS) % (4 * kUmmaThreads) == 0, "conversion passes");
+    constexpr int UNITS = TT * UPR;
+    static_assert(UNITS % (4 * kUmmaThreads) == 0, "conversion passes");
 #pragma unroll 1
-    for (int e0 = threadIdx.x; e0 < 2 * UNITS; e0 += 4 * kUmmaThreads) {
+    for (int e0 = threadIdx.x; e0 < UNITS; e0 += 4 * kUmmaThreads) {
       uint4 w[4];
       uint32_t dst[4];
       bool zero[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int e = e0 + j * kUmmaThreads;
-        const bool kv = e >= UNITS;
-        const int ee = kv ? e - UNITS : e;
+        const int ee = e0 + j * kUmmaThreads;
         const int t = ee / UPR, cb = (ee % UPR) / 8, c = ee % 8;
-        w[j] = lds128((kv ? vst : kst) + (uint32_t)(cb * TT + t) * 128u + (uint32_t)((c ^ (t & p.swz)) << 4));
+        w[j] = lds128(src_base + (uint32_t)(cb * TT + t) * 128u + (uint32_t)((c ^ (t & p.swz)) << 4));
         const int dim0 = cb * 128 + 16 * c;
-        dst[j] = swz_unit(kv ? v16 : k16, dim0 / 64, TT, t, (dim0 % 64) / 8);
-        zero[j] = kv && !(h.tbase + t >= h.t0 && h.tbase + t < h.t1);
+        dst[j] = swz_unit(dst_base, dim0 / 64, TT, t, (dim0 % 64) / 8);
+        zero[j] = IS_V && !(h.tbase + t >= h.t0 && h.tbase + t < h.t1);
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -348,43 +362,49 @@ struct UmmaConsumer {
     return true;
   }
 
-  // Load this thread's S^T row (64 row scores of its token).
-  __device__ __forceinline__ void load_srow(float (&x)[kUmmaRows]) {
+  // Load this thread's half of its token's S^T row (32 row scores).
+  __device__ __forceinline__ void load_srow(float (&x)[kHalfRows]) {
+    uint32_t v[32];
+    tmem_ld32(tmem + lane_base + (uint32_t)(kHalfRows * half), v);
+    tmem_wait_ld();
 #pragma unroll
-    for (int c0 = 0; c0 < kUmmaRows; c0 += 32) {
-      uint32_t v[32];
-      tmem_ld32(tmem + lane_base + (uint32_t)c0, v);
-      tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) x[c0 + i] = __uint_as_float(v[i]);
-    }
+    for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(v[i]);
   }
 
   // y[r] = score * c_r - m_r (log2 units, relative to the row's reference
   // max), -inf where masked; returns whether some visible y exceeds 8.
-  __device__ __forceinline__ bool scaled_rows(const StageView& h, bool interior, float ks, float (&y)[kUmmaRows]) {
+  __device__ __forceinline__ bool scaled_rows(const StageView& h, bool interior, float ks, float (&y)[kHalfRows]) {
     bool exceed = false;
     const bool tok_ok = tok >= 0;
+    const int rb = kHalfRows * half;
 #pragma unroll
-    for (int r4 = 0; r4 < kUmmaRows; r4 += 4) {
-      const float4 c4 = *reinterpret_cast<const float4*>(row_c() + r4);
-      const float4 m4 = *reinterpret_cast<const float4*>(row_m() + r4);
+    for (int r4 = 0; r4 < kHalfRows; r4 += 4) {
+      const float4 c4 = *reinterpret_cast<const float4*>(row_c() + rb + r4);
+      const float4 m4 = *reinterpret_cast<const float4*>(row_m() + rb + r4);
       const float cc[4] = {c4.x * ks, c4.y * ks, c4.z * ks, c4.w * ks};
       const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
       int pos[4] = {0, 0, 0, 0};
       if (!interior) {
-        const int4 p4 = *reinterpret_cast<const int4*>(row_pos() + r4);
+        const int4 p4 = *reinterpret_cast<const int4*>(row_pos() + rb + r4);
         pos[0] = p4.x;
         pos[1] = p4.y;
         pos[2] = p4.z;
         pos[3] = p4.w;
       }
+      if (interior && tok_ok) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float v = fmaf(y[r4 + i], cc[i], -mm[i]);
-        const bool vis = tok_ok && (interior || visible(h, tok, pos[i]));
-        y[r4 + i] = vis ? v : -INFINITY;
-        exceed |= vis && v > 8.f;
+        for (int i = 0; i < 4; ++i) {
+          y[r4 + i] = fmaf(y[r4 + i], cc[i], -mm[i]);
+          exceed |= y[r4 + i] > 8.f;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float v = fmaf(y[r4 + i], cc[i], -mm[i]);
+          const bool vis = tok_ok && (interior || visible(h, tok, pos[i]));
+          y[r4 + i] = vis ? v : -INFINITY;
+          exceed |= vis && v > 8.f;
+        }
       }
     }
     return exceed;
@@ -393,16 +413,17 @@ struct UmmaConsumer {
   // Slow path: raise the reference max of rows whose stage max exceeds it;
   // rescale O and L by 2^(m_old - m_new) in TMEM.
   __device__ void raise_max(const StageView& h, bool interior, float ks) {
-    float x[kUmmaRows];
+    float x[kHalfRows];
     load_srow(x);
+    const int rb = kHalfRows * half;
     // stage max of each row in absolute log2 units
 #pragma unroll
-    for (int r4 = 0; r4 < kUmmaRows; r4 += 4) {
-      const float4 c4 = *reinterpret_cast<const float4*>(row_c() + r4);
+    for (int r4 = 0; r4 < kHalfRows; r4 += 4) {
+      const float4 c4 = *reinterpret_cast<const float4*>(row_c() + rb + r4);
       const float cc[4] = {c4.x * ks, c4.y * ks, c4.z * ks, c4.w * ks};
       int pos[4] = {0, 0, 0, 0};
       if (!interior) {
-        const int4 p4 = *reinterpret_cast<const int4*>(row_pos() + r4);
+        const int4 p4 = *reinterpret_cast<const int4*>(row_pos() + rb + r4);
         pos[0] = p4.x;
         pos[1] = p4.y;
         pos[2] = p4.z;
@@ -414,7 +435,7 @@ struct UmmaConsumer {
         float v = vis ? x[r4 + i] * cc[i] : -INFINITY;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-        if (lane == 0) row_smax()[warp * kUmmaRows + r4 + i] = v;
+        if (lane == 0) row_smax()[(warp & 3) * kUmmaRows + rb + r4 + i] = v;
       }
     }
     named_bar(1, kUmmaThreads);
@@ -432,7 +453,7 @@ struct UmmaConsumer {
       row_alpha()[rr] = alpha;
     }
     named_bar(1, kUmmaThreads);
-    if (o_valid) {
+    if (o_valid && half == 0) {
       const float alpha = row_own ? row_alpha()[r] : 1.f;
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
@@ -456,33 +477,34 @@ struct UmmaConsumer {
   }
 
   // Scores of this thread's token -> P^T row (16-bit, 128 bytes, swizzled).
-  __device__ void softmax_stage(const StageView& h, uint32_t sst) {
-    // every row's window is fully inside this stage's tokens?
-    const bool interior = flags()[1] != 0 && h.tbase >= h.t0 && h.tbase + TT <= h.t1 &&
-                          (!p.causal || h.tbase + TT - 1 <= flags()[2]) && (p.window == 0 || h.tbase > flags()[3] - p.window);
-    const float ks = (VTOK && tok >= 0) ? lds_f32(sst + 4u * tok) : 1.f;
-    float y[kUmmaRows];
+  // every row's window is fully inside this stage's tokens?
+  __device__ __forceinline__ bool interior_stage(const StageView& h) const {
+    return flags()[1] != 0 && h.tbase >= h.t0 && h.tbase + TT <= h.t1 &&
+           (!p.causal || h.tbase + TT - 1 <= flags()[2]) && (p.window == 0 || h.tbase > flags()[3] - p.window);
+  }
+  __device__ __forceinline__ float token_kscale(uint32_t sst) const {
+    return (VTOK && tok >= 0) ? lds_f32(sst + 4u * tok) : 1.f;
+  }
+
+  // Scores -> P^T rows against the current reference max. Returns whether
+  // some score exceeds its row's reference by more than 2^8 (the caller then
+  // raises the max and calls this again).
+  __device__ bool softmax_stage(const StageView& h, uint32_t sst) {
+    const bool interior = interior_stage(h);
+    const float ks = token_kscale(sst);
+    float y[kHalfRows];
     load_srow(y);
-    bool exceed = scaled_rows(h, interior, ks, y);
-    // block-wide vote through shared memory
-    if (threadIdx.x == 0) flags()[0] = 0;
-    named_bar(1, kUmmaThreads);
-    if (__any_sync(0xffffffffu, exceed) && lane == 0) flags()[0] = 1;
-    named_bar(1, kUmmaThreads);
-    if (flags()[0]) {
-      raise_max(h, interior, ks);
-      load_srow(y);
-      (void)scaled_rows(h, interior, ks, y);
-    }
-    if (tok < 0) return;
+    const bool exceed = scaled_rows(h, interior, ks, y);
+    if (tok < 0) return exceed;
     // slots outside the token range may hold poisoned scales: P is 0 there
     const bool tok_in = h.tbase + tok >= h.t0 && h.tbase + tok < h.t1;
     const float vs = VTOK ? (tok_in ? lds_f32(sst + 4u * (TT + tok)) : 0.f) : 1.f;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int uu = 0; uu < 4; ++uu) {
+      const int u = 4 * half + uu;  // 16-byte unit = rows 8u .. 8u + 7
       float e[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) e[i] = (y[8 * u + i] == -INFINITY) ? 0.f : ex2(y[8 * u + i]);
+      for (int i = 0; i < 8; ++i) e[i] = ex2(y[8 * uu + i]);  // ex2(-inf) = +0
       uint4 o, ou;
       if constexpr (FP8) {
         ou = make_uint4(pack_f16(e[0], e[1]), pack_f16(e[2], e[3]), pack_f16(e[4], e[5]), pack_f16(e[6], e[7]));
@@ -499,6 +521,7 @@ struct UmmaConsumer {
       }
       sts128(swz_unit(pt16(), 0, TT, tok, u), o);
     }
+    return exceed;
   }
 
   // Per-segment row facts used by the interior test: [1] all rows valid
@@ -552,7 +575,7 @@ struct UmmaConsumer {
     float* cp_o = reinterpret_cast<float*>(sm.base + p.off_cpart);
     float* cp_ml = cp_o + (size_t)p.Rpad * D;
     float L = 0.f;
-    if (o_valid) {
+    if (o_valid && half == 0) {
       uint32_t lv[32];
       tmem_ld32(tmem + lane_base + kLCol, lv);
       tmem_wait_ld();
@@ -560,7 +583,7 @@ struct UmmaConsumer {
     }
     const float M = row_own ? row_m()[r] : -INFINITY;
 #pragma unroll 1
-    for (int c0 = 0; c0 < D; c0 += 32) {
+    for (int c0 = 0; c0 < D && half == 0; c0 += 32) {
       uint32_t v[32];
       if (o_valid) {
         tmem_ld32(tmem + lane_base + kUmmaOCol + (uint32_t)c0, v);
@@ -648,37 +671,48 @@ struct UmmaConsumer {
       const uint32_t kst = sm.stage(s, p);
       const uint32_t vst = kst + (uint32_t)TT * 128u * NCH;
       const uint32_t sst = kst + p.off_scale;
-      // the previous PV reads P (and V); it must finish before they are rewritten
-      if (pv_pending) wait_pv();
       const bool has_tokens = h.t1 > h.t0;
-      if (has_tokens) {
-        if constexpr (FP8)
-          convert_stage(kst, vst, h);
-        else
-          clear_ragged_v(vst, h);
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      tc_fence_before();
-      named_bar(1, kUmmaThreads);
-      // FP8 stages are free once converted, unless the softmax still reads
-      // their per-token scales; BF16 stages once the PV that reads them is done
-      const bool release_now = !has_tokens || (FP8 && !VTOK);
-      if (release_now) {
+      if (!has_tokens) {
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.empty(s, p));
-      }
-      if (has_tokens) {
+      } else {
+        // K operand (the previous S chain, its only reader, has completed);
+        // the previous PV may still run meanwhile
+        if constexpr (FP8) convert_tensor<false>(kst, h);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        named_bar(1, kUmmaThreads);
         if (threadIdx.x == 0) {
           tc_fence_after();
           issue_s(FP8 ? sm.base_u32 + p.off_k16 : kst);
         }
+        // V and P are rewritten only after the previous PV has completed; the
+        // V conversion overlaps the S chain
+        if (pv_pending) wait_pv();
+        if constexpr (FP8)
+          convert_tensor<true>(vst, h);
+        else
+          clear_ragged_v(vst, h);
+        if (FP8 && !VTOK) {
+          // this warp is done with the stage's bytes
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sm.empty(s, p));
+        }
         if (!mbar_wait_spin(sbar(), ph_s)) fail();
         ph_s ^= 1u;
         tc_fence_after();
-        softmax_stage(h, sst);
+        bool exceed = softmax_stage(h, sst);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
-        named_bar(1, kUmmaThreads);
+        if (named_bar_or(1, kUmmaThreads, exceed)) {
+          // rare: a row's max moved past its reference; raise it (rescaling
+          // O and L) and recompute this stage's P
+          raise_max(h, interior_stage(h), token_kscale(sst));
+          (void)softmax_stage(h, sst);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          tc_fence_before();
+          named_bar(1, kUmmaThreads);
+        }
         if (FP8 && VTOK) {
           __syncwarp();
           if (lane == 0) mbar_arrive(sm.empty(s, p));
@@ -698,9 +732,9 @@ struct UmmaConsumer {
   }
 };
 
-// Producer warp = warp 4; consumer warps 0..3.
+// Producer warp = warp 8; consumer warps 0..7.
 template <bool FP8, int D, bool VTOK>
-__global__ void __launch_bounds__(160, 1) pa_umma_kernel(const __grid_constant__ PaParams p,
+__global__ void __launch_bounds__(288, 1) pa_umma_kernel(const __grid_constant__ PaParams p,
                                                          const __grid_constant__ CUtensorMap tmK,
                                                          const __grid_constant__ CUtensorMap tmV) {
   extern __shared__ uint8_t smem_raw[];

@@ -29,9 +29,12 @@ def kernel_shape(d):
     k = dict(R=R, G=G, nt=nt, rw=rw, wr=wr, wt=wt, ncw=wr * wt, rpad=wr * rw, elt=elt, rb=rb,
              tt=tt, tw=tw, bh=min(d["page_size"], tt), umma=False)
     # more than 16 rows on dense decode: the tcgen05 consumer (4 warps of 16 rows)
-    if d.get("consumer", 0) == 2 and d.get("sparse_topk", 0) == 0 and R > 16 and (
-            d["head_dim"] == 128 or (d["kv_dtype"] == 0 and d["head_dim"] == 256)):
-        k.update(umma=True, nt=2, rw=16, wr=4, wt=1, ncw=4, rpad=-(-R // 8) * 8)
+    supported = d.get("sparse_topk", 0) == 0 and R > 16 and (
+        d["head_dim"] == 128 or (d["kv_dtype"] == 0 and d["head_dim"] == 256))
+    consumer = d.get("consumer", 0)
+    auto_tmem = d["kv_dtype"] == 0 and d["head_dim"] == 128
+    if supported and (consumer == 2 or (consumer == 0 and auto_tmem)):
+        k.update(umma=True, nt=2, rw=16, wr=4, wt=2, ncw=8, rpad=-(-R // 8) * 8)
     return k
 
 

@@ -78,7 +78,7 @@ def test_sparse_full(orc, kv):
         assert_parity(gpu, ref, what=f"sparse {m}")
 
 
-@pytest.mark.parametrize("consumer", [pa.PA_CONSUMER_AUTO, pa.PA_CONSUMER_TMEM], ids=["auto", "tmem"])
+@pytest.mark.parametrize("consumer", [pa.PA_CONSUMER_TILE, pa.PA_CONSUMER_TMEM], ids=["tile", "tmem"])
 @pytest.mark.parametrize("kv", [pw.KV_FP8, pw.KV_BF16], ids=["fp8", "bf16"])
 def test_mtp4_full(orc, kv, consumer):
     w = pw.mtp4(kv_dtype=kv)
