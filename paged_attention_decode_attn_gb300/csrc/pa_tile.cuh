@@ -532,12 +532,28 @@ struct Producer {
     }
   }
 
-  // Sparse stages: row r of stage k holds index position tbase + r. The index
-  // loads of a stage are issued together (and for the next stage while this
-  // one's gathers are in flight), then the block-table loads together, so a
-  // stage costs one dependent round trip on the producer's path.
-  int pf_b = -1, pf_pos = -1;
-  int pf_idx[4];
+  // Sparse stages: row r of stage k holds index position tbase + r. Loads
+  // run ahead of the stages: when stage k's gathers are issued, the page ids
+  // of stage k+1 (whose indices arrived meanwhile) and the indices of stage
+  // k+2 are requested, so a stage rarely waits on a block-table round trip.
+  int la_b = -1, la_pos = -1;  // stage whose indices and page ids are requested
+  int la_idx[4], la_phys[4];
+  int nx_b = -1, nx_pos = -1;  // stage whose indices are requested
+  int nx_idx[4];
+
+  __device__ __forceinline__ void load_phys(int b, int L, const int* idx, int* phys) const {
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int t = idx[rr];
+      phys[rr] = (t >= 0 && t < L) ? __ldg(p.block_table + (size_t)b * p.maxp + t / p.S) : -1;
+    }
+  }
+  // Request the indices of the stage at index position pos of sequence b.
+  __device__ __forceinline__ void request_indices(int b, int pos) {
+    nx_b = b;
+    nx_pos = pos;
+    load_indices(b, pos, p.topk, nx_idx);
+  }
 
   __device__ __forceinline__ void load_indices(int b, int pos0, int pos_end, int* idx) const {
 #pragma unroll
@@ -556,20 +572,29 @@ struct Producer {
     const uint32_t vst = kst + (uint32_t)TT * 128u * NCH;
     const bool ktok = p.scale_mode == kScalePerToken;
     const bool empty = !(h.t1 > h.t0);
-    int idx[4];
+    int idx[4], phys[4];
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) idx[rr] = phys[rr] = -1;
     if (!empty) {
-      if (pf_b == h.b && pf_pos == h.tbase) {
+      if (la_b == h.b && la_pos == h.tbase) {
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) idx[rr] = pf_idx[rr];
+        for (int rr = 0; rr < 4; ++rr) {
+          idx[rr] = la_idx[rr];
+          phys[rr] = la_phys[rr];
+        }
       } else {
-        load_indices(h.b, h.tbase, h.t1, idx);
-      }
-    }
-    int phys[4];
+        if (nx_b == h.b && nx_pos == h.tbase) {
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-      const int t = empty ? -1 : idx[rr];
-      phys[rr] = (t >= 0 && t < h.L) ? __ldg(p.block_table + (size_t)h.b * p.maxp + t / p.S) : -1;
+          for (int rr = 0; rr < 4; ++rr) idx[rr] = nx_idx[rr];
+        } else {
+          load_indices(h.b, h.tbase, p.topk, idx);
+        }
+        load_phys(h.b, h.L, idx, phys);
+      }
+      // positions past the stage's range carry no token
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr)
+        if (h.tbase + rr * 32 + lane >= h.t1) idx[rr] = -1;
     }
     int yv[4];
 #pragma unroll
@@ -627,14 +652,21 @@ struct Producer {
         }
       }
     }
-    // prefetch the next stage's indices of this segment
+    // look ahead: page ids of the next stage, indices of the one after
+    la_b = -1;
     const int next = h.tbase + TT;
-    if (!empty && next < h.t1 + TT && next < p.topk) {
-      load_indices(h.b, next, p.topk, pf_idx);
-      pf_b = h.b;
-      pf_pos = next;
-    } else {
-      pf_b = -1;
+    if (!empty && next < p.topk) {
+      if (nx_b == h.b && nx_pos == next) {
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) la_idx[rr] = nx_idx[rr];
+      } else {
+        load_indices(h.b, next, p.topk, la_idx);
+      }
+      load_phys(h.b, h.L, la_idx, la_phys);
+      la_b = h.b;
+      la_pos = next;
+      nx_b = -1;
+      if (next + TT < p.topk) request_indices(h.b, next + TT);
     }
   }
 
@@ -693,6 +725,8 @@ struct Producer {
       const int tbase = (r.c_lo + k0) * p.TT;
       const int lp0 = p.S >= p.TT ? tbase / p.S : max(tbase, r.lo) / p.S;
       stage_window(b, r.L, lp0, p.S < p.TT ? p.TT / p.S : 1);
+    } else if (p.topk > 0 && k1 > k0 && !(la_b == b && la_pos == k0 * p.TT) && !(nx_b == b && nx_pos == k0 * p.TT)) {
+      request_indices(b, k0 * p.TT);  // the first stage's indices, before the query copy
     }
     if (!load_q(b, g)) return;
     for (int k = k0; k < kend && ok; ++k) {

@@ -160,6 +160,9 @@ struct UmmaConsumer {
   int pend_stage = -1;  // BF16: stage the outstanding PV reads, handed back when it completes
   bool ok = true;
   int seg_L = 0;
+  // operand descriptors (built once) and barrier addresses
+  uint64_t dq = 0, dpt = 0, dpu = 0, dones = 0, dk16 = 0, dv16 = 0;
+  uint32_t sbar_addr = 0, obar_addr = 0;
 
   __device__ UmmaConsumer(const PaParams& p_, Smem s) : p(p_), sm(s) {
     warp = threadIdx.x >> 5;
@@ -219,6 +222,14 @@ struct UmmaConsumer {
     named_bar(1, kUmmaThreads);
     tc_fence_after();
     tmem = *reinterpret_cast<volatile uint32_t*>(sm.base + p.off_tslot);
+    dq = umma_sdesc(q16(), 16, 1024);
+    dpt = umma_sdesc(pt16(), TT * 128u, 1024);
+    dpu = umma_sdesc(pu16(), TT * 128u, 1024);
+    dones = umma_sdesc(ones16(), 16, 1024);
+    dk16 = umma_sdesc(sm.base_u32 + p.off_k16, 16, 1024);
+    dv16 = umma_sdesc(sm.base_u32 + p.off_v16, TT * 128u, 1024);
+    sbar_addr = sbar();
+    obar_addr = obar();
   }
 
   __device__ void teardown() {
@@ -540,32 +551,33 @@ struct UmmaConsumer {
     }
   }
 
-  __device__ void issue_s(uint32_t kbase) {
+  // Descriptor of the operand byte_off bytes past a base descriptor's start
+  // (the start field is the low 14 bits of address / 16; operands lie below
+  // 256 KiB, so the add never carries out of it).
+  __device__ __forceinline__ static uint64_t dadd(uint64_t d, uint32_t byte_off) { return d + (uint64_t)(byte_off >> 4); }
+
+  __device__ void issue_s(uint64_t dk) {
 #pragma unroll
     for (int j = 0; j < D / 16; ++j) {
-      const uint64_t ad = umma_sdesc(kbase + (uint32_t)(j / 4) * (TT * 128u) + (uint32_t)(j % 4) * 32u, 16, 1024);
-      const uint64_t bd = umma_sdesc(q16() + (uint32_t)(j / 4) * (kUmmaRows * 128u) + (uint32_t)(j % 4) * 32u, 16, 1024);
+      const uint64_t ad = dadd(dk, (uint32_t)(j / 4) * (TT * 128u) + (uint32_t)(j % 4) * 32u);
+      const uint64_t bd = dadd(dq, (uint32_t)(j / 4) * (kUmmaRows * 128u) + (uint32_t)(j % 4) * 32u);
       umma_f16(tmem, ad, bd, kIdescS, j > 0 ? 1u : 0u);
     }
-    umma_commit(sbar());
+    umma_commit(sbar_addr);
   }
-
-  __device__ void issue_pv(uint32_t vbase, bool accumulate) {
+  __device__ void issue_pv(uint64_t dv, bool accumulate) {
     // A = P^T stored [TT tokens][64 rows]: MN-major, one 64-row chunk;
     // B = V [TT tokens][D]: MN-major, D/64 chunks of TT*128 bytes
 #pragma unroll
-    for (int j = 0; j < TT / 16; ++j) {
-      const uint64_t ad = umma_sdesc(pt16() + (uint32_t)j * 2048u, TT * 128u, 1024);
-      const uint64_t bd = umma_sdesc(vbase + (uint32_t)j * 2048u, TT * 128u, 1024);
-      umma_f16(tmem + kUmmaOCol, ad, bd, kIdescPV, (accumulate || j > 0) ? 1u : 0u);
-    }
+    for (int j = 0; j < TT / 16; ++j)
+      umma_f16(tmem + kUmmaOCol, dadd(dpt, (uint32_t)j * 2048u), dadd(dv, (uint32_t)j * 2048u), kIdescPV,
+               (accumulate || j > 0) ? 1u : 0u);
 #pragma unroll
-    for (int j = 0; j < TT / 16; ++j) {
-      const uint64_t ad = umma_sdesc((VTOK ? pu16() : pt16()) + (uint32_t)j * 2048u, TT * 128u, 1024);
-      const uint64_t bd = umma_sdesc(ones16() + (uint32_t)(j / 4) * (16 * 128u) + (uint32_t)(j % 4) * 32u, 16, 1024);
-      umma_f16(tmem + kLCol, ad, bd, kIdescL, (accumulate || j > 0) ? 1u : 0u);
-    }
-    umma_commit(obar());
+    for (int j = 0; j < TT / 16; ++j)
+      umma_f16(tmem + kLCol, dadd(VTOK ? dpu : dpt, (uint32_t)j * 2048u),
+               dadd(dones, (uint32_t)(j / 4) * (16 * 128u) + (uint32_t)(j % 4) * 32u), kIdescL,
+               (accumulate || j > 0) ? 1u : 0u);
+    umma_commit(obar_addr);
   }
 
   __device__ void end_segment(const StageView& h, int slot, const MergeDesc& md) {
@@ -684,7 +696,7 @@ struct UmmaConsumer {
         named_bar(1, kUmmaThreads);
         if (threadIdx.x == 0) {
           tc_fence_after();
-          issue_s(FP8 ? sm.base_u32 + p.off_k16 : kst);
+          issue_s(FP8 ? dk16 : umma_sdesc(kst, 16, 1024));
         }
         // V and P are rewritten only after the previous PV has completed; the
         // V conversion overlaps the S chain
@@ -719,7 +731,7 @@ struct UmmaConsumer {
         }
         if (threadIdx.x == 0) {
           tc_fence_after();
-          issue_pv(FP8 ? sm.base_u32 + p.off_v16 : vst, o_valid);
+          issue_pv(FP8 ? dv16 : umma_sdesc(vst, TT * 128u, 1024), o_valid);
         }
         pv_pending = true;
         o_valid = true;
