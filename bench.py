@@ -72,10 +72,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str = "dense"):
-    """DRAM bytes per launch from the committed ncu summary of this workload,
-    if it was taken on the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", f"pa_tile_{workload}.md")
+def profiled_traffic(workload: str = "dense", kernel: str = "pa_tile"):
+    """DRAM bytes per launch from the committed ncu summary of this kernel on
+    this workload (profiles/<kernel>_<workload>.md), if it was taken on the
+    current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -371,6 +372,7 @@ def main():
 
     if rank == 0:
         peak, peak_kind = measured_peak_gbs()
+        kernel_name = "pa_umma_kernel" if plan.info["consumer"] == pa.PA_CONSUMER_TMEM else "pa_tile_kernel"
         per_launch_us = float(np.mean(per_call_ms)) * 1000.0
         achieved = alg / (per_launch_us * 1e-6) / 1e9
         value = tot_bytes / tot_s / 1e9
@@ -390,8 +392,9 @@ def main():
                                                          "block_threads", "num_stages", "stage_tokens",
                                                          "ctas_per_sm", "launches_per_call")}},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_kind": peak_kind, "traffic": profiled_traffic(args.workload),
-                         "algorithmic_bytes_per_launch": alg, "kernel": "pa_tile_kernel"},
+                         "frac": achieved / peak, "peak_kind": peak_kind,
+                         "traffic": profiled_traffic(args.workload, kernel_name.replace("_kernel", "")),
+                         "algorithmic_bytes_per_launch": alg, "kernel": kernel_name},
             "e2e": {"value": e2e_bytes / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "steps": e2e_steps},
             "gpu_launches": int(K * plan.info["launches_per_call"]),
