@@ -132,7 +132,10 @@ pa::SmemLayout smem_layout(const pa_plan_desc& d, const KernelShape& k, int ns, 
   L.off_k16 = L.off_v16 = L.off_q16 = L.off_p16 = 0;
   if (k.umma) {
     // 1024-aligned 16-bit operands (stage_bytes is a multiple of 1024)
-    if (d.kv_dtype == PA_KV_FP8_E4M3) {
+    // FP8 head_dim 128 runs FP8 MMAs on the stage itself; other FP8 shapes
+    // convert K and V to FP16 operands
+    const bool f8mma = d.kv_dtype == PA_KV_FP8_E4M3 && d.head_dim == 128 && !k.vtok;
+    if (d.kv_dtype == PA_KV_FP8_E4M3 && !f8mma) {
       L.off_k16 = (int)off;
       off += (size_t)k.tt * d.head_dim * 2;
       L.off_v16 = (int)off;
@@ -143,7 +146,7 @@ pa::SmemLayout smem_layout(const pa_plan_desc& d, const KernelShape& k, int ns, 
     // P^T ([tokens][64 rows]), its unscaled copy under per-token V scales,
     // then a 16 x tokens operand of ones for the row sums
     L.off_p16 = (int)off;
-    off += (size_t)(k.vtok ? 2 : 1) * k.tt * kUmmaRows * 2 + (size_t)16 * k.tt * 2;
+    off += (size_t)(k.vtok ? 2 : 1) * k.tt * kUmmaRows * 2 + (size_t)16 * k.tt * (f8mma ? 1 : 2);
   }
   L.off_merge = (int)off;
   L.off_cpart = (int)off;  // cluster merge: this CTA's partial (O, then max/sum)

@@ -34,6 +34,8 @@
 // ordering of the tensor-memory MMAs are this implementation's.
 #pragma once
 
+#include <cuda_fp8.h>
+
 #include "pa_tile.cuh"
 
 namespace pa {
@@ -63,6 +65,30 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
           d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Four floats -> four e4m3 bytes (first value in the lowest byte), RN, saturating.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+// Leading term of a two-term e4m3 split: x rounded to nearest-even at 4
+// significant bits, which e4m3 holds exactly for 2^-6 <= |x| <= 448; 0 below
+// 2^-6 (the trailing term x - lead then carries all of x).
+__device__ __forceinline__ float e4m3_lead(float x) {
+  const float ax = fabsf(x);
+  if (ax < 0.015625f) return 0.f;
+  uint32_t u = __float_as_uint(ax);
+  u = (u + 0x7FFFFu + ((u >> 20) & 1u)) & 0xFFF00000u;
+  return copysignf(__uint_as_float(u), x);
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
@@ -135,20 +161,33 @@ struct UmmaConsumer {
   static constexpr int ELT = FP8 ? 1 : 2;
   static constexpr int NCH = D * ELT / 128;         // 128-byte blocks per token row of a stage
   static constexpr int TT = 32768 / (2 * D * ELT);  // tokens per stage (M of S^T)
-  static constexpr uint32_t kLCol = kUmmaOCol + D;  // row sums, 16 equal columns
+  // FP8 at head_dim 128 with per-tensor scales: FP8 MMAs (kind::f8f6f4) read
+  // K and V from the stage itself; Q and P enter as two-term FP8 sums
+  // (hi + lo), stacked as 128 rows. Otherwise FP8 stages are converted to
+  // FP16 operands (CONV): with per-token scales P is multiplied by the V
+  // scale (~amax/448), which would put most of P * v_scale in e4m3's
+  // subnormal range, where the two-term sum loses its precision.
+  static constexpr bool F8 = FP8 && D == 128 && !VTOK;
+  static constexpr bool CONV = FP8 && !F8;
+  static constexpr int SN = F8 ? 128 : kUmmaRows;  // N of S^T
+  static constexpr int OM = F8 ? 128 : kUmmaRows;  // M of O and L
+  static constexpr int KSTEP = F8 ? 32 : 16;       // K of one MMA
+  static constexpr uint32_t kOCol = F8 ? 128u : kUmmaOCol;
+  static constexpr uint32_t kLCol = kOCol + D;  // row sums, 16 equal columns
   static constexpr uint32_t kTmemCols = (kLCol + 16) <= 256 ? 256u : 512u;
   static_assert(TT == 64 || TT == 128, "stage tokens");
-  // S^T = K Q^T: M = TT tokens, N = 64 rows, A = K (K-major), B = Q (K-major)
-  static constexpr uint32_t kIdescS = umma_idesc_ab(!FP8, TT, kUmmaRows, false, false);
-  // O += P V: M = 64 rows, N = D, A = P^T (MN-major), B = V (MN-major)
-  static constexpr uint32_t kIdescPV = umma_idesc_ab(!FP8, kUmmaRows, D, true, true);
+  // S^T = K Q^T: M = TT tokens, N = SN rows, A = K (K-major), B = Q (K-major)
+  static constexpr uint32_t kIdescS = umma_idesc_ab(!FP8, TT, SN, false, false);
+  // O += P V: M = OM rows, N = D, A = P^T (MN-major), B = V (MN-major)
+  static constexpr uint32_t kIdescPV = umma_idesc_ab(!FP8, OM, D, true, true);
   // L += P 1: N = 16, B = ones (K-major)
-  static constexpr uint32_t kIdescL = umma_idesc_ab(!FP8, kUmmaRows, 16, true, false);
+  static constexpr uint32_t kIdescL = umma_idesc_ab(!FP8, OM, 16, true, false);
 
   const PaParams& p;
   Smem sm;
   int warp, lane;
   int r;          // O row owned by this thread (M = 64 layout: lane < 16 of warp w -> row 16w + lane)
+  int olane_row;  // row whose O lane this thread reads (F8: lane 32q + l -> row (32q + l) % 64)
   bool row_own;   // r < R
   int tok;        // S^T row (stage token) held by this thread, -1 if none
   int half;       // which 32 of the 64 rows this thread's softmax covers
@@ -169,8 +208,16 @@ struct UmmaConsumer {
     lane = threadIdx.x & 31;
     const int quarter = warp & 3;
     half = warp >> 2;
-    r = 16 * quarter + lane;
-    row_own = half == 0 && lane < 16 && r < p.R;
+    if constexpr (F8) {
+      // O lanes 0..63 hold the rows' hi parts, 64..127 the lo parts
+      olane_row = (32 * quarter + lane) & 63;
+      r = olane_row;
+      row_own = half == 0 && quarter < 2 && r < p.R;
+    } else {
+      r = 16 * quarter + lane;
+      olane_row = r;
+      row_own = half == 0 && lane < 16 && r < p.R;
+    }
     // M = 128: token 32q + lane; M = 64: token 16q + lane for lane < 16
     tok = TT == 128 ? 32 * quarter + lane : (lane < 16 ? 16 * quarter + lane : -1);
     lane_base = (uint32_t)(32 * quarter) << 16;
@@ -209,8 +256,8 @@ struct UmmaConsumer {
     for (uint32_t o = threadIdx.x * 16u; o < (uint32_t)(kUmmaRows * D * 2); o += kUmmaThreads * 16u)
       sts128(q16() + o, make_uint4(0, 0, 0, 0));
     // ones operand (16 x TT, K-major; every element 1.0)
-    const uint32_t one2 = FP8 ? 0x3C003C00u : 0x3F803F80u;
-    for (uint32_t o = threadIdx.x * 16u; o < (uint32_t)(16 * TT * 2); o += kUmmaThreads * 16u)
+    const uint32_t one2 = F8 ? 0x38383838u : (FP8 ? 0x3C003C00u : 0x3F803F80u);
+    for (uint32_t o = threadIdx.x * 16u; o < (uint32_t)(16 * TT * (F8 ? 1 : 2)); o += kUmmaThreads * 16u)
       sts128(ones16() + o, make_uint4(one2, one2, one2, one2));
     if (warp == 0) {
       asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sm.base_u32 + p.off_tslot),
@@ -266,7 +313,49 @@ struct UmmaConsumer {
       float c = 0.f;
       if (rr < p.R) {
         const uint32_t qrow = sm.qbuf(qs, p) + (uint32_t)rr * (uint32_t)(D * 2);
-        if constexpr (FP8) {
+        if constexpr (F8) {
+          // power-of-two row scale to a max in [128, 256), then q = hi + lo
+          // in e4m3 (rows rr and 64 + rr of the Q operand)
+          float amax = 0.f;
+          for (int u = 0; u < D / 8; ++u) {
+            const uint4 w = lds128(qrow + 16u * u);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              amax = fmaxf(amax, fabsf(bf16_bits_to_f32(ws[e] & 0xFFFFu)));
+              amax = fmaxf(amax, fabsf(bf16_bits_to_f32(ws[e] >> 16)));
+            }
+          }
+          int ex = 0;
+          if (amax > 0.f) {
+            const int e2 = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+            ex = max(-126, min(126, 7 - e2));
+          }
+          const float sc = __uint_as_float((uint32_t)(ex + 127) << 23);
+          const float inv = __uint_as_float((uint32_t)(127 - ex) << 23);
+          for (int u = 0; u < D / 16; ++u) {  // 16 values = one 16-byte unit of a row
+            const uint4 w0 = lds128(qrow + 32u * u), w1 = lds128(qrow + 32u * u + 16u);
+            const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            float hv[16], lv[16];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float a = bf16_bits_to_f32(ws[e] & 0xFFFFu) * sc, b = bf16_bits_to_f32(ws[e] >> 16) * sc;
+              hv[2 * e] = e4m3_lead(a);
+              hv[2 * e + 1] = e4m3_lead(b);
+              lv[2 * e] = a - hv[2 * e];
+              lv[2 * e + 1] = b - hv[2 * e + 1];
+            }
+            const uint4 ho = make_uint4(pack_e4m3x4(hv[0], hv[1], hv[2], hv[3]), pack_e4m3x4(hv[4], hv[5], hv[6], hv[7]),
+                                        pack_e4m3x4(hv[8], hv[9], hv[10], hv[11]),
+                                        pack_e4m3x4(hv[12], hv[13], hv[14], hv[15]));
+            const uint4 lo = make_uint4(pack_e4m3x4(lv[0], lv[1], lv[2], lv[3]), pack_e4m3x4(lv[4], lv[5], lv[6], lv[7]),
+                                        pack_e4m3x4(lv[8], lv[9], lv[10], lv[11]),
+                                        pack_e4m3x4(lv[12], lv[13], lv[14], lv[15]));
+            sts128(swz_unit(q16(), 0, 128, rr, u), ho);
+            sts128(swz_unit(q16(), 0, 128, 64 + rr, u), lo);
+          }
+          c = inv * p.sm_scale_log2 * (p.scale_mode == kScalePerTensor ? kscale : 1.f);
+        } else if constexpr (FP8) {
           float amax = 0.f;
           for (int u = 0; u < D / 8; ++u) {
             const uint4 w = lds128(qrow + 16u * u);
@@ -380,6 +469,12 @@ struct UmmaConsumer {
     tmem_wait_ld();
 #pragma unroll
     for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(v[i]);
+    if constexpr (F8) {  // + the lo rows' partial scores
+      tmem_ld32(tmem + lane_base + (uint32_t)(kUmmaRows + kHalfRows * half), v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] += __uint_as_float(v[i]);
+    }
   }
 
   // y[r] = score * c_r - m_r (log2 units, relative to the row's reference
@@ -465,16 +560,17 @@ struct UmmaConsumer {
     }
     named_bar(1, kUmmaThreads);
     if (o_valid && half == 0) {
-      const float alpha = row_own ? row_alpha()[r] : 1.f;
+      // F8: every lane of the 128-row O holds a hi or lo part of row olane_row
+      const float alpha = ((F8 || lane < 16) && olane_row < p.R) ? row_alpha()[olane_row] : 1.f;
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t v[32];
-          tmem_ld32(tmem + lane_base + kUmmaOCol + (uint32_t)c0, v);
+          tmem_ld32(tmem + lane_base + kOCol + (uint32_t)c0, v);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-          tmem_st32(tmem + lane_base + kUmmaOCol + (uint32_t)c0, v);
+          tmem_st32(tmem + lane_base + kOCol + (uint32_t)c0, v);
         }
         uint32_t lv[32];  // L occupies the first 16 of these columns
         tmem_ld32(tmem + lane_base + kLCol, lv);
@@ -510,6 +606,43 @@ struct UmmaConsumer {
     // slots outside the token range may hold poisoned scales: P is 0 there
     const bool tok_in = h.tbase + tok >= h.t0 && h.tbase + tok < h.t1;
     const float vs = VTOK ? (tok_in ? lds_f32(sst + 4u * (TT + tok)) : 0.f) : 1.f;
+    if constexpr (F8) {
+      // P^T row of this token: bytes [0, 64) the rows' hi terms, [64, 128)
+      // the lo terms; this thread's 32 rows are units 2h, 2h+1 and 4+2h, 5+2h
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        float e[16], hv[16], lv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          e[i] = ex2(y[16 * g + i]);  // ex2(-inf) = +0
+          const float pn = VTOK ? e[i] * vs : e[i];
+          hv[i] = e4m3_lead(pn);
+          lv[i] = pn - hv[i];
+        }
+        const int u = 2 * half + g;
+        sts128(swz_unit(pt16(), 0, TT, tok, u),
+               make_uint4(pack_e4m3x4(hv[0], hv[1], hv[2], hv[3]), pack_e4m3x4(hv[4], hv[5], hv[6], hv[7]),
+                          pack_e4m3x4(hv[8], hv[9], hv[10], hv[11]), pack_e4m3x4(hv[12], hv[13], hv[14], hv[15])));
+        sts128(swz_unit(pt16(), 0, TT, tok, 4 + u),
+               make_uint4(pack_e4m3x4(lv[0], lv[1], lv[2], lv[3]), pack_e4m3x4(lv[4], lv[5], lv[6], lv[7]),
+                          pack_e4m3x4(lv[8], lv[9], lv[10], lv[11]), pack_e4m3x4(lv[12], lv[13], lv[14], lv[15])));
+        if constexpr (VTOK) {
+          // the row sums take the plain P
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            hv[i] = e4m3_lead(e[i]);
+            lv[i] = e[i] - hv[i];
+          }
+          sts128(swz_unit(pu16(), 0, TT, tok, u),
+                 make_uint4(pack_e4m3x4(hv[0], hv[1], hv[2], hv[3]), pack_e4m3x4(hv[4], hv[5], hv[6], hv[7]),
+                            pack_e4m3x4(hv[8], hv[9], hv[10], hv[11]), pack_e4m3x4(hv[12], hv[13], hv[14], hv[15])));
+          sts128(swz_unit(pu16(), 0, TT, tok, 4 + u),
+                 make_uint4(pack_e4m3x4(lv[0], lv[1], lv[2], lv[3]), pack_e4m3x4(lv[4], lv[5], lv[6], lv[7]),
+                            pack_e4m3x4(lv[8], lv[9], lv[10], lv[11]), pack_e4m3x4(lv[12], lv[13], lv[14], lv[15])));
+        }
+      }
+      return exceed;
+    }
 #pragma unroll
     for (int uu = 0; uu < 4; ++uu) {
       const int u = 4 * half + uu;  // 16-byte unit = rows 8u .. 8u + 7
@@ -557,20 +690,41 @@ struct UmmaConsumer {
   __device__ __forceinline__ static uint64_t dadd(uint64_t d, uint32_t byte_off) { return d + (uint64_t)(byte_off >> 4); }
 
   __device__ void issue_s(uint64_t dk) {
+    if constexpr (F8) {
+      // K rows are 128 bytes = 128 e4m3 values: one chunk, 32-byte k-steps
 #pragma unroll
-    for (int j = 0; j < D / 16; ++j) {
-      const uint64_t ad = dadd(dk, (uint32_t)(j / 4) * (TT * 128u) + (uint32_t)(j % 4) * 32u);
-      const uint64_t bd = dadd(dq, (uint32_t)(j / 4) * (kUmmaRows * 128u) + (uint32_t)(j % 4) * 32u);
-      umma_f16(tmem, ad, bd, kIdescS, j > 0 ? 1u : 0u);
+      for (int j = 0; j < D / 32; ++j)
+        umma_f8(tmem, dadd(dk, (uint32_t)j * 32u), dadd(dq, (uint32_t)j * 32u), kIdescS, j > 0 ? 1u : 0u);
+    } else {
+#pragma unroll
+      for (int j = 0; j < D / 16; ++j) {
+        const uint64_t ad = dadd(dk, (uint32_t)(j / 4) * (TT * 128u) + (uint32_t)(j % 4) * 32u);
+        const uint64_t bd = dadd(dq, (uint32_t)(j / 4) * (kUmmaRows * 128u) + (uint32_t)(j % 4) * 32u);
+        umma_f16(tmem, ad, bd, kIdescS, j > 0 ? 1u : 0u);
+      }
     }
     umma_commit(sbar_addr);
   }
   __device__ void issue_pv(uint64_t dv, bool accumulate) {
+    if constexpr (F8) {
+      // A = P^T [TT tokens][128 hi/lo rows], B = V [TT tokens][128 dims]:
+      // both MN-major e4m3, 32 tokens (4 KiB) per k-step
+#pragma unroll
+      for (int j = 0; j < TT / 32; ++j)
+        umma_f8(tmem + kOCol, dadd(dpt, (uint32_t)j * 4096u), dadd(dv, (uint32_t)j * 4096u), kIdescPV,
+                (accumulate || j > 0) ? 1u : 0u);
+#pragma unroll
+      for (int j = 0; j < TT / 32; ++j)
+        umma_f8(tmem + kLCol, dadd(VTOK ? dpu : dpt, (uint32_t)j * 4096u), dadd(dones, (uint32_t)j * 32u), kIdescL,
+                (accumulate || j > 0) ? 1u : 0u);
+      umma_commit(obar_addr);
+      return;
+    }
     // A = P^T stored [TT tokens][64 rows]: MN-major, one 64-row chunk;
     // B = V [TT tokens][D]: MN-major, D/64 chunks of TT*128 bytes
 #pragma unroll
     for (int j = 0; j < TT / 16; ++j)
-      umma_f16(tmem + kUmmaOCol, dadd(dpt, (uint32_t)j * 2048u), dadd(dv, (uint32_t)j * 2048u), kIdescPV,
+      umma_f16(tmem + kOCol, dadd(dpt, (uint32_t)j * 2048u), dadd(dv, (uint32_t)j * 2048u), kIdescPV,
                (accumulate || j > 0) ? 1u : 0u);
 #pragma unroll
     for (int j = 0; j < TT / 16; ++j)
@@ -586,29 +740,12 @@ struct UmmaConsumer {
     const bool cluster = p.merge == kMergeCluster;
     float* cp_o = reinterpret_cast<float*>(sm.base + p.off_cpart);
     float* cp_ml = cp_o + (size_t)p.Rpad * D;
-    float L = 0.f;
-    if (o_valid && half == 0) {
-      uint32_t lv[32];
-      tmem_ld32(tmem + lane_base + kLCol, lv);
-      tmem_wait_ld();
-      L = __uint_as_float(lv[0]);
-    }
     const float M = row_own ? row_m()[r] : -INFINITY;
-#pragma unroll 1
-    for (int c0 = 0; c0 < D && half == 0; c0 += 32) {
-      uint32_t v[32];
-      if (o_valid) {
-        tmem_ld32(tmem + lane_base + kUmmaOCol + (uint32_t)c0, v);
-        tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0u;
-      }
-      if (!row_own) continue;
+    // write 32 columns of this thread's row (row_own threads)
+    auto emit = [&](int c0, const float* v, float L) {
 #pragma unroll
       for (int i = 0; i < 32; i += 4) {
-        const float4 f = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]), __uint_as_float(v[i + 2]),
-                                     __uint_as_float(v[i + 3]));
+        const float4 f = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
         const int d = c0 + i;
         if (whole)
           finalize_store<D>(p, vscale, f, M, L, h.b, h.g, r, d);
@@ -616,6 +753,68 @@ struct UmmaConsumer {
           *reinterpret_cast<float4*>(cp_o + (size_t)r * D + d) = f;
         else
           *reinterpret_cast<float4*>(p.part_o + ((size_t)slot * p.Rpad + r) * D + d) = f;
+      }
+    };
+    float L = 0.f;
+    if constexpr (F8) {
+      // O and L rows are hi part (lanes 0..63) + lo part (lanes 64..127):
+      // quarters 2, 3 pass theirs through shared memory (the P^T buffer, idle
+      // now) 32 columns at a time
+      float* scr = reinterpret_cast<float*>(sm.base + p.off_p16);  // [64 rows][33]
+      const bool lo_part = half == 0 && (warp & 3) >= 2;
+      const bool hi_part = half == 0 && (warp & 3) < 2;
+      uint32_t lv[32];
+      if (o_valid && half == 0) {
+        tmem_ld32(tmem + lane_base + kLCol, lv);
+        tmem_wait_ld();
+      }
+      if (lo_part) scr[64 * 33 + olane_row] = o_valid ? __uint_as_float(lv[0]) : 0.f;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t v[32];
+        if (o_valid && half == 0) {
+          tmem_ld32(tmem + lane_base + kOCol + (uint32_t)c0, v);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        if (lo_part) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) scr[olane_row * 33 + i] = __uint_as_float(v[i]);
+        }
+        named_bar(1, kUmmaThreads);
+        if (hi_part) {
+          if (c0 == 0) L = (o_valid ? __uint_as_float(lv[0]) : 0.f) + scr[64 * 33 + olane_row];
+          float f[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]) + scr[olane_row * 33 + i];
+          if (row_own) emit(c0, f, L);
+        }
+        named_bar(1, kUmmaThreads);
+      }
+    } else {
+      if (o_valid && half == 0) {
+        uint32_t lv[32];
+        tmem_ld32(tmem + lane_base + kLCol, lv);
+        tmem_wait_ld();
+        L = __uint_as_float(lv[0]);
+      }
+#pragma unroll 1
+      for (int c0 = 0; c0 < D && half == 0; c0 += 32) {
+        uint32_t v[32];
+        if (o_valid) {
+          tmem_ld32(tmem + lane_base + kOCol + (uint32_t)c0, v);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        if (!row_own) continue;
+        float f[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+        emit(c0, f, L);
       }
     }
     if (row_own && !whole) {
@@ -690,22 +889,22 @@ struct UmmaConsumer {
       } else {
         // K operand (the previous S chain, its only reader, has completed);
         // the previous PV may still run meanwhile
-        if constexpr (FP8) convert_tensor<false>(kst, h);
+        if constexpr (CONV) convert_tensor<false>(kst, h);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
         named_bar(1, kUmmaThreads);
         if (threadIdx.x == 0) {
           tc_fence_after();
-          issue_s(FP8 ? dk16 : umma_sdesc(kst, 16, 1024));
+          issue_s(CONV ? dk16 : umma_sdesc(kst, 16, 1024));
         }
         // V and P are rewritten only after the previous PV has completed; the
         // V conversion overlaps the S chain
         if (pv_pending) wait_pv();
-        if constexpr (FP8)
+        if constexpr (CONV)
           convert_tensor<true>(vst, h);
         else
           clear_ragged_v(vst, h);
-        if (FP8 && !VTOK) {
+        if (CONV && !VTOK) {
           // this warp is done with the stage's bytes
           __syncwarp();
           if (lane == 0) mbar_arrive(sm.empty(s, p));
@@ -725,17 +924,17 @@ struct UmmaConsumer {
           tc_fence_before();
           named_bar(1, kUmmaThreads);
         }
-        if (FP8 && VTOK) {
+        if (CONV && VTOK) {
           __syncwarp();
           if (lane == 0) mbar_arrive(sm.empty(s, p));
         }
         if (threadIdx.x == 0) {
           tc_fence_after();
-          issue_pv(FP8 ? dv16 : umma_sdesc(vst, TT * 128u, 1024), o_valid);
+          issue_pv(CONV ? dv16 : umma_sdesc(vst, TT * 128u, 1024), o_valid);
         }
         pv_pending = true;
         o_valid = true;
-        if (!FP8) pend_stage = s;
+        if (!CONV) pend_stage = s;  // the MMAs read this stage in place
       }
       if (h.flags & kSegLast) end_segment(h, slot, md);
       ++n;

@@ -42,11 +42,13 @@ def smem_total(d, k, ns, cluster, nq):
     stage = 2 * k["tt"] * k["rb"] + (1024 if d["scale_mode"] == 2 else 0)
     off = ns * stage
     if k["umma"]:
-        if d["kv_dtype"] == 0:
+        vtok = d["kv_dtype"] == 0 and d["scale_mode"] == 2
+        f8mma = d["kv_dtype"] == 0 and d["head_dim"] == 128 and not vtok  # FP8 MMAs on the stage itself
+        if d["kv_dtype"] == 0 and not f8mma:
             off += 2 * k["tt"] * d["head_dim"] * 2  # 16-bit K and V operands
         off += 64 * d["head_dim"] * 2  # Q operand (64 rows)
         vtok = d["kv_dtype"] == 0 and d["scale_mode"] == 2
-        off += (2 if vtok else 1) * k["tt"] * 64 * 2 + 16 * k["tt"] * 2  # P^T (+ unscaled), ones
+        off += (2 if vtok else 1) * k["tt"] * 64 * 2 + 16 * k["tt"] * (1 if f8mma else 2)  # P^T (+ unscaled), ones
     if cluster:
         off += align(k["rpad"] * d["head_dim"] * 4 + k["rpad"] * 8, 128)
     off += ns * 128 + ns * 16 + 32 + 32

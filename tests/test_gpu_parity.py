@@ -122,6 +122,22 @@ def test_group_shapes(orc, group, ql):
         assert_parity(gpu, ref, what=f"group {group} ql {ql} consumer {consumer}")
 
 
+@pytest.mark.parametrize("window,sinks", [(0, False), (37, True)])
+def test_fp8_per_token_wide_group(orc, window, sinks):
+    """FP8 per-token scales, head_dim 128, 32 rows per KV head: both stage
+    consumers (the tensor-memory one runs FP8 MMAs on the stage bytes)."""
+    w = pw.make_dense("pt32", batch=4, hkv=2, group=16, head_dim=128, query_len=2, page_size=16,
+                      ctx_lens=[2, 77, 400, 1500], kv_dtype=pw.KV_FP8, scale_mode=pw.SCALE_PER_TOKEN,
+                      seed=88, causal=1, window=window, with_sinks=sinks)
+    dw = DeviceWorkload(w)
+    ref = orc.decode(w)
+    for consumer in (pa.PA_CONSUMER_TILE, pa.PA_CONSUMER_TMEM):
+        for m in (dict(), dict(sm_count_override=5, ctas_per_sm_override=1)):
+            gpu, plan = decode(dw, consumer=consumer, **m)
+            assert plan.info["consumer"] == consumer
+            assert_parity(gpu, ref, what=f"fp8 per-token 32 rows consumer {consumer} {m}")
+
+
 def test_noncausal_mtp(orc):
     w = pw.make_dense("nc", batch=3, hkv=1, group=8, head_dim=128, query_len=3, page_size=16,
                       ctx_lens=[2, 40, 300], kv_dtype=pw.KV_FP8, scale_mode=pw.SCALE_PER_TENSOR,
