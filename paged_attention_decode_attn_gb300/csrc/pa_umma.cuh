@@ -1,37 +1,38 @@
-// tcgen05 consumer for query-row groups of 17..64 rows (MTP verify rows and
-// wide GQA groups), dense paged decode on sm_103a.
+// Tensor-memory (tcgen05) consumer for query-row groups of 17..64 rows per KV
+// head (MTP verify rows x GQA), dense paged decode on sm_103a.
 //
 // The producer warp, the stage ring, the Q ring, the schedules and the
-// partial merges are those of the tile kernel (pa_tile.cuh). What changes is
-// how a stage is consumed: instead of every 8-row warp converting the whole
-// stage and running mma.sync, the stage is turned once into 16-bit operands
-// in shared memory and two tcgen05.mma chains run on it with accumulators in
+// partial merges are those of the tile kernel (pa_tile.cuh). A stage is
+// consumed with tcgen05.mma chains issued by one thread, accumulators in
 // tensor memory:
 //
-//   S[64 x TT]  = Q[64 x D] . K[TT x D]^T     (A = Q, K-major; B = K, K-major)
-//   O[64 x D]  += P[64 x TT] . V[TT x D]      (A = P, K-major; B = V, MN-major)
+//   S^T[TT x N] = K[TT x D] . Q^T     (M = the stage's tokens; N = 64 rows)
+//   O[M x D]   += P[M x TT] . V        (A = P^T and B = V both MN-major)
+//   L[M x 16]  += P . ones             (the row sums, from the tensor cores)
 //
-// M = 64 rows (the group's R <= 64 rows, the rest zero). Under the M = 64
-// accumulator layout row r sits in TMEM lane 32*(r/16) + r%16, so thread
-// `lane` (< 16) of consumer warp w owns row 16*w + lane: it reads its score
-// row with tcgen05.ld, applies scale and masks, keeps the row's running max
-// and sum in registers (no shuffles: the whole row is in one thread), writes
-// its row of P, and at the segment end reads its row of O.
+// One thread holds one token's row of S^T (warps w and w + 4 share TMEM lane
+// quarter w and split its 64 row scores), applies scale and masks, and writes
+// its token's row of P^T. The softmax keeps a lazy reference max per row: P is
+// taken against it, and only a score more than 2^8 above it (always on a
+// segment's first stage, rarely later) sends the CTA through a slow path that
+// reduces the stage's row maxima across threads and rescales O and L in TMEM.
+// The row owners (M = 64: lane l < 16 of warp q holds row 16q + l) read O and
+// L at the segment end.
 //
-// Operands: FP8 caches are converted exactly to FP16 (K and V keep the
-// stage's row layout, so V serves as an MN-major operand without a
-// transpose), with Q in FP16 under an exact power-of-two row scale; BF16
-// caches are used in place by the MMAs, with Q and P in BF16. Every shared
-// operand uses the 128-byte swizzle in 64-element (128-byte) chunks.
-//
-// The running max used for the exponentials is raised lazily: only when a
-// row's max grows by more than 2^8 is O rescaled (in TMEM) and the max
-// replaced, so P stays below 2^8 and O, the sum and the stored max remain
-// consistent (the partial merge takes the stored max as the reference).
+// Operands (128-byte swizzle, 128-byte chunks):
+//  * BF16 caches: the stage is read in place; Q and P BF16 (kind::f16).
+//  * FP8 caches, head_dim 128, per-tensor scales: the stage is read in place by
+//    kind::f8f6f4 MMAs; Q and P enter as two-term e4m3 sums hi + lo, stacked
+//    as 128 rows, so S^T has 128 columns (hi and lo halves added per row) and
+//    O and L 128 lanes (halves added at the segment end).
+//  * other FP8 shapes: K and V converted exactly to FP16 in their row layout
+//    (V stays an MN-major operand, no transpose); Q in FP16 under an exact
+//    power-of-two row scale, P in FP16 below 2^8.
 //
 // Sources of the method: the tile kernel's pages (split-KV partials, scale
-// before mask, per-token scales folded into P, MTP rows); the layout and
-// ordering of the tensor-memory MMAs are this implementation's.
+// before mask, per-token scales folded into P, MTP rows); the tensor-memory
+// layout, the operand splits and the ordering of the MMA chains are this
+// implementation's.
 #pragma once
 
 #include <cuda_fp8.h>
@@ -198,7 +199,6 @@ struct UmmaConsumer {
   uint32_t ph_s = 0, ph_o = 0;
   int pend_stage = -1;  // BF16: stage the outstanding PV reads, handed back when it completes
   bool ok = true;
-  int seg_L = 0;
   // operand descriptors (built once) and barrier addresses
   uint64_t dq = 0, dpt = 0, dpu = 0, dones = 0, dk16 = 0, dv16 = 0;
   uint32_t sbar_addr = 0, obar_addr = 0;
@@ -307,7 +307,6 @@ struct UmmaConsumer {
     got = __all_sync(0xffffffffu, got);
     if (!got) return false;
     ++nq;
-    seg_L = L;
     if (threadIdx.x < kUmmaRows) {
       const int rr = threadIdx.x;
       float c = 0.f;
