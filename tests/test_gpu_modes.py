@@ -122,18 +122,26 @@ def test_relocation_bit_identical():
     assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("merge", [pa.PA_MERGE_LAST_ARRIVER, pa.PA_MERGE_REDUCER, pa.PA_MERGE_CLUSTER])
-def test_graph_replay_refresh_and_poison(merge):
+@pytest.mark.parametrize("merge,wide", [(pa.PA_MERGE_LAST_ARRIVER, False), (pa.PA_MERGE_REDUCER, False),
+                                        (pa.PA_MERGE_CLUSTER, False), (pa.PA_MERGE_LAST_ARRIVER, True),
+                                        (pa.PA_MERGE_CLUSTER, True)])
+def test_graph_replay_refresh_and_poison(merge, wide):
     """Capture one decode in a CUDA graph; before each replay poison the output
     with NaN and change the context lengths in place. Every replay must equal
     an eager call on the same lengths bit for bit, and the oracle within
-    tolerance; arrival counters end at zero."""
+    tolerance; arrival counters end at zero. `wide`: 32 rows per KV head, so
+    the captured kernel is the tensor-memory consumer."""
     orc = oracle.get()
     w = _w(seed=12)
+    if wide:
+        w = pw.make_dense("modes-wide", batch=7, hkv=2, group=16, head_dim=128, query_len=2, page_size=16,
+                          ctx_lens=[0, 3, 90, 600, 1300, 2222, 4001], kv_dtype=pw.KV_FP8,
+                          scale_mode=pw.SCALE_PER_TENSOR, seed=12, causal=1, window=0, with_sinks=True)
     dw = DeviceWorkload(w)
     kw = dict(sm_count_override=6, ctas_per_sm_override=1) if merge != pa.PA_MERGE_CLUSTER else dict(
         schedule=pa.PA_SCHED_PER_UNIT, max_partitions=4)
     plan = pa.Plan(**dw.plan_fields(merge_mode=merge, max_context_len=8192, **kw))
+    assert plan.info["consumer"] == (pa.PA_CONSUMER_TMEM if wide else pa.PA_CONSUMER_TILE)
     stream = torch.cuda.Stream()
     dw.poison_out()
     with torch.cuda.stream(stream):
