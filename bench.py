@@ -62,13 +62,22 @@ def measured_peak_gbs():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+# Sources that define each kernel: its own translation units and headers,
+# plus the shared header and the host code that sets its launch.
+KERNEL_SOURCES = {
+    "pa_tile": ("pa_tile.cuh", "pa_tile_fp8_d128.cu", "pa_tile_fp8_d256.cu", "pa_tile_bf16.cu"),
+    "pa_umma": ("pa_tile.cuh", "pa_umma.cuh", "pa_umma_fp8.cu", "pa_umma_bf16.cu"),
+    "pa_reduce": ("pa_tile.cuh", "pa_reduce.cu"),
+}
+SHARED_SOURCES = ("pa_internal.h", "pa_host.cu")
+
+
+def kernel_source_hash(kernel: str = "pa_tile") -> str:
     csrc = os.path.join(ROOT, "paged_attention_decode_attn_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            h.update(name.encode())
-            h.update(open(os.path.join(csrc, name), "rb").read())
+    for name in sorted(set(KERNEL_SOURCES[kernel]) | set(SHARED_SOURCES)):
+        h.update(name.encode())
+        h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -83,7 +92,7 @@ def profiled_traffic(workload: str = "dense", kernel: str = "pa_tile"):
         return None
     m_hash = re.search(r"source_hash:\s*([0-9a-f]+)", text)
     m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(kernel):
         return None
     return int(m_bytes.group(1))
 
