@@ -172,7 +172,6 @@ struct UmmaConsumer {
   static constexpr bool CONV = FP8 && !F8;
   static constexpr int SN = F8 ? 128 : kUmmaRows;  // N of S^T
   static constexpr int OM = F8 ? 128 : kUmmaRows;  // M of O and L
-  static constexpr int KSTEP = F8 ? 32 : 16;       // K of one MMA
   static constexpr uint32_t kOCol = F8 ? 128u : kUmmaOCol;
   static constexpr uint32_t kLCol = kOCol + D;  // row sums, 16 equal columns
   static constexpr uint32_t kTmemCols = (kLCol + 16) <= 256 ? 256u : 512u;
@@ -197,7 +196,7 @@ struct UmmaConsumer {
   bool o_valid = false, pv_pending = false;
   int nq = 0;
   uint32_t ph_s = 0, ph_o = 0;
-  int pend_stage = -1;  // BF16: stage the outstanding PV reads, handed back when it completes
+  int pend_stage = -1;  // stage read in place by the outstanding PV (BF16, FP8 MMAs), handed back when it completes
   bool ok = true;
   // operand descriptors (built once) and barrier addresses
   uint64_t dq = 0, dpt = 0, dpu = 0, dones = 0, dk16 = 0, dv16 = 0;
