@@ -72,12 +72,20 @@ KERNEL_SOURCES = {
 SHARED_SOURCES = ("pa_internal.h", "pa_host.cu")
 
 
+def _code_only(text: str) -> str:
+    """Source text without C/C++ comments and blank lines (what compiles)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash(kernel: str = "pa_tile") -> str:
+    """Hash of the code (comments excluded) of the sources defining a kernel."""
     csrc = os.path.join(ROOT, "paged_attention_decode_attn_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(set(KERNEL_SOURCES[kernel]) | set(SHARED_SOURCES)):
         h.update(name.encode())
-        h.update(open(os.path.join(csrc, name), "rb").read())
+        h.update(_code_only(open(os.path.join(csrc, name), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -56,11 +56,12 @@ struct pa_plan {
 
 namespace {
 
-// Largest dynamic shared memory a CTA may use while two CTAs share an SM.
 // A segment's fixed cost (query rows, token-group merge, output or partial
 // write) is about one stage of streaming; the balanced schedule charges it as
 // one virtual chunk per unit.
 constexpr int kSegCostChunks = 1;
+// Largest dynamic shared memory a CTA may use while two CTAs share an SM, and
+// with one CTA per SM.
 constexpr int kSmemTwoPerSm = 112 * 1024;
 constexpr int kSmemOnePerSm = 226 * 1024;
 
@@ -78,7 +79,7 @@ bool umma_supported(const pa_plan_desc& d, int R) {
   return d.head_dim == 128;
 }
 // AUTO takes the tensor-memory consumer where it measured faster: FP8 caches
-// at head_dim 128 (GQA16 x MTP4: 0.88 ms against 1.09 ms per call). At head_dim
+// at head_dim 128 (GQA16 x MTP4: 0.74 ms against 1.09 ms per call). At head_dim
 // 256 and on BF16 caches the tile consumer is still as fast or faster.
 bool use_umma(const pa_plan_desc& d, int R) {
   if (d.consumer == PA_CONSUMER_TILE || !umma_supported(d, R)) return false;
