@@ -182,29 +182,54 @@ def aggregate(local_seconds: float, local_bytes: int, group=None):
     return float(t.item()), int(b.item())
 
 
-def cpu_baseline(w, units=CPU_SAMPLE_UNITS, seed=0):
-    """The oracle, as it is, on a bounded sample of units (single thread)."""
+def _unit_bytes(w, units):
+    """Algorithmic bytes of the sampled (sequence, KV head) units."""
+    L = w.ctx_lens.astype(np.int64)
+    per_tok = w.head_dim * w.elt_bytes * 2
+    total = 0
+    for u in units:
+        b = int(u) // w.num_kv_heads
+        total += int(L[b]) * per_tok + ((int(L[b]) + w.page_size - 1) // w.page_size) * 4
+        total += 2 * w.group * w.query_len * w.head_dim * 2
+    return total
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, units=CPU_SAMPLE_UNITS, seed=0, threads=1):
+    """The oracle, as it is, on a bounded sample of units. threads > 1 runs a
+    thread pool over the sampled units, one oracle call per unit (the C oracle
+    runs without the GIL); threads == 1 is one call over all of them."""
+    import concurrent.futures as cf
+
     import oracle
 
     orc = oracle.get()
     U = w.batch * w.num_kv_heads
     rng = np.random.default_rng(seed)
     pick = rng.choice(U, size=min(units, U), replace=False)
-    mask = np.zeros(U, dtype=np.uint8)
-    mask[pick] = 1
+
+    def run(sel):
+        mask = np.zeros(U, dtype=np.uint8)
+        mask[sel] = 1
+        orc.decode(w, unit_mask=mask)
+
     t0 = time.perf_counter()
-    orc.decode(w, unit_mask=mask)
+    if threads <= 1:
+        run(pick)
+    else:
+        with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(lambda u: run([u]), pick))
     dt = time.perf_counter() - t0
-    sub_bytes = 0
-    L = w.ctx_lens.astype(np.int64)
-    per_tok = w.head_dim * w.elt_bytes * 2
-    for u in pick:
-        b = int(u) // w.num_kv_heads
-        sub_bytes += int(L[b]) * per_tok + ((int(L[b]) + w.page_size - 1) // w.page_size) * 4
-        sub_bytes += 2 * w.group * w.query_len * w.head_dim * 2
-    return {"value": sub_bytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+    how = "single-threaded" if threads <= 1 else f"a pool of {threads} threads, one unit per task"
+    return {"value": _unit_bytes(w, pick) / dt / 1e9, "unit": "GB/s", "cores": max(1, threads), "kind": "oracle",
             "sample": f"{len(pick)} of {U} (sequence, KV head) units of the same workload, "
-                      f"{dt:.1f} s single-threaded C (double precision)",
+                      f"{dt:.1f} s, {how}, C in double precision",
             "seconds": dt}
 
 
@@ -217,11 +242,13 @@ WORKLOADS = {
                "tokens per row, 4096-page pool"),
     "mtp4": ("dense MTP4 verify: batch 32, 4 KV heads, GQA16, head_dim 128, query length 4 causal, page 128, "
              "contexts U[4096, 65536]"),
+    "sparse_prefill": ("sparse prefill: one prompt of N rows (--rows, default 1024), 16 query heads, 1 KV head, "
+                       "head_dim 128, page 16, row r attends to min(r + 1, 2048) tokens, 4096-page pool"),
 }
 
 
 SEQ_LEN = {"dense": "U[1024,8192]", "tiny": "{37,100}", "d256": "{0, 8K+tail, 128K+tail}",
-           "sparse": "2048 of 131072", "mtp4": "U[4096,65536]"}
+           "sparse": "2048 of 131072", "mtp4": "U[4096,65536]", "sparse_prefill": "min(r + 1, 2048) of r + 1"}
 MERGES = {"auto": 0, "direct": 1, "cluster": 2, "last-arriver": 3, "reducer": 4}
 CONSUMERS = {"auto": 0, "tile": 1, "tmem": 2}
 
@@ -238,6 +265,8 @@ def make_workload(args, rank):
         return pw.sparse(kv_dtype=kv)
     if args.workload == "mtp4":
         return pw.mtp4(kv_dtype=kv)
+    if args.workload == "sparse_prefill":
+        return pw.sparse_prefill(kv_dtype=kv, rows=args.rows)
     raise ValueError(args.workload)
 
 
@@ -246,10 +275,11 @@ def run_reference(args):
     if rank != 0:
         return 0
     w = pw.dense()
+    cores = host_cores()
     vals, secs = [], 0.0
-    units = max(4, CPU_SAMPLE_UNITS // 4)
+    units = 2 * cores
     for s in range(args.warmup_ref + args.steps_ref):
-        r = cpu_baseline(w, units=units, seed=s)
+        r = cpu_baseline(w, units=units, seed=s, threads=cores)
         if s >= args.warmup_ref:
             vals.append(r["value"])
             secs += r["seconds"]
@@ -260,11 +290,43 @@ def run_reference(args):
             "data": "synthetic",
             "config": {"workload": WORKLOAD, "global_batch": 64, "seq_len": "U[1024,8192]",
                        "parallelism": "replicas", "l2": "cpu"},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{units} random units per step of the same workload"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{units} random units per step of the same workload, a pool of "
+                                       f"{cores} threads"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
+
+
+def warm_us_per_call(step, stream, calls=10, replays=5, runs=5, rounds=3):
+    """The pages' warm protocol: a CUDA graph of `calls` decodes, replayed
+    `replays` times per run; the minimum over `runs` runs, the median over
+    `rounds` rounds, in µs per call (no L2 eviction between calls)."""
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        step(stream)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(calls):
+                step(stream)
+    torch.cuda.synchronize()
+    meds = []
+    for _ in range(rounds):
+        best = float("inf")
+        for _ in range(runs):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                for _ in range(replays):
+                    g.replay()
+                b.record(stream)
+            b.synchronize()
+            best = min(best, a.elapsed_time(b) * 1000.0 / (replays * calls))
+        meds.append(best)
+    return float(np.median(meds))
 
 
 def main():
@@ -278,6 +340,8 @@ def main():
     ap.add_argument("--workload", default="dense", choices=sorted(WORKLOADS),
                     help="the headline line uses the default dense workload; the others are for profiling")
     ap.add_argument("--kv", default="fp8", choices=["fp8", "bf16"], help="sparse and mtp4 cache format")
+    ap.add_argument("--rows", type=int, default=1024, help="sparse_prefill: prompt rows")
+    ap.add_argument("--no-warm", action="store_true", help="skip the warm CUDA-graph timing")
     ap.add_argument("--ql", type=int, default=1, help="d256: query length (MTP rows)")
     ap.add_argument("--window", type=int, default=0, help="d256: sliding window (0 = off)")
     ap.add_argument("--sinks", action="store_true", help="d256: per-head sink logits")
@@ -333,13 +397,14 @@ def main():
     def flush_l2():
         return flush.sum(dtype=torch.int64)
 
-    def step():
+    def step(on=None):
+        on = stream if on is None else on
         if w.topk:
             plan.decode_sparse(out, d["q"], d["k"], d["v"], d["bt"], d["ctx"], d["idx"], d.get("ks"), d.get("vs"),
-                               d.get("sinks"), stream=stream)
+                               d.get("sinks"), stream=on)
         else:
             plan.decode(out, d["q"], d["k"], d["v"], d["bt"], d["ctx"], d.get("ks"), d.get("vs"), w.window,
-                        d.get("sinks"), stream=stream)
+                        d.get("sinks"), stream=on)
 
     for _ in range(args.warmup):
         flush_l2()
@@ -367,6 +432,8 @@ def main():
     local_s = float(per_call_ms.sum()) / 1000.0
     tot_s, tot_bytes = aggregate(local_s, alg * K)
     status = plan.device_status()
+
+    warm_us = None if args.no_warm else warm_us_per_call(step, torch.cuda.Stream(dev))
 
     # end to end through the public API: pinned host inputs -> device, decode, output -> host
     e2e_steps = args.e2e_steps
@@ -418,9 +485,16 @@ def main():
             "clocks": clk.summary(),
             "device_status": status,
         }
+        if warm_us is not None:
+            line["us_per_call_warm"] = warm_us
+            line["warm_protocol"] = "10-call CUDA graph x 5 replays, min of 5 runs, median of 3 rounds, no L2 eviction"
         if world == 1 and not args.no_cpu_baseline and args.workload == "dense":
-            cb = cpu_baseline(w)
+            cores = host_cores()
+            cb = cpu_baseline(w, units=max(CPU_SAMPLE_UNITS, 4 * cores), threads=cores)
             cb.pop("seconds")
+            single = cpu_baseline(w, units=CPU_SAMPLE_UNITS // 2, seed=1)
+            single.pop("seconds")
+            cb["single_thread"] = single
             line["cpu_baseline"] = cb
         print(json.dumps(line))
     if world > 1:

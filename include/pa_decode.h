@@ -115,7 +115,7 @@ typedef struct pa_plan_desc {
   int batch;
   int num_q_heads;
   int num_kv_heads;      /* num_q_heads % num_kv_heads == 0 */
-  int head_dim;          /* 128 or 256 */
+  int head_dim;          /* 128 or 256 (PA_ERR_UNSUPPORTED otherwise) */
   int query_len;         /* 1..4 (MTP rows); rows = query_len * group <= 64 */
   int page_size;         /* 16, 32, 64, 128 or 256 tokens */
   int max_pages_per_seq; /* block-table row stride (int32 elements) */
@@ -163,31 +163,77 @@ typedef struct pa_plan_info {
 typedef struct pa_plan pa_plan_t;
 
 /* Validate desc, size partitions from the SM count and occupancy, pick the
- * merge mechanism. Host only: with both overrides set it touches no device. */
+ * merge mechanism. Follows PR "Add paged-attention Tile kernel" (the
+ * per-sequence plan limit defaults to the device's compute-unit count; head
+ * dimension and shape checks reject what the kernels cannot run) and PR "Merge
+ * gfx1250 PA decode partitions in the tile kernel and speed up dense decode",
+ * Partition merges (cluster merge for 2..16 partitions, last-arriver merge
+ * for one-slot plans, the reducer otherwise).
+ * desc: read only, not retained. out: receives a host-heap plan owned by the
+ * caller (release with pa_plan_destroy); set to NULL on failure.
+ * Errors: PA_ERR_INVALID_ARG (bad field), PA_ERR_UNSUPPORTED (valid but not
+ * built: head_dim, rows, page size), PA_ERR_CUDA (device attribute or
+ * occupancy query failed). Host only: with both overrides set it touches no
+ * device; otherwise it queries the plan's device and restores the caller's
+ * current device before returning. */
 PA_API pa_status pa_plan_create(const pa_plan_desc* desc, pa_plan_t** out);
 
-/* Bytes of caller-owned device workspace the plan needs (partials, arrival
- * counters at one 128-byte line each, status word). */
+/* Bytes of caller-owned device workspace the plan needs: partial (max, sum,
+ * unnormalised output) per split segment (PR "Add paged-attention Tile
+ * kernel": exp_sums, max_logits and tmp_output of a partitioned call), arrival
+ * counters at one 128-byte line each (PR "Merge gfx1250 PA decode partitions
+ * in the tile kernel and speed up dense decode", Partition merges:
+ * [batch, kv_heads, 32] int32), reducer descriptors and the status word.
+ * Returns 0 for a NULL plan. */
 PA_API size_t pa_plan_workspace_bytes(const pa_plan_t* plan);
 
 /* Bind zero-filled device memory of at least pa_plan_workspace_bytes bytes
- * (16-byte aligned). The plan does not take ownership. */
+ * (256-byte aligned) on the plan's device. The plan does not take ownership;
+ * the memory must outlive every decode enqueued with the plan. The arrival
+ * counters in it are zeroed once here by the caller and reset by their last
+ * arrival afterwards (PR "Merge gfx1250 PA decode partitions in the tile
+ * kernel and speed up dense decode", Partition merges), so CUDA-graph replays
+ * need no host work. Errors: PA_ERR_INVALID_ARG (NULL plan), PA_ERR_WORKSPACE
+ * (NULL, misaligned or too small). */
 PA_API pa_status pa_plan_set_workspace(pa_plan_t* plan, void* dev_ptr, size_t bytes);
 
+/* Copy the resolved plan (partitions, stage size, merge mode, grid,
+ * workspace layout) into *info, for tests that check the sizing rule of PR
+ * "Add paged-attention Tile kernel" (partition count from the compute-unit
+ * count) bit for bit. Errors: PA_ERR_INVALID_ARG for NULL arguments. */
 PA_API pa_status pa_plan_get_info(const pa_plan_t* plan, pa_plan_info* info);
 
+/* Free a plan (NULL is a no-op). Decodes already enqueued with it are not
+ * affected: they carry their arguments by value. */
 PA_API void pa_plan_destroy(pa_plan_t* plan);
 
 /* Dense paged decode of one batch on `stream` (a cudaStream_t; NULL = legacy
- * default stream). window: 0 = off, else W >= 1 (requires causal or
- * query_len 1). Returns after enqueueing; errors in the kernel's bounded
- * waits show up in the status word (pa_plan_info.status_offset). */
+ * default stream): PR "Add paged-attention Tile kernel" (pa_decode(output,
+ * query, key_cache, value_cache, block_tables, context_lengths, key_scale,
+ * value_scale, ...)), with the sliding window and sinks of PR "Extend packed
+ * D256 PA decode pipe to page16, transposed V and sliding windows" and PR
+ * "Merge gfx1250 PA decode partitions in the tile kernel and speed up dense
+ * decode". window: 0 = off, else W >= 1 (requires causal or query_len 1).
+ * Scales: required (device float32) when the plan's scale_mode is not NONE.
+ * Errors: PA_ERR_INVALID_ARG (NULL or misaligned pointer, negative window,
+ * sparse plan), PA_ERR_UNSUPPORTED (window with non-causal multi-token
+ * queries), PA_ERR_WORKSPACE (none bound), PA_ERR_CUDA (launch failed).
+ * Returns after enqueueing; a page id outside [0, num_pages) or a bounded
+ * wait that ran out sets a bit in the device status word
+ * (pa_plan_info.status_offset inside the workspace). */
 PA_API pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
                     const int32_t* block_table, const int32_t* ctx_lens, const float* k_scale,
                     const float* v_scale, int window, const float* sinks, const pa_plan_t* plan,
                     void* stream);
 
-/* Sparse (top-k index list) decode: query_len 1, no causal mask or window. */
+/* Sparse (top-k index list) decode: each sequence (query_len 1) attends to
+ * the tokens its row of topk_idx lists, gathered through the block table (PR
+ * "Merge gfx1250 PA decode partitions in the tile kernel and speed up dense
+ * decode": sparse decode over 2048 top-k page16 tokens per row, and sparse
+ * prefill, where row r lists min(r + 1, 2048) tokens and the remaining entries
+ * are ignored). No causal mask or window; entries outside [0, L_b) are skipped.
+ * Errors as pa_decode, plus PA_ERR_INVALID_ARG for a dense plan or a NULL
+ * topk_idx. */
 PA_API pa_status pa_decode_sparse(void* out, const void* q, const void* k_cache, const void* v_cache,
                            const int32_t* block_table, const int32_t* ctx_lens,
                            const int32_t* topk_idx, const float* k_scale, const float* v_scale,
@@ -205,7 +251,11 @@ PA_API pa_status pa_decode_sparse(void* out, const void* q, const void* k_cache,
  * address (cudaGetSymbolAddress); make that first call before any stream
  * capture. Every call shares the one buffer: calls that can overlap on the
  * GPU race, so serialise them. Each call zeroes the scratch's counters and
- * status word on `stream` before its kernel. */
+ * status word on `stream` before its kernel. The device status word lives in
+ * that private scratch, so on this path a page id out of range or a bounded
+ * wait that ran out is not reported to the caller (pa_decode reports both
+ * through the workspace's status word); a caller that needs that check
+ * should use pa_decode. */
 PA_API pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
                                    const int32_t* block_table, const int32_t* ctx_lens, const float* k_scale,
                                    const float* v_scale, int window, const float* sinks, const pa_plan_t* plan,

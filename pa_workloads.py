@@ -23,6 +23,9 @@ Workloads follow the shapes the reference pages measure:
   speed up dense decode", Performance).
 * "mtp4": batch 32, 4 KV heads, GQA16, D128, QL4 causal, page 128, contexts
   uniform in [4096, 65536] (same PR, "Dense tile kernels": MTP4 at GQA16).
+* "sparse_prefill": 1024 (or 8192) prompt rows, 16 query heads, 1 KV head,
+  D128, page 16, row r attends to min(r + 1, 2048) of the prompt's first r + 1
+  tokens (same PR, Performance: the sparse prefill rows).
 
 Cache layout is ``[num_pages, num_kv_heads, page_size, head_dim]`` (bytes for
 FP8, BF16 bit patterns for BF16). Every pool page that no sequence uses, every
@@ -126,11 +129,13 @@ def _pool_and_table(rng, ctx_lens, page_size, pool_pages, max_pages):
 
 
 def _fill_cache(rng, num_pages, hkv, S, D, used_pages, valid_slots, kv_dtype,
-                scale_mode, amplitude=1.0, vfun=None):
+                scale_mode, amplitude=1.0, vfun=None, token_sigma=0.0):
     """Generate one paged cache (K or V) plus its scales.
 
     ``valid_slots[p]`` = number of leading valid slots of physical page p
-    (0 for unused pages). Invalid slots are NaN-poisoned.
+    (0 for unused pages). Invalid slots are NaN-poisoned. ``token_sigma`` > 0
+    multiplies each token's row by e^(token_sigma * N(0,1)), so token
+    magnitudes vary (the pages' check that catches a misplaced scale).
     """
     elt = 1 if kv_dtype == KV_FP8 else 2
     shape = (num_pages, hkv, S, D)
@@ -138,6 +143,8 @@ def _fill_cache(rng, num_pages, hkv, S, D, used_pages, valid_slots, kv_dtype,
     vals = rng.standard_normal((n_used, hkv, S, D), dtype=np.float32)
     if amplitude != 1.0:
         vals *= np.float32(amplitude)
+    if token_sigma > 0:
+        vals *= np.exp(np.float32(token_sigma) * rng.standard_normal((n_used, hkv, S, 1), dtype=np.float32))
     if vfun is not None:
         vals = vfun(used_pages, vals)
     slot_ok = np.arange(S)[None, :] < valid_slots[used_pages][:, None]  # [n_used, S]
@@ -172,8 +179,12 @@ def _fill_cache(rng, num_pages, hkv, S, D, used_pages, valid_slots, kv_dtype,
 def make_dense(name, *, batch, hkv, group, head_dim, query_len, page_size,
                ctx_lens, kv_dtype, scale_mode, seed, pool_pages=None,
                causal=1, window=0, with_sinks=False, max_pages=None,
-               v_amplitude=1.0, vfun=None):
-    """Build a dense paged-decode workload with the given context lengths."""
+               v_amplitude=1.0, vfun=None, q_amplitude=1.0, token_sigma=0.0):
+    """Build a dense paged-decode workload with the given context lengths.
+
+    ``q_amplitude`` scales the N(0,1) query values before BF16 rounding (large
+    logits); ``token_sigma`` > 0 varies K and V token magnitudes by
+    e^(token_sigma * N(0,1)); ``v_amplitude`` scales V."""
     rng = np.random.default_rng(seed)
     ctx_lens = np.asarray(ctx_lens, dtype=np.int32)
     need = (ctx_lens.astype(np.int64) + page_size - 1) // page_size
@@ -188,11 +199,15 @@ def make_dense(name, *, batch, hkv, group, head_dim, query_len, page_size,
         for j in range(int(need[b])):
             valid[table[b, j]] = min(page_size, L - j * page_size)
     hq = hkv * group
-    q = bf16_bits(rng.standard_normal((batch * query_len, hq, head_dim), dtype=np.float32))
+    qv = rng.standard_normal((batch * query_len, hq, head_dim), dtype=np.float32)
+    if q_amplitude != 1.0:
+        qv *= np.float32(q_amplitude)
+    q = bf16_bits(qv)
     kc, ks = _fill_cache(rng, pool_pages, hkv, page_size, head_dim, used, valid,
-                         kv_dtype, scale_mode)
+                         kv_dtype, scale_mode, token_sigma=token_sigma)
     vc, vs = _fill_cache(rng, pool_pages, hkv, page_size, head_dim, used, valid,
-                         kv_dtype, scale_mode, amplitude=v_amplitude, vfun=vfun)
+                         kv_dtype, scale_mode, amplitude=v_amplitude, vfun=vfun,
+                         token_sigma=token_sigma)
     sinks = rng.standard_normal(hq, dtype=np.float32) if with_sinks else None
     if kv_dtype == KV_BF16:
         scale_mode = SCALE_NONE
@@ -290,6 +305,50 @@ def sparse(seed: int = 1004, kv_dtype: int = KV_FP8, rows: int = 64,
     return Workload(name="sparse", batch=rows, num_q_heads=hq, num_kv_heads=hkv,
                     head_dim=head_dim, query_len=1, page_size=page_size,
                     num_pages=pool_pages, max_pages_per_seq=max_pages,
+                    kv_dtype=kv_dtype, scale_mode=smode, q=q, k_cache=kc,
+                    v_cache=vc, block_table=table, ctx_lens=ctx, k_scale=ks,
+                    v_scale=vs, causal=0, window=0, sinks=None, topk=topk,
+                    topk_idx=idx, seed=seed)
+
+
+def sparse_prefill(seed: int = 1006, kv_dtype: int = KV_FP8, rows: int = 1024,
+                   topk: int = 2048, pool_pages: int = 4096, page_size: int = 16,
+                   head_dim: int = 128, group: int = 16) -> Workload:
+    """Sparse prefill: one prompt of ``rows`` tokens, each query row r its own
+    decode row (query length 1) whose context is the prompt's first r + 1
+    tokens; row r lists min(r + 1, topk) token indices out of [0, r] (all of
+    them while r < topk, else a sorted sample without replacement), the rest
+    of its index row is -1. The prompt's pages come from one random
+    permutation of a ``pool_pages`` page16 pool and every row shares its block
+    table (PR "Merge gfx1250 PA decode partitions in the tile kernel and speed
+    up dense decode", Performance: prefill rows see min(row + 1, 2048) tokens)."""
+    rng = np.random.default_rng(seed)
+    hkv = 1
+    n_pages = (rows + page_size - 1) // page_size
+    if n_pages + 1 > pool_pages:
+        raise ValueError("page pool too small")
+    perm = rng.permutation(pool_pages).astype(np.int32)
+    pages = perm[:n_pages]
+    table = np.broadcast_to(pages, (rows, n_pages)).copy()
+    ctx = np.arange(1, rows + 1, dtype=np.int32)
+    idx = np.full((rows, topk), -1, dtype=np.int32)
+    for r in range(rows):
+        n = min(r + 1, topk)
+        if n == r + 1:
+            idx[r, :n] = np.arange(n, dtype=np.int32)
+        else:
+            idx[r, :n] = np.sort(rng.choice(r + 1, size=n, replace=False)).astype(np.int32)
+    valid = np.zeros(pool_pages, dtype=np.int64)
+    for j, pg in enumerate(pages):
+        valid[pg] = min(page_size, rows - j * page_size)
+    hq = hkv * group
+    q = bf16_bits(rng.standard_normal((rows, hq, head_dim), dtype=np.float32))
+    smode = SCALE_PER_TENSOR if kv_dtype == KV_FP8 else SCALE_NONE
+    kc, ks = _fill_cache(rng, pool_pages, hkv, page_size, head_dim, pages, valid, kv_dtype, smode)
+    vc, vs = _fill_cache(rng, pool_pages, hkv, page_size, head_dim, pages, valid, kv_dtype, smode)
+    return Workload(name="sparse_prefill", batch=rows, num_q_heads=hq, num_kv_heads=hkv,
+                    head_dim=head_dim, query_len=1, page_size=page_size,
+                    num_pages=pool_pages, max_pages_per_seq=n_pages,
                     kv_dtype=kv_dtype, scale_mode=smode, q=q, k_cache=kc,
                     v_cache=vc, block_table=table, ctx_lens=ctx, k_scale=ks,
                     v_scale=vs, causal=0, window=0, sinks=None, topk=topk,

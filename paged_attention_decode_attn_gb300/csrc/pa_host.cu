@@ -4,9 +4,10 @@
 
 #include <cmath>
 #include <cstdarg>
-#include <new>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
+#include <new>
 #include <string>
 
 #include "pa_decode.h"
@@ -43,15 +44,18 @@ struct pa_plan {
   pa::PaParams base;
   const void* tile_fn = nullptr;
   const void* reduce_fn = nullptr;
-  bool attrs_set = false;
   void* ws = nullptr;
   size_t ws_bytes = 0;
   size_t off_part_o = 0, off_part_ml = 0, off_counters = 0, off_desc = 0, off_status = 0;
-  // TMA descriptor cache (re-encoded when the cache pointers change)
-  const void* tm_k = nullptr;
-  const void* tm_v = nullptr;
-  CUtensorMap tmK, tmV;
-  bool tm_valid = false;
+  // Launch cache: kernel attributes set once per plan, TMA descriptors of the
+  // last cache pointers. A decode takes the plan as const; this cache is the
+  // only state it updates, under the plan's own lock.
+  mutable std::mutex cache_mu;
+  mutable bool attrs_set = false;
+  mutable const void* tm_k = nullptr;
+  mutable const void* tm_v = nullptr;
+  mutable CUtensorMap tmK, tmV;
+  mutable bool tm_valid = false;
 };
 
 namespace {
@@ -437,9 +441,12 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   return PA_OK;
 }
 
-pa_status set_kernel_attrs(pa_plan* pl) {
+// Kernel attributes (dynamic shared memory, non-portable cluster size) are
+// set once per plan, on the plan's device. Caller holds pl->cache_mu.
+pa_status set_kernel_attrs(const pa_plan* pl) {
   if (pl->attrs_set) return PA_OK;
-  cudaError_t e = cudaSetDevice(pl->desc.device);
+  pa::DeviceGuard guard(pl->desc.device);
+  cudaError_t e = guard.error();
   if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
   e = cudaFuncSetAttribute(pl->tile_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl->info.smem_bytes);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
@@ -483,10 +490,10 @@ pa_status encode_cache_map(const pa_plan* pl, const void* base, CUtensorMap* tm)
   return PA_OK;
 }
 
-pa_status launch(const pa_plan* cpl, void* out, const void* q, const void* k_cache, const void* v_cache,
+// Validate the call and launch the plan's kernel(s) on workspace `ws`.
+pa_status launch(const pa_plan* pl, void* ws_ptr, void* out, const void* q, const void* k_cache, const void* v_cache,
                  const int32_t* block_table, const int32_t* ctx_lens, const int32_t* topk_idx, const float* k_scale,
                  const float* v_scale, int window, const float* sinks, void* stream) {
-  pa_plan* pl = const_cast<pa_plan*>(cpl);
   const pa_plan_desc& d = pl->desc;
   if (d.batch == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !block_table || !ctx_lens)
@@ -500,20 +507,27 @@ pa_status launch(const pa_plan* cpl, void* out, const void* q, const void* k_cac
   if (window < 0) return fail(PA_ERR_INVALID_ARG, "window must be >= 0");
   if (window > 0 && !d.causal && d.query_len > 1)
     return fail(PA_ERR_UNSUPPORTED, "a window with non-causal multi-token queries is not defined");
-  if (!pl->ws) return fail(PA_ERR_WORKSPACE, "no workspace bound to the plan");
-  pa_status st = set_kernel_attrs(pl);
-  if (st != PA_OK) return st;
-  if (!pl->tm_valid || pl->tm_k != k_cache || pl->tm_v != v_cache) {
-    st = encode_cache_map(pl, k_cache, &pl->tmK);
+  if (!ws_ptr) return fail(PA_ERR_WORKSPACE, "no workspace bound to the plan");
+  CUtensorMap tmK, tmV;
+  {
+    std::lock_guard<std::mutex> lock(pl->cache_mu);
+    pa_status st = set_kernel_attrs(pl);
     if (st != PA_OK) return st;
-    st = encode_cache_map(pl, v_cache, &pl->tmV);
-    if (st != PA_OK) return st;
-    pl->tm_k = k_cache;
-    pl->tm_v = v_cache;
-    pl->tm_valid = true;
+    if (!pl->tm_valid || pl->tm_k != k_cache || pl->tm_v != v_cache) {
+      pl->tm_valid = false;
+      st = encode_cache_map(pl, k_cache, &pl->tmK);
+      if (st != PA_OK) return st;
+      st = encode_cache_map(pl, v_cache, &pl->tmV);
+      if (st != PA_OK) return st;
+      pl->tm_k = k_cache;
+      pl->tm_v = v_cache;
+      pl->tm_valid = true;
+    }
+    tmK = pl->tmK;
+    tmV = pl->tmV;
   }
   pa::PaParams p = pl->base;
-  uint8_t* ws = static_cast<uint8_t*>(pl->ws);
+  uint8_t* ws = static_cast<uint8_t*>(ws_ptr);
   p.out = static_cast<uint16_t*>(out);
   p.q = static_cast<const uint16_t*>(q);
   p.block_table = block_table;
@@ -544,7 +558,7 @@ pa_status launch(const pa_plan* cpl, void* out, const void* q, const void* k_cac
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  void* args[] = {&p, &pl->tmK, &pl->tmV};
+  void* args[] = {&p, &tmK, &tmV};
   cudaError_t e = cudaLaunchKernelExC(&cfg, pl->tile_fn, args);
   if (e != cudaSuccess) return cuda_fail(e, "tile kernel launch");
   if (pl->info.merge_mode == PA_MERGE_REDUCER) {
@@ -565,15 +579,14 @@ pa_status launch(const pa_plan* cpl, void* out, const void* q, const void* k_cac
 namespace pa {
 
 // Decode with an explicit workspace in place of the plan's bound one. The
-// plan itself is not modified (a stack copy carries the workspace pointer).
+// plan's launch cache (kernel attributes, tensor maps) is shared with
+// pa_decode; its bound workspace is neither used nor changed.
 pa_status launch_on_workspace(const pa_plan* plan, void* ws, size_t ws_bytes, void* out, const void* q,
                               const void* k_cache, const void* v_cache, const int32_t* block_table,
                               const int32_t* ctx_lens, const float* k_scale, const float* v_scale, int window,
                               const float* sinks, void* stream) {
-  pa_plan local = *plan;
-  local.ws = ws;
-  local.ws_bytes = ws_bytes;
-  return launch(&local, out, q, k_cache, v_cache, block_table, ctx_lens, nullptr, k_scale, v_scale, window, sinks,
+  if (ws_bytes < plan->info.workspace_bytes) return fail(PA_ERR_WORKSPACE, "scratch smaller than the plan's workspace");
+  return launch(plan, ws, out, q, k_cache, v_cache, block_table, ctx_lens, nullptr, k_scale, v_scale, window, sinks,
                 stream);
 }
 
@@ -616,8 +629,11 @@ pa_status pa_plan_create(const pa_plan_desc* desc, pa_plan_t** out) {
     st = set_kernel_attrs(pl);
     int n = 0;
     if (st == PA_OK) {
-      cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pl->tile_fn, pl->info.block_threads,
-                                                                    pl->info.smem_bytes);
+      pa::DeviceGuard guard(desc->device);
+      cudaError_t e = guard.error();
+      if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pl->tile_fn, pl->info.block_threads,
+                                                         pl->info.smem_bytes);
       if (e != cudaSuccess) st = cuda_fail(e, "occupancy query");
     }
     if (st == PA_OK) {
@@ -664,8 +680,8 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
                     const float* sinks, const pa_plan_t* plan, void* stream) {
   if (!plan) return fail(PA_ERR_INVALID_ARG, "null plan");
   if (plan->desc.sparse_topk > 0) return fail(PA_ERR_INVALID_ARG, "the plan is for sparse decode");
-  return launch(plan, out, q, k_cache, v_cache, block_table, ctx_lens, nullptr, k_scale, v_scale, window, sinks,
-                stream);
+  return launch(plan, plan->ws, out, q, k_cache, v_cache, block_table, ctx_lens, nullptr, k_scale, v_scale, window,
+                sinks, stream);
 }
 
 pa_status pa_decode_sparse(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -675,7 +691,8 @@ pa_status pa_decode_sparse(void* out, const void* q, const void* k_cache, const 
   if (!plan) return fail(PA_ERR_INVALID_ARG, "null plan");
   if (plan->desc.sparse_topk == 0) return fail(PA_ERR_INVALID_ARG, "the plan is for dense decode");
   if (!topk_idx) return fail(PA_ERR_INVALID_ARG, "null topk_idx");
-  return launch(plan, out, q, k_cache, v_cache, block_table, ctx_lens, topk_idx, k_scale, v_scale, 0, sinks, stream);
+  return launch(plan, plan->ws, out, q, k_cache, v_cache, block_table, ctx_lens, topk_idx, k_scale, v_scale, 0, sinks,
+                stream);
 }
 
 const char* pa_strerror(pa_status s) {

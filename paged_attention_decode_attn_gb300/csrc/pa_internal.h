@@ -84,6 +84,28 @@ struct pa_plan;
 
 namespace pa {
 
+// Makes `device` current for the guard's lifetime and restores the caller's
+// current device on every return path.
+class DeviceGuard {
+ public:
+  explicit DeviceGuard(int device) {
+    err_ = cudaGetDevice(&prev_);
+    if (err_ == cudaSuccess && prev_ != device) {
+      err_ = cudaSetDevice(device);
+      switched_ = err_ == cudaSuccess;
+    }
+  }
+  ~DeviceGuard() {
+    if (switched_) (void)cudaSetDevice(prev_);
+  }
+  cudaError_t error() const { return err_; }
+
+ private:
+  int prev_ = 0;
+  bool switched_ = false;
+  cudaError_t err_ = cudaSuccess;
+};
+
 // Host helpers shared with the no-allocation entry point (pa_noalloc.cu).
 pa_status launch_on_workspace(const pa_plan* plan, void* ws, size_t ws_bytes, void* out, const void* q,
                               const void* k_cache, const void* v_cache, const int32_t* block_table,

@@ -40,7 +40,8 @@ pa_status scratch_address(int device, void** out) {
   if (device < 0 || device >= kMaxDevices) return pa::set_error(PA_ERR_INVALID_ARG, "device ordinal out of range");
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
   if (!g_scratch_addr[device]) {
-    cudaError_t e = cudaSetDevice(device);
+    pa::DeviceGuard guard(device);  // restores the caller's current device on return
+    cudaError_t e = guard.error();
     if (e != cudaSuccess) return pa::set_error(PA_ERR_CUDA, cudaGetErrorString(e));
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);

@@ -84,3 +84,16 @@ def test_mtp4_full(orc, kv, consumer):
     w = pw.mtp4(kv_dtype=kv)
     gpu, plan = decode(DeviceWorkload(w), max_context_len=65536, consumer=consumer)
     check(orc, w, gpu, 6, seed=kv)
+
+
+@pytest.mark.parametrize("rows,kv", [(1024, pw.KV_FP8), (1024, pw.KV_BF16), (8192, pw.KV_FP8)],
+                         ids=["1024-fp8", "1024-bf16", "8192-fp8"])
+def test_sparse_prefill_full(orc, rows, kv):
+    """Sparse prefill at the pages' row counts, in the benchmark's automatic
+    plan; checked on sampled rows, always including the first, the row where
+    the 2048-token cap starts, and the last."""
+    w = pw.sparse_prefill(kv_dtype=kv, rows=rows)
+    gpu, plan = decode(DeviceWorkload(w))
+    assert plan.info["launches_per_call"] == 1
+    include = [0, 1, min(2047, rows - 1), min(2048, rows - 1), rows - 1]
+    check(orc, w, gpu, 48, seed=rows, include=include)

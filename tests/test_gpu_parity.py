@@ -177,3 +177,18 @@ def test_sparse_per_token_and_sinks(orc):
     w = base.with_(topk=200, topk_idx=idx)
     gpu, _ = decode(DeviceWorkload(w))
     assert_parity(gpu, orc.decode(w), what="sparse per-token sinks")
+
+
+@pytest.mark.parametrize("kv", [pw.KV_FP8, pw.KV_BF16], ids=["fp8", "bf16"])
+def test_sparse_prefill_small(orc, kv):
+    """Sparse prefill: row r of a 300-token prompt attends to min(r + 1, 128)
+    of its first r + 1 tokens (one-slot plans write their rows directly;
+    split rows merge through every mechanism)."""
+    w = pw.sparse_prefill(kv_dtype=kv, rows=300, topk=128, pool_pages=64, seed=77)
+    ref = orc.decode(w)
+    dw = DeviceWorkload(w)
+    for m in SPARSE_MODES:
+        gpu, plan = decode(dw, **m)
+        assert_parity(gpu, ref, what=f"sparse prefill {m}")
+    gpu, plan = decode(dw)
+    assert plan.info["merge_mode"] == pa.PA_MERGE_DIRECT  # rows >> SMs: one slot per row
