@@ -66,7 +66,7 @@ def measured_peak_gbs():
 # plus the shared header and the host code that sets its launch.
 KERNEL_SOURCES = {
     "pa_tile": ("pa_tile.cuh", "pa_tile_fp8_d128.cu", "pa_tile_fp8_d256.cu", "pa_tile_bf16.cu"),
-    "pa_umma": ("pa_tile.cuh", "pa_umma.cuh", "pa_umma_fp8.cu", "pa_umma_bf16.cu"),
+    "pa_mtp": ("pa_tile.cuh", "pa_tc.cuh", "pa_mtp.cuh", "pa_mtp_fp8.cu", "pa_mtp_bf16.cu"),
     "pa_reduce": ("pa_tile.cuh", "pa_reduce.cu"),
 }
 SHARED_SOURCES = ("pa_internal.h", "pa_host.cu")
@@ -100,7 +100,9 @@ def profiled_traffic(workload: str = "dense", kernel: str = "pa_tile"):
         return None
     m_hash = re.search(r"source_hash:\s*([0-9a-f]+)", text)
     m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(kernel):
+    if not m_hash or not m_bytes or kernel not in KERNEL_SOURCES:
+        return None
+    if m_hash.group(1) != kernel_source_hash(kernel):
         return None
     return int(m_bytes.group(1))
 
@@ -260,11 +262,11 @@ def make_workload(args, rank):
     if args.workload == "tiny":
         return pw.tiny()
     if args.workload == "d256":
-        return pw.d256(query_len=args.ql, window=args.window, with_sinks=args.sinks)
+        return pw.d256(query_len=args.ql, window=args.window, with_sinks=args.sinks, batch=args.batch or 16)
     if args.workload == "sparse":
         return pw.sparse(kv_dtype=kv)
     if args.workload == "mtp4":
-        return pw.mtp4(kv_dtype=kv)
+        return pw.mtp4(kv_dtype=kv, batch=args.batch or 32)
     if args.workload == "sparse_prefill":
         return pw.sparse_prefill(kv_dtype=kv, rows=args.rows)
     raise ValueError(args.workload)
@@ -341,6 +343,8 @@ def main():
                     help="the headline line uses the default dense workload; the others are for profiling")
     ap.add_argument("--kv", default="fp8", choices=["fp8", "bf16"], help="sparse and mtp4 cache format")
     ap.add_argument("--rows", type=int, default=1024, help="sparse_prefill: prompt rows")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="mtp4/d256: batch override (a smaller case for profiler captures; 0 = the workload's)")
     ap.add_argument("--no-warm", action="store_true", help="skip the warm CUDA-graph timing")
     ap.add_argument("--ql", type=int, default=1, help="d256: query length (MTP rows)")
     ap.add_argument("--window", type=int, default=0, help="d256: sliding window (0 = off)")
@@ -456,7 +460,7 @@ def main():
 
     if rank == 0:
         peak, peak_kind = measured_peak_gbs()
-        kernel_name = "pa_umma_kernel" if plan.info["consumer"] == pa.PA_CONSUMER_TMEM else "pa_tile_kernel"
+        kernel_name = "pa_mtp_kernel" if plan.info["consumer"] == pa.PA_CONSUMER_TMEM else "pa_tile_kernel"
         per_launch_us = float(np.mean(per_call_ms)) * 1000.0
         achieved = alg / (per_launch_us * 1e-6) / 1e9
         value = tot_bytes / tot_s / 1e9

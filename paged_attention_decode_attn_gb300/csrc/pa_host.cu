@@ -71,26 +71,26 @@ constexpr int kSmemOnePerSm = 226 * 1024;
 
 struct KernelShape {
   int nt, rw, wr, wt, ncw, rpad, elt, rb, nch, tt, tw, bh;
+  int rh;  // tensor-memory consumer: query rows per softmax warpgroup
   bool vtok, umma;
 };
 
 // Groups of more than 16 query rows per KV head (MTP verify, wide GQA) on
-// dense decode can run the tensor-memory (tcgen05) consumer: eight warps,
-// one 64-row MMA block.
+// dense decode can run the tensor-memory (tcgen05) consumer: two softmax
+// warpgroups over one MMA block of up to 64 rows, a producer warp and an
+// MMA-issue warp.
 bool umma_supported(const pa_plan_desc& d, int R) {
   if (d.sparse_topk > 0 || R <= 16) return false;
   if (d.kv_dtype == PA_KV_FP8_E4M3) return d.head_dim == 128 || d.head_dim == 256;
   return d.head_dim == 128;
 }
-// AUTO takes the tensor-memory consumer where it measured faster: FP8 caches
-// at head_dim 128 (GQA16 x MTP4: 0.74 ms against 1.09 ms per call). At head_dim
-// 256 and on BF16 caches the tile consumer is still as fast or faster.
+// AUTO takes the tensor-memory consumer wherever it covers the shape.
 bool use_umma(const pa_plan_desc& d, int R) {
   if (d.consumer == PA_CONSUMER_TILE || !umma_supported(d, R)) return false;
-  if (d.consumer == PA_CONSUMER_TMEM) return true;
-  return d.kv_dtype == PA_KV_FP8_E4M3 && d.head_dim == 128;
+  return true;
 }
-constexpr int kUmmaRows = 64;
+constexpr int kMtpThreads = 320;  // 8 softmax warps, the producer warp, the MMA warp
+constexpr int kMtpTokens = 128;   // tokens per stage (M of S^T)
 
 KernelShape kernel_shape(const pa_plan_desc& d) {
   KernelShape k;
@@ -112,18 +112,21 @@ KernelShape kernel_shape(const pa_plan_desc& d) {
   int tt = 32768 / (2 * k.rb);
   k.tt = tt < 16 ? 16 : (tt > 128 ? 128 : tt);
   k.tw = (d.kv_dtype == PA_KV_FP8_E4M3 && d.head_dim == 128) ? 2 : 1;
-  k.bh = d.page_size < k.tt ? d.page_size : k.tt;
   k.vtok = d.kv_dtype == PA_KV_FP8_E4M3 && d.scale_mode == PA_SCALE_PER_TOKEN;
   k.umma = use_umma(d, R);
+  k.rh = 0;
   if (k.umma) {
-    // rows 16*w .. 16*w + 15 belong to consumer warp w (M = 64 TMEM layout)
+    // warpgroup w owns rows [w*rh, (w+1)*rh); 128-token stages (M = 128)
+    k.rh = R <= 32 ? 16 : 32;
     k.nt = 2;
-    k.rw = 16;
-    k.wr = 4;
-    k.wt = 2;  // warps w and w + 4 split each token's row scores
+    k.rw = k.rh;
+    k.wr = 2;
+    k.wt = 4;  // the four warps of a warpgroup split each stage's tokens
     k.ncw = 8;
     k.rpad = (R + 7) / 8 * 8;
+    k.tt = kMtpTokens;
   }
+  k.bh = d.page_size < k.tt ? d.page_size : k.tt;
   return k;
 }
 
@@ -135,54 +138,51 @@ pa::SmemLayout smem_layout(const pa_plan_desc& d, const KernelShape& k, int ns, 
   L.off_stage = 0;
   size_t off = (size_t)ns * L.stage_bytes;
   L.off_k16 = L.off_v16 = L.off_q16 = L.off_p16 = 0;
-  if (k.umma) {
-    // 1024-aligned 16-bit operands (stage_bytes is a multiple of 1024)
-    // FP8 head_dim 128 runs FP8 MMAs on the stage itself; other FP8 shapes
-    // convert K and V to FP16 operands
-    const bool f8mma = d.kv_dtype == PA_KV_FP8_E4M3 && d.head_dim == 128 && !k.vtok;
-    if (d.kv_dtype == PA_KV_FP8_E4M3 && !f8mma) {
-      L.off_k16 = (int)off;
-      off += (size_t)k.tt * d.head_dim * 2;
-      L.off_v16 = (int)off;
-      off += (size_t)k.tt * d.head_dim * 2;
-    }
-    L.off_q16 = (int)off;
-    off += (size_t)kUmmaRows * d.head_dim * 2;
-    // P^T ([tokens][64 rows]), its unscaled copy under per-token V scales,
-    // then a 16 x tokens operand of ones for the row sums
-    L.off_p16 = (int)off;
-    off += (size_t)(k.vtok ? 2 : 1) * k.tt * kUmmaRows * 2 + (size_t)16 * k.tt * (f8mma ? 1 : 2);
-  }
   L.off_merge = (int)off;
   L.off_cpart = (int)off;  // cluster merge: this CTA's partial (O, then max/sum)
-  if (cluster) off += align_up((size_t)k.rpad * d.head_dim * 4 + (size_t)k.rpad * 8, 128);
+  if (k.umma) {
+    // Q operand (FP8: three e4m3 terms of [D/128 chunks][RN rows][128 B];
+    // BF16: [D/64 chunks][RN rows][128 B]), then two P^T buffers of
+    // [128 tokens][128 B] and the 8 KiB ones operand, 1024-aligned
+    const int rn = 2 * k.rh;
+    const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
+    L.off_q16 = (int)off;
+    off += fp8 ? (size_t)3 * d.head_dim * rn : (size_t)2 * d.head_dim * rn;
+    off = align_up(off, 1024);
+    L.off_p16 = (int)off;
+    off += (size_t)2 * k.tt * 128 + 8192;
+    // the cluster partial reuses the ring, idle once the CTA's work is done
+    L.off_cpart = 0;
+  } else if (cluster) {
+    off += align_up((size_t)k.rpad * d.head_dim * 4 + (size_t)k.rpad * 8, 128);
+  }
   L.off_hdr = (int)off;
   off += (size_t)ns * 128;
   L.off_bar = (int)off;
   off += (size_t)ns * 16 + 32;  // full/empty per stage, then full/empty per Q slot
-  L.off_ubar = (int)off;  // tcgen05 commit barriers (S, O)
-  off += 16;
+  L.off_ubar = (int)off;  // tensor-memory consumer: its ten pipeline barriers
+  off += k.umma ? 128 : 16;
   L.off_tslot = (int)off;  // tensor-memory address written by tcgen05.alloc
   off += 16;
-  L.off_rows = (int)off;  // tcgen05 consumer: per-row state (8 x 64 words) and 4 flags
-  off += k.umma ? (size_t)(8 * kUmmaRows + 4) * 4 : 0;
+  L.off_rows = (int)off;  // tensor-memory consumer: per-row state (8 x 64 words)
+  off += k.umma ? (size_t)8 * 64 * 4 : 0;
   off = align_up(off, 16);
   L.off_misc = (int)off;
   off += 64;
   L.off_pend = (int)off;  // queued last-arriver merges: 8 entries of 32 bytes
   off += 8 * 32;
   L.off_mml = (int)off;  // (max, sum) of the token-group warps at a segment end
-  off += align_up((size_t)k.wt * k.rpad * 8, 128);
+  off += k.umma ? 0 : align_up((size_t)k.wt * k.rpad * 8, 128);
   L.q_slot_bytes = k.rpad * d.head_dim * 2;  // a unit's BF16 query rows
   L.nq = nq;
-  L.off_q = (int)off;
-  off += (size_t)nq * L.q_slot_bytes;
+  L.off_q = (int)align_up(off, 16);
+  off = (size_t)L.off_q + (size_t)nq * L.q_slot_bytes;
   L.total = (int)(off + 1024);  // slack for aligning the base to 1024 bytes
   return L;
 }
 
 const void* pick_tile_kernel(const pa_plan_desc& d, const KernelShape& k) {
-  if (k.umma) return pa::umma_kernel(d.kv_dtype == PA_KV_FP8_E4M3, d.head_dim, k.vtok);
+  if (k.umma) return pa::mtp_kernel(d.kv_dtype == PA_KV_FP8_E4M3, d.head_dim, k.vtok, k.rh);
   if (d.kv_dtype == PA_KV_FP8_E4M3) {
     if (d.head_dim == 128) return pa::tile_kernel_fp8_d128(k.vtok, k.ncw > 4);
     return k.ncw > 4 ? nullptr : pa::tile_kernel_fp8_d256(k.vtok);
@@ -259,7 +259,12 @@ pa_status resolve_schedule(const pa_plan_desc& d, const KernelShape& k, int sm_c
     if (sched == PA_SCHED_BALANCED) return fail(PA_ERR_INVALID_ARG, "cluster merge needs the per-unit schedule");
     sched = PA_SCHED_PER_UNIT;
   }
-  if (sched == PA_SCHED_AUTO) sched = d.sparse_topk > 0 ? PA_SCHED_PER_UNIT : PA_SCHED_BALANCED;
+  // Sparse decode splits each row over P CTAs while the rows leave resident
+  // CTA slots free; with more rows than slots (sparse prefill) a persistent
+  // balanced grid streams them, as dense decode does.
+  if (sched == PA_SCHED_AUTO)
+    sched = (d.sparse_topk > 0 && (long long)units <= (long long)sm_count * ctas_per_sm) ? PA_SCHED_PER_UNIT
+                                                                                         : PA_SCHED_BALANCED;
   if (sched == PA_SCHED_PER_UNIT) {
     if (P == 0) {
       // Fill the resident CTA slots once: P = slots / units, in [1, 16], and
@@ -312,7 +317,7 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   int budget = kSmemTwoPerSm;
   for (int attempt = two_per_sm ? 0 : 1; attempt < 2 && ns < 3; ++attempt) {
     budget = attempt == 0 ? kSmemTwoPerSm : kSmemOnePerSm;
-    for (nq = 2; nq >= 1; --nq) {
+    for (nq = k.umma ? 1 : 2; nq >= 1; --nq) {
       const pa::SmemLayout l0 = smem_layout(d, k, 0, d.sparse_topk > 0 || d.merge_mode == PA_MERGE_CLUSTER, nq);
       const int stage = l0.stage_bytes + 128 + 16;
       ns = (budget - l0.total) / stage;
@@ -374,7 +379,7 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   in.rows_per_warp = k.rw;
   in.row_warps = k.wr;
   in.token_warps = k.wt;
-  in.block_threads = (k.ncw + 1) * 32;
+  in.block_threads = k.umma ? kMtpThreads : (k.ncw + 1) * 32;
   in.grid = (int)grid;
   in.cluster = cluster ? P : 1;
   in.ctas_per_sm = ctas_per_sm;

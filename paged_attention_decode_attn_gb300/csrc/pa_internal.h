@@ -13,8 +13,11 @@ enum : int { kSchedBalanced = 1, kSchedPerUnit = 2 };
 enum : int { kMergeDirect = 1, kMergeCluster = 2, kMergeLastArriver = 3, kMergeReducer = 4 };
 enum : int { kScaleNone = 0, kScalePerTensor = 1, kScalePerToken = 2 };
 
-// Device status bits (int32 in the workspace).
-enum : int { kStatusTimeout = 1, kStatusBadPage = 2, kStatusInternal = 4 };
+// Device status bits (int32 in the workspace). kStatusScaleRange: a per-token
+// V scale of a visible token outside [-2048, 2048] on the tensor-memory
+// consumer (its FP16 V operand holds v * scale * 2^-4); that token's V is
+// taken as zero.
+enum : int { kStatusTimeout = 1, kStatusBadPage = 2, kStatusInternal = 4, kStatusScaleRange = 8 };
 
 // Stage header flags.
 enum : int { kSegFirst = 1, kSegLast = 2, kSegWhole = 4 };
@@ -75,8 +78,9 @@ const void* tile_kernel_fp8_d128(int vtok, int wide);
 const void* tile_kernel_fp8_d256(int vtok);
 const void* tile_kernel_bf16(int d, int wide);
 const void* reduce_kernel(int d);
-// tcgen05 consumer instantiations (FP8 head_dim 128/256, BF16 head_dim 128).
-const void* umma_kernel(int fp8, int d, int vtok);
+// Tensor-memory consumer instantiations (FP8 head_dim 128/256, BF16 head_dim
+// 128; rh = query rows per softmax warpgroup, 16 or 32).
+const void* mtp_kernel(int fp8, int d, int vtok, int rh);
 
 }  // namespace pa
 

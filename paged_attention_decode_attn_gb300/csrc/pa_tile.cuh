@@ -423,7 +423,7 @@ struct Producer {
   // sequence (same block-table row, same start)
   int first_base = 0, first_cur = -1, first_next = -1;
 
-  __device__ Producer(const PaParams& p_, const CUtensorMap* k, const CUtensorMap* v, Smem s)
+  __device__ __forceinline__ Producer(const PaParams& p_, const CUtensorMap* k, const CUtensorMap* v, Smem s)
       : p(p_), tmK(k), tmV(v), sm(s), lane(threadIdx.x & 31) {}
 
   __device__ __forceinline__ int load_pid(int b, int lp) const {
@@ -480,7 +480,7 @@ struct Producer {
     return got;
   }
 
-  __device__ void emit_dense(const StageHdr& h) {
+  __device__ __forceinline__ void emit_dense(const StageHdr& h) {
     int s;
     if (!acquire_stage(s)) return;
     const int S = p.S, TT = p.TT, BH = p.BH;
@@ -564,7 +564,7 @@ struct Producer {
     }
   }
 
-  __device__ void emit_sparse(StageHdr h) {
+  __device__ __forceinline__ void emit_sparse(StageHdr h) {
     int s;
     if (!acquire_stage(s)) return;
     const int TT = p.TT;
@@ -620,7 +620,9 @@ struct Producer {
         asm volatile("st.shared.f32 [%0], %1;" ::"r"(sc + TT * 4 + row * 4), "f"(vv) : "memory");
       }
     }
-    const uint32_t bytes = empty ? 0u : (uint32_t)TT * 128u * NCH * 2u;
+    // a stage none of whose index positions holds a token of [0, L) moves no bytes
+    const bool skip = empty || (h.mask[0] | h.mask[1] | h.mask[2] | h.mask[3]) == 0u;
+    const uint32_t bytes = skip ? 0u : (uint32_t)TT * 128u * NCH * 2u;
     __syncwarp();
     if (lane == 0) {
       *sm.hdr(s, p) = h;
@@ -630,7 +632,7 @@ struct Producer {
         mbar_arrive(sm.full(s, p));
     }
     __syncwarp();
-    if (!empty) {
+    if (!skip) {
       // lane q gathers stage rows 4q .. 4q+3 (round 4q / 32 of the y registers)
       int y4[4];
 #pragma unroll
@@ -673,7 +675,7 @@ struct Producer {
   // Query rows of unit (b, g) into Q ring slot nq % NQ: one bulk copy per
   // query position, since the G heads that share KV head g are contiguous.
   int nq = 0;
-  __device__ bool load_q(int b, int g) {
+  __device__ __forceinline__ bool load_q(int b, int g) {
     const int qs = nq % p.NQ;
     bool got = mbar_wait(sm.qempty(qs, p), ((nq / p.NQ) & 1) ^ 1);
     got = __all_sync(0xffffffffu, got);
@@ -695,7 +697,7 @@ struct Producer {
     return true;
   }
 
-  __device__ void emit_end() {
+  __device__ __forceinline__ void emit_end() {
     int s;
     if (!acquire_stage(s)) return;
     if (lane == 0) {
@@ -707,7 +709,7 @@ struct Producer {
   }
 
   // Emit the stages of one segment: chunks [k0, k1) of unit (b, g).
-  __device__ void segment(int b, int g, const UnitRange& r, int k0, int k1, bool whole, int slot, const MergeDesc& md) {
+  __device__ __forceinline__ void segment(int b, int g, const UnitRange& r, int k0, int k1, bool whole, int slot, const MergeDesc& md) {
     StageHdr h;
     h.unit = b * p.Hkv + g;
     h.b = b;
@@ -748,7 +750,7 @@ struct Producer {
     }
   }
 
-  __device__ void run() {
+  __device__ __forceinline__ void run() {
     if (lane == 0) {
       prefetch_tmap(tmK);
       prefetch_tmap(tmV);

@@ -27,14 +27,16 @@ def kernel_shape(d):
     tt = min(128, max(16, 32768 // (2 * rb)))
     tw = 2 if (d["kv_dtype"] == 0 and d["head_dim"] == 128) else 1
     k = dict(R=R, G=G, nt=nt, rw=rw, wr=wr, wt=wt, ncw=wr * wt, rpad=wr * rw, elt=elt, rb=rb,
-             tt=tt, tw=tw, bh=min(d["page_size"], tt), umma=False)
-    # more than 16 rows on dense decode: the tcgen05 consumer (4 warps of 16 rows)
+             tt=tt, tw=tw, bh=min(d["page_size"], tt), umma=False, rh=0)
+    # more than 16 rows on dense decode: the tensor-memory consumer (two
+    # softmax warpgroups of rh rows, 128-token stages), taken by AUTO
     supported = d.get("sparse_topk", 0) == 0 and R > 16 and (
         d["head_dim"] == 128 or (d["kv_dtype"] == 0 and d["head_dim"] == 256))
     consumer = d.get("consumer", 0)
-    auto_tmem = d["kv_dtype"] == 0 and d["head_dim"] == 128
-    if supported and (consumer == 2 or (consumer == 0 and auto_tmem)):
-        k.update(umma=True, nt=2, rw=16, wr=4, wt=2, ncw=8, rpad=-(-R // 8) * 8)
+    if supported and consumer in (0, 2):
+        rh = 16 if R <= 32 else 32
+        k.update(umma=True, rh=rh, nt=2, rw=rh, wr=2, wt=4, ncw=8, rpad=-(-R // 8) * 8, tt=128,
+                 bh=min(d["page_size"], 128))
     return k
 
 
@@ -42,19 +44,18 @@ def smem_total(d, k, ns, cluster, nq):
     stage = 2 * k["tt"] * k["rb"] + (1024 if d["scale_mode"] == 2 else 0)
     off = ns * stage
     if k["umma"]:
-        vtok = d["kv_dtype"] == 0 and d["scale_mode"] == 2
-        f8mma = d["kv_dtype"] == 0 and d["head_dim"] == 128 and not vtok  # FP8 MMAs on the stage itself
-        if d["kv_dtype"] == 0 and not f8mma:
-            off += 2 * k["tt"] * d["head_dim"] * 2  # 16-bit K and V operands
-        off += 64 * d["head_dim"] * 2  # Q operand (64 rows)
-        vtok = d["kv_dtype"] == 0 and d["scale_mode"] == 2
-        off += (2 if vtok else 1) * k["tt"] * 64 * 2 + 16 * k["tt"] * (1 if f8mma else 2)  # P^T (+ unscaled), ones
-    if cluster:
+        rn = 2 * k["rh"]
+        off += (3 if d["kv_dtype"] == 0 else 2) * d["head_dim"] * rn  # Q operand
+        off = align(off, 1024)
+        off += 2 * k["tt"] * 128 + 8192  # two P^T slots, the ones operand
+    elif cluster:
         off += align(k["rpad"] * d["head_dim"] * 4 + k["rpad"] * 8, 128)
-    off += ns * 128 + ns * 16 + 32 + 32
+    off += ns * 128 + ns * 16 + 32 + (128 if k["umma"] else 16) + 16
     if k["umma"]:
-        off = align(off + (8 * 64 + 4) * 4, 16)  # per-row state
-    off += 64 + 8 * 32 + align(k["wt"] * k["rpad"] * 8, 128)
+        off += 8 * 64 * 4  # per-row state
+    off = align(off, 16)
+    off += 64 + 8 * 32 + (0 if k["umma"] else align(k["wt"] * k["rpad"] * 8, 128))
+    off = align(off, 16)
     off += nq * k["rpad"] * d["head_dim"] * 2  # Q ring: nq slots of BF16 query rows
     return stage, off + 1024
 
@@ -69,7 +70,7 @@ def plan(d):
         if ns >= 3:
             break
         budget = SMEM_TWO if attempt == 0 else SMEM_ONE
-        for nq in (2, 1):
+        for nq in ((1,) if k["umma"] else (2, 1)):
             stage, total0 = smem_total(d, k, 0, cl0, nq)
             ns = min(8, (budget - total0) // (stage + 144))
             if ns >= 3:
@@ -83,7 +84,7 @@ def plan(d):
     if merge == 2:
         sched = 2
     if sched == 0:
-        sched = 2 if d.get("sparse_topk", 0) > 0 else 1
+        sched = 2 if (d.get("sparse_topk", 0) > 0 and units <= sm * cps) else 1
     if sched == 2:
         if P == 0:
             p = sm * cps // units if units > 0 else 1
@@ -121,7 +122,7 @@ def plan(d):
     off += 256
     return dict(merge_mode=merge, schedule=sched, num_partitions=P if sched == 2 else 0,
                 stage_tokens=k["tt"], num_stages=ns, rows=k["R"], rows_per_warp=k["rw"],
-                row_warps=k["wr"], token_warps=k["wt"], block_threads=(k["ncw"] + 1) * 32,
+                row_warps=k["wr"], token_warps=k["wt"], block_threads=320 if k["umma"] else (k["ncw"] + 1) * 32,
                 grid=grid, cluster=P if cluster else 1, ctas_per_sm=cps, sm_count=sm,
                 launches_per_call=2 if merge == 4 else 1, units=units, consumer=2 if k["umma"] else 1,
                 smem_bytes=smem,

@@ -1,5 +1,5 @@
 """The two-term e4m3 split used by the tensor-memory consumer's FP8 MMAs
-(pa_umma.cuh: e4m3_lead), restated with numpy and checked against torch's
+(pa_tc.cuh: e4m3_lead), restated with numpy and checked against torch's
 e4m3 (float8_e4m3fn) cast, which rounds to nearest-even with saturation.
 
 A value x is carried as hi + lo with hi = x rounded to 4 significant bits
