@@ -61,9 +61,12 @@ struct pa_plan {
 namespace {
 
 // A segment's fixed cost (query rows, token-group merge, output or partial
-// write) is about one stage of streaming; the balanced schedule charges it as
-// one virtual chunk per unit.
+// write) in stages of streaming, charged by the balanced schedule as virtual
+// chunks per unit: about one stage on the tile consumer; about four on the
+// tensor-memory consumer (Q split into its operand, pipeline drain, epilogue
+// through tensor memory).
 constexpr int kSegCostChunks = 1;
+constexpr int kSegCostChunksTmem = 4;
 // Largest dynamic shared memory a CTA may use while two CTAs share an SM, and
 // with one CTA per SM.
 constexpr int kSmemTwoPerSm = 112 * 1024;
@@ -142,15 +145,15 @@ pa::SmemLayout smem_layout(const pa_plan_desc& d, const KernelShape& k, int ns, 
   L.off_cpart = (int)off;  // cluster merge: this CTA's partial (O, then max/sum)
   if (k.umma) {
     // Q operand (FP8: three e4m3 terms of [D/128 chunks][RN rows][128 B];
-    // BF16: [D/64 chunks][RN rows][128 B]), then two P^T buffers of
-    // [128 tokens][128 B] and the 8 KiB ones operand, 1024-aligned
+    // BF16: [D/64 chunks][RN rows][128 B]), then the P^T slots of
+    // [128 tokens][128 B] and the 2 KiB ones operand, 1024-aligned
     const int rn = 2 * k.rh;
     const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
     L.off_q16 = (int)off;
     off += fp8 ? (size_t)3 * d.head_dim * rn : (size_t)2 * d.head_dim * rn;
     off = align_up(off, 1024);
     L.off_p16 = (int)off;
-    off += (size_t)2 * k.tt * 128 + 8192;
+    off += (size_t)(fp8 ? 3 : 2) * k.tt * 128 + 2048;  // P^T slots (FP8: three buffers; BF16: hi, lo), ones
     // the cluster partial reuses the ring, idle once the CTA's work is done
     L.off_cpart = 0;
   } else if (cluster) {
@@ -160,7 +163,7 @@ pa::SmemLayout smem_layout(const pa_plan_desc& d, const KernelShape& k, int ns, 
   off += (size_t)ns * 128;
   L.off_bar = (int)off;
   off += (size_t)ns * 16 + 32;  // full/empty per stage, then full/empty per Q slot
-  L.off_ubar = (int)off;  // tensor-memory consumer: its ten pipeline barriers
+  L.off_ubar = (int)off;  // tensor-memory consumer: its eleven pipeline barriers
   off += k.umma ? 128 : 16;
   L.off_tslot = (int)off;  // tensor-memory address written by tcgen05.alloc
   off += 16;
@@ -414,7 +417,7 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   p.sched = sched;
   p.merge = kernel_merge;
   p.C = sched == PA_SCHED_BALANCED ? (int)grid : 0;
-  p.seg_cost = sched == PA_SCHED_BALANCED ? kSegCostChunks : 0;
+  p.seg_cost = sched == PA_SCHED_BALANCED ? (k.umma ? kSegCostChunksTmem : kSegCostChunks) : 0;
   p.P = sched == PA_SCHED_PER_UNIT ? P : 0;
   p.TT = k.tt;
   p.NS = ns;

@@ -124,15 +124,42 @@ __device__ __forceinline__ float rowmax_transpose(float (&v)[RH], int lane) {
   return v[0];
 }
 
+// Maximum of N values as a tree of three-input maxima (fixed bounds, so the
+// temporaries stay in registers).
+template <int N>
+struct Max3Tree {
+  __device__ __forceinline__ static float run(const float (&a)[N]) {
+    constexpr int M = (N + 2) / 3;
+    float b[M];
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+      if (3 * i + 2 < N)
+        b[i] = fmax3(a[3 * i], a[3 * i + 1], a[3 * i + 2]);
+      else if (3 * i + 1 < N)
+        b[i] = fmaxf(a[3 * i], a[3 * i + 1]);
+      else
+        b[i] = a[3 * i];
+    }
+    return Max3Tree<M>::run(b);
+  }
+};
+template <>
+struct Max3Tree<1> {
+  __device__ __forceinline__ static float run(const float (&a)[1]) { return a[0]; }
+};
+
 // Pipeline barriers of the consumer (eight bytes each, from p.off_ubar).
 struct MtpBars {
   uint32_t base;
   __device__ __forceinline__ uint32_t s_full(int i) const { return base + 8u * i; }   // S(k) in TMEM
   __device__ __forceinline__ uint32_t s_free(int i) const { return base + 16u + 8u * i; }  // S(k) read
   __device__ __forceinline__ uint32_t p_full(int i) const { return base + 32u + 8u * i; }  // P(k), V(k) ready
-  __device__ __forceinline__ uint32_t pv_done(int i) const { return base + 48u + 8u * i; }  // PV(k) complete
-  __device__ __forceinline__ uint32_t q_ready() const { return base + 64u; }  // segment's Q operand written
-  __device__ __forceinline__ uint32_t drained() const { return base + 72u; }  // every MMA complete
+  // PV(k) complete, three barriers indexed k % 3: between two observations
+  // the softmax warps leave up to three PVs unobserved (their P buffers), so
+  // no barrier may complete twice in that window
+  __device__ __forceinline__ uint32_t pv_done(int i) const { return base + 48u + 8u * i; }
+  __device__ __forceinline__ uint32_t q_ready() const { return base + 72u; }  // segment's Q operand written
+  __device__ __forceinline__ uint32_t drained() const { return base + 80u; }  // every MMA complete
 };
 
 template <bool FP8, int D, bool VTOK, int RH>
@@ -145,11 +172,13 @@ struct MtpCfg {
   static constexpr int QTERMS = FP8 ? 3 : 1;
   static constexpr int QCH = FP8 ? D / 128 : D / 64;  // 128-byte chunks per query row of the Q operand
   static constexpr uint32_t kQTermBytes = (uint32_t)QCH * RN * 128u;
-  // P^T slots of [128 tokens][128 B]: FP8 caches keep one FP16 term in two
-  // buffers (P(k) is written while PV(k-1) reads the other); BF16 caches keep
-  // P as two BF16 terms hi + lo (about 16 significant bits) in one buffer.
+  // P^T slots of [128 tokens][128 B]: FP8 caches keep one FP16 term in three
+  // buffers (P(k) is written while PV(k-1) and PV(k-2) may still read the
+  // others); BF16 caches keep P as two BF16 terms hi + lo (about 16
+  // significant bits) in one buffer.
   static constexpr int PT = FP8 ? 1 : 2;  // terms
-  static constexpr int PB = FP8 ? 2 : 1;  // buffers
+  static constexpr int PB = FP8 ? 3 : 1;  // buffers
+  static constexpr int NP = PT * PB;      // slots
   // tensor-memory columns
   static constexpr uint32_t kColS = 0;           // S^T buffers: [0, RN) and [RN, 2 RN)
   static constexpr uint32_t kColO = 2 * RN;      // O^T: DCH blocks of RN columns
@@ -165,8 +194,8 @@ struct MtpCfg {
 
 // Shared-memory regions of the consumer (byte offsets from the aligned base):
 //   p.off_q16  Q operand: QTERMS x [QCH chunks][RN rows][128 B]
-//   p.off_p16  P^T: two slots of [128 tokens][128 B] (rows of warpgroup w at
-//              bytes [w*RH*2, (w+1)*RH*2)), then the ones operand (8 KiB)
+//   p.off_p16  P^T: NP slots of [128 tokens][128 B] (rows of warpgroup w at
+//              bytes [w*RH*2, (w+1)*RH*2)), then the ones operand (2 KiB)
 //   p.off_rows row state: c[64], m[64], pos[64], alpha[64], red[4][64]
 template <bool FP8, int D, bool VTOK, int RH>
 struct MtpSoftmax {
@@ -226,7 +255,7 @@ struct MtpSoftmax {
   // Wait until PV(x) has completed (completions are observed in order).
   __device__ __forceinline__ bool wait_pv(int x) {
     while (kd <= x) {
-      if (!mbar_wait(bars.pv_done(kd & 1), (kd >> 1) & 1)) {
+      if (!mbar_wait(bars.pv_done(kd % 3), (kd / 3) & 1)) {
         fail();
         return false;
       }
@@ -238,7 +267,11 @@ struct MtpSoftmax {
 
   // Build the segment's Q operand from the Q ring (rows past R are zeros),
   // the per-row score scale c_r and position, reset the reference max.
-  __device__ __forceinline__ bool begin_segment(int L) {
+  // has_tokens: the segment's first stage holds tokens. Only such segments
+  // signal q_ready (and only they make the MMA thread wait for it): an empty
+  // unit's segment never waits on the MMA thread, so signalling for it could
+  // complete two q_ready phases before the MMA thread observed the first.
+  __device__ __forceinline__ bool begin_segment(int L, bool has_tokens) {
     // every softmax thread is done with the previous segment's row state
     // (its epilogue reads row_m) before it is reset here
     named_bar(kBarStage, kMtpSoftThreads);
@@ -328,7 +361,7 @@ struct MtpSoftmax {
     named_bar(kBarStage, kMtpSoftThreads);
     __syncwarp();
     if (lane == 0) {
-      mbar_arrive(bars.q_ready());
+      if (has_tokens) mbar_arrive(bars.q_ready());
       mbar_arrive(sm.qempty(qs, p));
     }
     seg_k0 = k;
@@ -359,7 +392,6 @@ struct MtpSoftmax {
   // In place: y = s * c_r * ks - m_r (log2 units against the reference max),
   // -inf where masked; returns the largest y.
   __device__ __forceinline__ float scores(const StageView& h, bool interior, float ks, float (&y)[RH]) {
-    float mx = -INFINITY;
 #pragma unroll
     for (int i = 0; i < RH; i += 4) {
       const float4 c4 = lds128f(row_c_u32(wg * RH + i));
@@ -368,10 +400,7 @@ struct MtpSoftmax {
       const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
       if (interior) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          y[i + j] = fmaf(VTOK ? y[i + j] * ks : y[i + j], cc[j], -mm[j]);
-          mx = fmaxf(mx, y[i + j]);
-        }
+        for (int j = 0; j < 4; ++j) y[i + j] = fmaf(VTOK ? y[i + j] * ks : y[i + j], cc[j], -mm[j]);
       } else {
         const int4 p4 = lds128i(row_pos_u32(wg * RH + i));
         const int pos[4] = {p4.x, p4.y, p4.z, p4.w};
@@ -379,11 +408,10 @@ struct MtpSoftmax {
         for (int j = 0; j < 4; ++j) {
           const float v = fmaf(VTOK ? y[i + j] * ks : y[i + j], cc[j], -mm[j]);
           y[i + j] = visible(h, pos[j]) ? v : -INFINITY;
-          mx = fmaxf(mx, y[i + j]);
         }
       }
     }
-    return mx;
+    return Max3Tree<RH>::run(y);  // the largest y
   }
 
   // Slow path (all softmax threads): raise the reference max of rows whose
@@ -452,59 +480,55 @@ struct MtpSoftmax {
     return true;
   }
 
-  // This thread's share of the stage's V bytes (FP8 caches), read before the
-  // in-place conversion overwrites them.
-  static constexpr int kVUnits = TT * C::NCH * 8 / kMtpSoftThreads;  // 16-byte FP8 units per thread
-  __device__ __forceinline__ void load_v(uint32_t vst, uint4 (&w)[kVUnits]) const {
-#pragma unroll
-    for (int j = 0; j < kVUnits; ++j) {
-      const int e = threadIdx.x + j * kMtpSoftThreads;
-      const int t = e / (8 * C::NCH), cb = (e / 8) % C::NCH, cc = e % 8;
-      w[j] = lds128(vst + (uint32_t)(cb * TT + t) * 128u + (uint32_t)((cc ^ (t & 7)) << 4));
-    }
+  // This thread's FP8 V units (16 bytes each) of the stage: unit j is e =
+  // threadIdx.x + 256 j, token e / (8 NCH), 128-byte chunk (e / 8) % NCH,
+  // 16-byte column e % 8.
+  static constexpr int kVUnits = TT * C::NCH * 8 / kMtpSoftThreads;
+  __device__ __forceinline__ uint4 load_v_unit(uint32_t vst, int j) const {
+    const int e = threadIdx.x + j * kMtpSoftThreads;
+    const int t = e / (8 * C::NCH), cb = (e / 8) % C::NCH, cc = e % 8;
+    return lds128(vst + (uint32_t)(cb * TT + t) * 128u + (uint32_t)((cc ^ (t & 7)) << 4));
   }
-  // FP16 V^T operand over the stage's K and V bytes: [D/64 chunks][TT][128 B];
-  // tokens outside the stage's range become zeros (poisoned slots never reach
-  // the MMA); per-token V scales (times 2^-4) are folded in.
-  __device__ __forceinline__ void store_v16(uint32_t kst, uint32_t sst, const StageView& h,
-                                            const uint4 (&w)[kVUnits]) const {
-#pragma unroll
-    for (int j = 0; j < kVUnits; ++j) {
-      const int e = threadIdx.x + j * kMtpSoftThreads;
-      const int t = e / (8 * C::NCH), cb = (e / 8) % C::NCH, cc = e % 8;
-      const bool in = h.tbase + t >= h.t0 && h.tbase + t < h.t1;
-      const int dim0 = cb * 128 + 16 * cc;
-      const uint32_t dst =
-          kst + (uint32_t)(dim0 / 64) * (TT * 128u) + (uint32_t)t * 128u + (uint32_t)(((((dim0 % 64) / 8)) ^ (t & 7)) << 4);
-      uint4 lo, hi;
-      lo.x = e4m3x2_to_f16x2(w[j].x & 0xFFFFu);
-      lo.y = e4m3x2_to_f16x2(w[j].x >> 16);
-      lo.z = e4m3x2_to_f16x2(w[j].y & 0xFFFFu);
-      lo.w = e4m3x2_to_f16x2(w[j].y >> 16);
-      hi.x = e4m3x2_to_f16x2(w[j].z & 0xFFFFu);
-      hi.y = e4m3x2_to_f16x2(w[j].z >> 16);
-      hi.z = e4m3x2_to_f16x2(w[j].w & 0xFFFFu);
-      hi.w = e4m3x2_to_f16x2(w[j].w >> 16);
-      if constexpr (VTOK) {
-        float vs = in ? lds_f32(sst + 4u * (uint32_t)(TT + t)) : 0.f;
-        if (in && !(fabsf(vs) <= 2048.f)) {
-          flag_status(p, kStatusScaleRange);
-          vs = 0.f;
-        }
-        const uint32_t s2 = pack_f16(vs * kVtokUnit, vs * kVtokUnit);
-        lo.x = hmul2_bits(lo.x, s2);
-        lo.y = hmul2_bits(lo.y, s2);
-        lo.z = hmul2_bits(lo.z, s2);
-        lo.w = hmul2_bits(lo.w, s2);
-        hi.x = hmul2_bits(hi.x, s2);
-        hi.y = hmul2_bits(hi.y, s2);
-        hi.z = hmul2_bits(hi.z, s2);
-        hi.w = hmul2_bits(hi.w, s2);
+  // The unit as FP16 into the V^T operand over the stage's K and V bytes:
+  // [D/64 chunks][TT][128 B]; tokens outside the stage's range become zeros
+  // (poisoned slots never reach the MMA); per-token V scales (times 2^-4) are
+  // folded in.
+  __device__ __forceinline__ void store_v16_unit(uint32_t kst, uint32_t sst, const StageView& h, int j,
+                                                 uint4 w) const {
+    const int e = threadIdx.x + j * kMtpSoftThreads;
+    const int t = e / (8 * C::NCH), cb = (e / 8) % C::NCH, cc = e % 8;
+    const bool in = h.tbase + t >= h.t0 && h.tbase + t < h.t1;
+    const int dim0 = cb * 128 + 16 * cc;
+    const uint32_t dst =
+        kst + (uint32_t)(dim0 / 64) * (TT * 128u) + (uint32_t)t * 128u + (uint32_t)((((dim0 % 64) / 8) ^ (t & 7)) << 4);
+    uint4 lo, hi;
+    lo.x = e4m3x2_to_f16x2(w.x & 0xFFFFu);
+    lo.y = e4m3x2_to_f16x2(w.x >> 16);
+    lo.z = e4m3x2_to_f16x2(w.y & 0xFFFFu);
+    lo.w = e4m3x2_to_f16x2(w.y >> 16);
+    hi.x = e4m3x2_to_f16x2(w.z & 0xFFFFu);
+    hi.y = e4m3x2_to_f16x2(w.z >> 16);
+    hi.z = e4m3x2_to_f16x2(w.w & 0xFFFFu);
+    hi.w = e4m3x2_to_f16x2(w.w >> 16);
+    if constexpr (VTOK) {
+      float vs = in ? lds_f32(sst + 4u * (uint32_t)(TT + t)) : 0.f;
+      if (in && !(fabsf(vs) <= 2048.f)) {
+        flag_status(p, kStatusScaleRange);
+        vs = 0.f;
       }
-      if (!in) lo = hi = make_uint4(0, 0, 0, 0);
-      sts128(dst, lo);
-      sts128(dst ^ 16u, hi);
+      const uint32_t s2 = pack_f16(vs * kVtokUnit, vs * kVtokUnit);
+      lo.x = hmul2_bits(lo.x, s2);
+      lo.y = hmul2_bits(lo.y, s2);
+      lo.z = hmul2_bits(lo.z, s2);
+      lo.w = hmul2_bits(lo.w, s2);
+      hi.x = hmul2_bits(hi.x, s2);
+      hi.y = hmul2_bits(hi.y, s2);
+      hi.z = hmul2_bits(hi.z, s2);
+      hi.w = hmul2_bits(hi.w, s2);
     }
+    if (!in) lo = hi = make_uint4(0, 0, 0, 0);
+    sts128(dst, lo);
+    sts128(dst ^ 16u, hi);
   }
   // BF16 stage used in place: this thread zeroes its token's V row when the
   // token is outside the stage's range.
@@ -547,8 +571,23 @@ struct MtpSoftmax {
     // store. FP8 caches: FP16 P in buffer k & 1, last read by PV(k - 2). BF16
     // caches: hi = bf16(p), lo = bf16(p - hi) in the one buffer, last read by
     // PV(k - 1).
+    if constexpr (FP8) {
+      // FP16 V over the stage's K and V bytes, before waiting on the P slot.
+      // A token's FP8 V row is read, and its FP16 chunk rows written, only by
+      // the eight lanes of one warp that convert it, unit by unit: reading
+      // the unit before the warp writes is enough ordering for the in-place
+      // copy.
+#pragma unroll
+      for (int j = 0; j < kVUnits; ++j) {
+        const uint4 w = load_v_unit(vst, j);
+        __syncwarp();
+        store_v16_unit(kst, sst, h, j, w);
+      }
+    } else if (!interior) {
+      clear_v_row(vst, h);
+    }
     if (k >= C::PB && !wait_pv(k - C::PB)) return false;
-    const int slot0 = FP8 ? buf : 0;
+    const int slot0 = FP8 ? k % C::PB : 0;
     const uint32_t prow = pslot(slot0) + (uint32_t)tok * 128u;
 #pragma unroll
     for (int u = 0; u < RH / 8; ++u) {
@@ -566,17 +605,6 @@ struct MtpSoftmax {
       const uint32_t off = (uint32_t)(((wg * (RH / 8) + u) ^ (tok & 7)) << 4);
       sts128(prow + off, make_uint4(hw[0], hw[1], hw[2], hw[3]));
       if constexpr (C::PT == 2) sts128(prow + TT * 128u + off, make_uint4(lw[0], lw[1], lw[2], lw[3]));
-    }
-    if constexpr (FP8) {
-      // A token's FP8 V row is read, and its FP16 chunk rows written, only by
-      // the eight lanes of one warp that convert it: reading every unit
-      // before the warp writes is enough ordering for the in-place copy.
-      uint4 vw[kVUnits];
-      load_v(vst, vw);
-      __syncwarp();
-      store_v16(kst, sst, h, vw);
-    } else if (!interior) {
-      clear_v_row(vst, h);
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
@@ -598,12 +626,23 @@ struct MtpSoftmax {
     const bool cluster = p.merge == kMergeCluster;
     float* cp_o = reinterpret_cast<float*>(sm.base + p.off_cpart);
     float* cp_ml = cp_o + (size_t)p.Rpad * D;
-    float Lr[RH];
+    // per row: the reference max M, the sum L, and the factor that turns O
+    // into the output (whole units: sink-adjusted 1/L times the V scale) or
+    // into the partial (the per-token V unit)
+    float Mr[RH], Lr[RH], f[RH];
     {
       uint32_t v[RH];
       if (o_valid) {
         tmem_ld_cols<RH>(tmem + lane_addr + C::kColL + (uint32_t)(wg * RH), v);
         tmem_wait_ld();
+      }
+#pragma unroll
+      for (int i = 0; i < RH; i += 4) {
+        const float4 m4 = lds128f(row_m_u32(wg * RH + i));
+        Mr[i] = m4.x;
+        Mr[i + 1] = m4.y;
+        Mr[i + 2] = m4.z;
+        Mr[i + 3] = m4.w;
       }
 #pragma unroll
       for (int i = 0; i < RH; ++i) {
@@ -613,6 +652,26 @@ struct MtpSoftmax {
       }
     }
     const float ounit = VTOK ? 1.f / kVtokUnit : 1.f;
+#pragma unroll
+    for (int i = 0; i < RH; ++i) {
+      if (whole) {
+        const int r = wg * RH + i;
+        float L = Lr[i], a = 1.f;
+        if (p.has_sinks && r < p.R) {
+          const float s2 = __ldg(p.sinks + h.g * p.G + r % p.G) * kLog2e;
+          const float M2 = fmaxf(Mr[i], s2);
+          a = (Mr[i] == -INFINITY) ? 0.f : ex2(Mr[i] - M2);
+          L = fmaf(L, a, ex2(s2 - M2));
+        }
+        f[i] = (L > 0.f) ? a * ((1.f / L) * vscale) : 0.f;
+      } else {
+        f[i] = ounit;
+      }
+    }
+    // O * f through shared memory (the P slots, idle once the last PV is
+    // done: [RN rows][D] f32), then every softmax thread writes 16-byte
+    // pieces of whole rows: fewer, wider stores than one float per row.
+    const uint32_t stg = sm.base_u32 + p.off_p16;
 #pragma unroll 1
     for (int cblk = 0; cblk < C::DCH; ++cblk) {
       uint32_t v[RH];
@@ -623,26 +682,37 @@ struct MtpSoftmax {
       const int d = cblk * 128 + tok;  // lane quarter q, lane l -> dim 32q + l of this block
 #pragma unroll
       for (int i = 0; i < RH; ++i) {
-        const int r = wg * RH + i;
-        if (r >= p.R) continue;
-        const float o = o_valid ? __uint_as_float(v[i]) : 0.f;
+        const float o = (o_valid ? __uint_as_float(v[i]) : 0.f) * f[i];
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(stg + 4u * (uint32_t)((wg * RH + i) * D + d)), "f"(o) : "memory");
+      }
+    }
+    named_bar(kBarStage, kMtpSoftThreads);
+    {
+      const int E = p.R * (D / 4);  // float4 pieces of the R rows
+      for (int e = threadIdx.x; e < E; e += kMtpSoftThreads) {
+        const int r = e / (D / 4), d = (e % (D / 4)) * 4;
+        const float4 o = lds128f(stg + 4u * (uint32_t)(r * D + d));
         if (whole) {
-          finalize_one(o, row_m()[r], Lr[i], h.b, h.g, r, d);
+          const int qi = r / p.G, head = h.g * p.G + r % p.G;
+          uint2 st;
+          st.x = pack_bf16(o.x, o.y);
+          st.y = pack_bf16(o.z, o.w);
+          *reinterpret_cast<uint2*>(p.out + ((size_t)(h.b * p.QL + qi) * p.Hq + head) * D + d) = st;
         } else if (cluster) {
-          cp_o[(size_t)r * D + d] = o * ounit;
+          *reinterpret_cast<float4*>(cp_o + (size_t)r * D + d) = o;
         } else {
-          p.part_o[((size_t)slot * p.Rpad + r) * D + d] = o * ounit;
+          *reinterpret_cast<float4*>(p.part_o + ((size_t)slot * p.Rpad + r) * D + d) = o;
         }
       }
     }
     // (max, sum) of the rows: one lane writes them all (compile-time indices
-    // keep m and L in registers)
+    // keep them in registers)
     if (!whole && quarter == 0 && lane == 0) {
 #pragma unroll
       for (int i = 0; i < RH; ++i) {
         const int r = wg * RH + i;
         if (r >= p.R) break;
-        const float2 ml = make_float2(row_m()[r], Lr[i]);
+        const float2 ml = make_float2(Mr[i], Lr[i]);
         if (cluster)
           *reinterpret_cast<float2*>(cp_ml + 2 * r) = ml;
         else
@@ -661,22 +731,6 @@ struct MtpSoftmax {
       named_bar(1, kMtpSoftThreads);
       la_run_queue<D>(p, sm, per_tensor_vscale(p), kMtpSoftThreads);
     }
-  }
-
-  // out = O * (1/L) * vscale with an optional sink logit, one element.
-  __device__ __forceinline__ void finalize_one(float O, float M, float L, int b, int g, int r, int d) const {
-    const int i = r / p.G;
-    const int head = g * p.G + r % p.G;
-    if (p.has_sinks) {
-      const float s2 = __ldg(p.sinks + head) * kLog2e;
-      const float M2 = fmaxf(M, s2);
-      const float a = (M == -INFINITY) ? 0.f : ex2(M - M2);
-      L = fmaf(L, a, ex2(s2 - M2));
-      O *= a;
-    }
-    const float inv = (L > 0.f) ? (1.f / L) * vscale : 0.f;
-    const __nv_bfloat16 v = __float2bfloat16_rn(O * inv);
-    p.out[((size_t)(b * p.QL + i) * p.Hq + head) * D + d] = *reinterpret_cast<const uint16_t*>(&v);
   }
 
   __device__ __forceinline__ void run() {
@@ -710,7 +764,7 @@ struct MtpSoftmax {
         slot = h3.x;
         md = MergeDesc{h3.y, h3.z, h3.w, sstride};
       }
-      if ((h.flags & kSegFirst) && !begin_segment(h.L)) break;
+      if ((h.flags & kSegFirst) && !begin_segment(h.L, h.t1 > h.t0)) break;
       if (h.t1 > h.t0) {
         if (!stage(h, s)) break;
       } else {
@@ -740,7 +794,9 @@ struct MtpIssuer {
     bars.base = sm.base_u32 + p.off_ubar;
     dq = umma_sdesc(sm.base_u32 + p.off_q16, 16, 1024);
     dp0 = umma_sdesc(sm.base_u32 + p.off_p16, TT * 128u, 1024);
-    dones = umma_sdesc(sm.base_u32 + p.off_p16 + 2u * TT * 128u, 16, 1024);
+    // the ones operand: 2 KiB of 1.0 read as [64 x 16] without swizzle (any
+    // core-matrix strides that stay inside the buffer read the same values)
+    dones = umma_sdesc_noswz(sm.base_u32 + p.off_p16 + (uint32_t)C::NP * TT * 128u, 128, 256);
   }
   __device__ __forceinline__ static uint64_t dadd(uint64_t d, uint32_t byte_off) { return d + (uint64_t)(byte_off >> 4); }
 
@@ -776,7 +832,6 @@ struct MtpIssuer {
   // O^T += V^T . P^T(kk), L^T += 1 . P^T(kk) (P(kk) is ready); then release
   // stage s.
   __device__ __forceinline__ void issue_pv(int kk, int s, bool acc) {
-    const int buf = kk & 1;
     tc_fence_after();
     const uint32_t kst = sm.stage(s, p);
     // V^T: FP8 caches -> FP16 copy over the stage's K and V bytes; BF16 -> the V bytes
@@ -784,7 +839,7 @@ struct MtpIssuer {
     const uint64_t dv = umma_sdesc(vbase, TT * 128u, 1024);
 #pragma unroll
     for (int t = 0; t < C::PT; ++t) {
-      const uint64_t dp = dadd(dp0, (uint32_t)((FP8 ? buf : 0) + t) * (TT * 128u));
+      const uint64_t dp = dadd(dp0, (uint32_t)((FP8 ? kk % C::PB : 0) + t) * (TT * 128u));
       const bool a0 = acc || t > 0;
 #pragma unroll
       for (int cblk = 0; cblk < C::DCH; ++cblk)
@@ -797,7 +852,7 @@ struct MtpIssuer {
       for (int j = 0; j < TT / 16; ++j)
         umma_f16(tmem + C::kColL, dones, dadd(dp, (uint32_t)j * 2048u), C::kIdL, (a0 || j > 0) ? 1u : 0u);
     }
-    umma_commit(bars.pv_done(buf));
+    umma_commit(bars.pv_done(kk % 3));
     umma_commit(sm.empty(s, p));
   }
 
@@ -857,7 +912,7 @@ struct MtpIssuer {
           hdr_ok = true;
           hflags = h0.x;
           htok = h0.w > h0.z;
-          need_q = (hflags & kSegFirst) != 0;
+          need_q = (hflags & kSegFirst) != 0 && htok;  // empty segments signal no q_ready
           if (hflags & kEnd) done = true;
           progress = true;
         }
@@ -952,18 +1007,18 @@ __global__ void __launch_bounds__(kMtpThreads, 1) pa_mtp_kernel(const __grid_con
       mbar_init(bar0 + 8u * i, 1);          // s_full: MMA commit
       mbar_init(bar0 + 16u + 8u * i, 8);    // s_free: softmax warps
       mbar_init(bar0 + 32u + 8u * i, 8);    // p_full: softmax warps
-      mbar_init(bar0 + 48u + 8u * i, 1);    // pv_done: MMA commit
     }
-    mbar_init(bar0 + 64u, 8);  // q_ready
-    mbar_init(bar0 + 72u, 1);  // drained
+    for (int i = 0; i < 3; ++i) mbar_init(bar0 + 48u + 8u * i, 1);  // pv_done: MMA commit
+    mbar_init(bar0 + 72u, 8);  // q_ready
+    mbar_init(bar0 + 80u, 1);  // drained
     for (int i = 0; i < 16; ++i) sm.misc(p)[i] = 0;
     fence_barrier_init();
   }
-  // the ones operand of the row sums (64 x 64 elements of 1.0, layout-free)
+  // the ones operand of the row sums (64 x 16 elements of 1.0, layout-free)
   {
     const uint32_t one2 = FP8 ? 0x3C003C00u : 0x3F803F80u;
-    const uint32_t ones = sm.base_u32 + p.off_p16 + 2u * kMtpTT * 128u;
-    for (uint32_t o = threadIdx.x * 16u; o < 8192u; o += kMtpThreads * 16u) sts128(ones + o, make_uint4(one2, one2, one2, one2));
+    const uint32_t ones = sm.base_u32 + p.off_p16 + (uint32_t)Cfg::NP * kMtpTT * 128u;
+    for (uint32_t o = threadIdx.x * 16u; o < 2048u; o += kMtpThreads * 16u) sts128(ones + o, make_uint4(one2, one2, one2, one2));
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sm.base_u32 + p.off_tslot),

@@ -23,6 +23,21 @@ __device__ __forceinline__ uint64_t umma_sdesc(uint32_t saddr, uint32_t lbo, uin
   d |= (uint64_t)2 << 61;  // 128-byte swizzle
   return d;
 }
+// Shared-memory matrix descriptor without swizzle (core matrices of eight
+// 16-byte rows; lbo and sbo are the byte strides between them).
+__device__ __forceinline__ uint64_t umma_sdesc_noswz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 // Instruction descriptor, kind::f16: FP32 accumulate, A and B both FP16 or
 // both BF16, each K-major or MN-major.
 __host__ __device__ constexpr uint32_t umma_idesc_ab(bool bf16, int M, int N, bool a_mn_major, bool b_mn_major) {

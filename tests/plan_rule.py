@@ -47,7 +47,7 @@ def smem_total(d, k, ns, cluster, nq):
         rn = 2 * k["rh"]
         off += (3 if d["kv_dtype"] == 0 else 2) * d["head_dim"] * rn  # Q operand
         off = align(off, 1024)
-        off += 2 * k["tt"] * 128 + 8192  # two P^T slots, the ones operand
+        off += (3 if d["kv_dtype"] == 0 else 2) * k["tt"] * 128 + 2048  # P^T slots, the ones operand
     elif cluster:
         off += align(k["rpad"] * d["head_dim"] * 4 + k["rpad"] * 8, 128)
     off += ns * 128 + ns * 16 + 32 + (128 if k["umma"] else 16) + 16

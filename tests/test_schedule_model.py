@@ -91,7 +91,7 @@ def check(chunks_per_unit, C0, A):
             assert slots_of[u] == expect, (u, slots_of[u], expect)
 
 
-@pytest.mark.parametrize("seg_cost", [0, 1, 2])
+@pytest.mark.parametrize("seg_cost", [0, 1, 2, 4])
 def test_balanced_schedule_invariants(seg_cost):
     rng = random.Random(1234 + seg_cost)
     for _ in range(1500):
