@@ -54,6 +54,7 @@ constexpr int kMtpThreads = 320;       // + producer warp 8 + MMA warp 9
 constexpr int kMtpProducerWarp = 8;
 constexpr int kMtpMmaWarp = 9;
 constexpr int kBarStage = 2;           // named barrier of the 256 softmax threads (1 = merges)
+constexpr int kBarWg0 = 3;             // 3, 4: named barriers of one softmax warpgroup (128 threads)
 constexpr float kVtokUnit = 0.0625f;   // per-token V scales enter FP16 V as vs * 2^-4
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
@@ -414,10 +415,10 @@ struct MtpSoftmax {
     return Max3Tree<RH>::run(y);  // the largest y
   }
 
-  // Slow path (all softmax threads): raise the reference max of rows whose
-  // stage maximum exceeds it by more than 2^8 and rescale their O and L
-  // columns in tensor memory (after the previous PV has completed). Leaves
-  // the stage's scores against the new reference in y.
+  // Slow path (one warpgroup, for its own rows): raise the reference max of
+  // rows whose stage maximum exceeds it by more than 2^8 and rescale their O
+  // and L columns in tensor memory (after the previous PV has completed).
+  // Leaves the stage's scores against the new reference in y.
   __device__ __forceinline__ bool raise_max(const StageView& h, bool interior, float ks, int buf, bool o_valid, float (&y)[RH]) {
     load_s(buf, y);
 #pragma unroll
@@ -442,9 +443,9 @@ struct MtpSoftmax {
       const float v = rowmax_transpose<RH>(y, lane);
       if (lane < RH) row_red()[quarter * 64 + wg * RH + lane] = v;
     }
-    named_bar(kBarStage, kMtpSoftThreads);
-    if (threadIdx.x < RN) {
-      const int r = threadIdx.x;
+    named_bar(kBarWg0 + wg, 128);
+    if (threadIdx.x - 128 * wg < RH) {
+      const int r = wg * RH + (threadIdx.x - 128 * wg);
       const float mold = row_m()[r];
       float smax = row_red()[r];
 #pragma unroll
@@ -456,7 +457,7 @@ struct MtpSoftmax {
       }
       row_alpha()[r] = alpha;
     }
-    named_bar(kBarStage, kMtpSoftThreads);
+    named_bar(kBarWg0 + wg, 128);
     bool any = false;
 #pragma unroll
     for (int i = 0; i < RH; ++i) any |= row_alpha()[wg * RH + i] != 1.f;
@@ -558,9 +559,11 @@ struct MtpSoftmax {
     float y[RH];
     load_s(buf, y);
     const float mx = scores(h, interior, ks, y);
-    // one vote per stage: some score above its reference by more than 2^8?
+    // one vote per stage and warpgroup: some score of its rows above the
+    // reference by more than 2^8? (The warpgroups own disjoint rows and O/L
+    // columns, so they vote and rescale independently and may drift apart.)
     const bool o_valid = k > seg_k0;
-    if (named_bar_or(kBarStage, kMtpSoftThreads, mx > 8.f)) {
+    if (named_bar_or(kBarWg0 + wg, 128, mx > 8.f)) {
       if (!raise_max(h, interior, ks, buf, o_valid, y)) return false;
     }
     // S(k) is read: its buffer may take S(k + 2)
