@@ -258,7 +258,7 @@ CONSUMERS = {"auto": 0, "tile": 1, "tmem": 2}
 def make_workload(args, rank):
     kv = pw.KV_BF16 if args.kv == "bf16" else pw.KV_FP8
     if args.workload == "dense":
-        return pw.dense(seed=1002 + rank)
+        return pw.dense(seed=1002 + rank, page_size=args.page)
     if args.workload == "tiny":
         return pw.tiny()
     if args.workload == "d256":
@@ -343,6 +343,7 @@ def main():
                     help="the headline line uses the default dense workload; the others are for profiling")
     ap.add_argument("--kv", default="fp8", choices=["fp8", "bf16"], help="sparse and mtp4 cache format")
     ap.add_argument("--rows", type=int, default=1024, help="sparse_prefill: prompt rows")
+    ap.add_argument("--page", type=int, default=16, help="dense: page size (16 is the workload's)")
     ap.add_argument("--batch", type=int, default=0,
                     help="mtp4/d256: batch override (a smaller case for profiler captures; 0 = the workload's)")
     ap.add_argument("--no-warm", action="store_true", help="skip the warm CUDA-graph timing")

@@ -235,14 +235,16 @@ def dense_lengths(seed: int, batch: int = 64, lo: int = 1024, hi: int = 8192):
 
 
 def dense(seed: int = 1002, batch: int = 64, lo: int = 1024, hi: int = 8192,
-          kv_dtype: int = KV_FP8) -> Workload:
-    """Batch 64, 8 KV heads, GQA8, D128, page 16, contexts U[1024, 8192], 40k-page pool."""
+          kv_dtype: int = KV_FP8, page_size: int = 16) -> Workload:
+    """Batch 64, 8 KV heads, GQA8, D128, page 16, contexts U[1024, 8192], 40k-page pool
+    (page_size other than 16 keeps the pool's bytes: 40000 * 16 / page_size pages)."""
     lens = dense_lengths(seed, batch, lo, hi)
+    pool = 40000 * 16 // page_size
     return make_dense("dense", batch=batch, hkv=8, group=8, head_dim=128,
-                      query_len=1, page_size=16, ctx_lens=lens, kv_dtype=kv_dtype,
+                      query_len=1, page_size=page_size, ctx_lens=lens, kv_dtype=kv_dtype,
                       scale_mode=SCALE_PER_TENSOR, seed=seed,
-                      pool_pages=max(40000, int(((lens + 15) // 16).sum()) + 8),
-                      max_pages=hi // 16)
+                      pool_pages=max(pool, int(((lens + page_size - 1) // page_size).sum()) + 8),
+                      max_pages=hi // page_size)
 
 
 def d256_lengths(seed: int, batch: int = 16, short: int = 8192, long: int = 131072):

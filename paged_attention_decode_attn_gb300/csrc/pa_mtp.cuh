@@ -996,6 +996,7 @@ __global__ void __launch_bounds__(kMtpThreads, 1) pa_mtp_kernel(const __grid_con
     sm.base_u32 = aligned;
   }
   const int warp = threadIdx.x >> 5;
+  if (warp == 0) prefetch_params(p);
   const uint32_t bar0 = sm.base_u32 + p.off_ubar;
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {

@@ -230,6 +230,8 @@ __device__ __forceinline__ long long seq_weight(const PaParams& p, int b) {
 // Total weight of the balanced schedule (warp-collective).
 __device__ __forceinline__ long long balanced_total(const PaParams& p, int lane) {
   long long tot = 0;
+  // unrolled so that several rounds' length loads are in flight together
+#pragma unroll 8
   for (int b0 = 0; b0 < p.B; b0 += 32) {
     int b = b0 + lane;
     long long cnt = 0;
@@ -317,6 +319,18 @@ struct Smem {
     return reinterpret_cast<volatile int*>(base + p.off_misc);
   }
 };
+
+// Read one field from each 64-byte line of the kernel parameters, all before
+// any is used: the first access to a line misses the constant cache and,
+// after L2 has been evicted, goes to DRAM; issued together the misses overlap
+// instead of stalling the producer's control flow one line at a time.
+__device__ __forceinline__ void prefetch_params(const PaParams& p) {
+  static_assert(sizeof(PaParams) <= 6 * 64, "one field per parameter line below");
+  const uint64_t a0 = reinterpret_cast<uint64_t>(p.out);
+  const uint64_t a1 = reinterpret_cast<uint64_t>(p.part_o);
+  const int a2 = p.B, a3 = p.window, a4 = p.C, a5 = p.off_hdr, a6 = p.off_q, a7 = p.off_rows;
+  asm volatile("" ::"l"(a0), "l"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7));
+}
 
 __device__ __forceinline__ void flag_status(const PaParams& p, int bits) {
   if (p.status) atomicOr(p.status, bits);
@@ -767,8 +781,14 @@ struct Producer {
       // CTA between a unit's first and last owner holds part of that unit.
       long long N;
       long long cnt_reg[kScanRegs];
-      const bool in_regs = p.B <= 32 * kScanRegs;
-      if (in_regs) {
+      // Sparse units all weigh the same (ceil(topk / TT) chunks whatever the
+      // context length): the schedule is closed-form, no length scan.
+      const bool uniform = p.topk > 0;
+      const long long wu_uniform = (long long)(max(1, (p.topk + p.TT - 1) / p.TT) + p.seg_cost);
+      const bool in_regs = !uniform && p.B <= 32 * kScanRegs;
+      if (uniform) {
+        N = (long long)p.B * p.Hkv * wu_uniform;
+      } else if (in_regs) {
         // chunk counts of sequences lane, lane + 32, ... loaded in one round trip
 #pragma unroll
         for (int i = 0; i < kScanRegs; ++i) {
@@ -790,7 +810,10 @@ struct Producer {
       const long long x1 = c < C ? sched_start(c + 1, N, C) : 0;
       // sequence holding global chunk xx and the chunk count before it
       auto locate = [&](long long xx, int& b, long long& excl) {
-        if (in_regs) {
+        if (uniform) {
+          b = (int)(xx / ((long long)p.Hkv * wu_uniform));
+          excl = (long long)b * p.Hkv * wu_uniform;
+        } else if (in_regs) {
           long long base = 0;
           b = p.B;
           excl = 0;
@@ -1623,6 +1646,7 @@ __global__ void __launch_bounds__(MAXW * 32, (D == 128 && MAXW == 5) ? 2 : 1) pa
     sm.base_u32 = aligned;
   }
   const int warp = threadIdx.x >> 5;
+  if (warp == 0) prefetch_params(p);
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
       mbar_init(sm.full(s, p), 1);
