@@ -425,7 +425,6 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   p.Wt = k.wt;
   p.NCW = k.ncw;
   p.BH = k.bh;
-  p.swz = d.sparse_topk > 0 ? 0 : 7;
   p.off_stage = L.off_stage;
   p.stage_bytes = L.stage_bytes;
   p.off_scale = L.off_scale;
@@ -485,14 +484,13 @@ pa_status encode_cache_map(const pa_plan* pl, const void* base, CUtensorMap* tm)
   auto fn = encode_fn();
   if (!fn) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   const int elt = d.kv_dtype == PA_KV_FP8_E4M3 ? 1 : 2;
-  const bool sparse = d.sparse_topk > 0;
   cuuint64_t dims[2] = {(cuuint64_t)d.head_dim, (cuuint64_t)d.num_pages * d.num_kv_heads * d.page_size};
   cuuint64_t strides[1] = {(cuuint64_t)d.head_dim * elt};
-  cuuint32_t box[2] = {(cuuint32_t)(128 / elt), sparse ? 1u : (cuuint32_t)pl->base.BH};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / elt), (cuuint32_t)pl->base.BH};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(tm, elt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  sparse ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return PA_OK;
@@ -544,6 +542,8 @@ pa_status launch(const pa_plan* pl, void* ws_ptr, void* out, const void* q, cons
   p.v_scale = v_scale;
   p.sinks = d.has_sinks ? sinks : nullptr;
   p.topk_idx = topk_idx;
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
   p.window = d.sparse_topk > 0 ? 0 : window;
   p.part_o = reinterpret_cast<float*>(ws + pl->off_part_o);
   p.part_ml = reinterpret_cast<float*>(ws + pl->off_part_ml);

@@ -54,7 +54,6 @@ struct PaParams {
   int NS;  // ring stages
   int Wr, Wt, NCW;  // row warps, token warps, consumer warps
   int BH;           // rows per dense TMA box = min(S, TT)
-  int swz;          // XOR mask of the 128-byte swizzle (7) or 0 (linear rows)
   // dynamic shared memory layout (byte offsets from a 1024-aligned base)
   int off_stage, stage_bytes, off_scale;  // off_scale: within a stage
   int off_hdr, off_bar, off_merge, off_cpart, off_misc, off_pend, off_mml;
@@ -62,6 +61,9 @@ struct PaParams {
   // tcgen05 consumer: 16-bit K and V operands (FP8 caches), Q and P operands,
   // the two MMA commit barriers, and the tensor-memory address slot
   int off_k16, off_v16, off_q16, off_p16, off_ubar, off_tslot, off_rows;
+  // cache bases for the sparse row gathers (dense stages load through the tensor maps)
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
 };
 
 // Host-visible shared-memory sizing for a kernel configuration.

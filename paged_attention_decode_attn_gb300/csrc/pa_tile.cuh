@@ -5,7 +5,7 @@
 //    chunks, stages block-table page ids in its registers (32 per coalesced
 //    load, the next batch prefetched), and fills a ring of shared-memory
 //    stages with TMA copies (cp.async.bulk.tensor, 128-byte swizzle; sparse
-//    rows with tile::gather4), completing on mbarriers;
+//    rows with 16-byte cp.async in the same swizzle), completing on mbarriers;
 //  * NCW consumer warps read each stage, compute S^T = K Q^T and O^T += V^T P^T
 //    with mma.sync m16n8k16 (tokens or head dims on the M side, query rows on
 //    the N side, so a GQA8 group fills the 8-wide N tile exactly), scale and
@@ -108,14 +108,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int x, int y0, int y1, int y2, int y3,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
-      "%4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
-      : "memory");
+// 16-byte (L2-only) and 4-byte asynchronous copies to shared memory; the
+// noinc arrive fires on `bar` once every copy this thread issued so far has
+// landed, without raising the barrier's expected count (it is part of it).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
@@ -578,13 +583,57 @@ struct Producer {
     }
   }
 
+  // Copy the valid rows of a sparse stage into its K and V buffers with
+  // 16-byte asynchronous copies. Stage row r (r < TTC = 128 / NCH tokens)
+  // owns chunk rows cb * TTC + r, one per 128-byte column block cb; each
+  // instruction moves four whole chunk rows (eight lanes per row), written
+  // in the 128-byte swizzle the consumers read (16-byte piece j of chunk
+  // row c at piece j ^ (c & 7)). Lane l holds the cache row y and the
+  // validity of stage rows l, 32 + l, ... (yv, mask). Rows without a token
+  // are not copied: their scores are masked and their V rows zeroed.
+  __device__ __forceinline__ void gather_rows(uint32_t kst, uint32_t vst, const int (&yv)[4], const unsigned (&mask)[4]) {
+    constexpr int TTC = 128 / NCH;
+    constexpr int kRowBytes = 128 * NCH;
+    const int j = lane & 7, rq = lane >> 3;
+    const uint8_t* kb = p.k_cache + j * 16;
+    const uint8_t* vb = p.v_cache + j * 16;
+#pragma unroll
+    for (int w = 0; w < TTC / 32; ++w) {
+#pragma unroll
+      for (int cb = 0; cb < NCH; ++cb) {
+#pragma unroll 2
+        for (int i = 0; i < 8; ++i) {
+          const int src = 4 * i + rq;  // stage row w * 32 + src
+          const int y = __shfl_sync(0xffffffffu, yv[w], src);
+          if ((mask[w] >> src) & 1u) {
+            const int c = cb * TTC + w * 32 + src;  // chunk row
+            const uint32_t off = (uint32_t)c * 128u + (uint32_t)((j ^ (c & 7)) << 4);
+            const size_t g = (size_t)y * kRowBytes + (size_t)cb * 128;
+            cp_async16(kst + off, kb + g);
+            cp_async16(vst + off, vb + g);
+          }
+        }
+      }
+    }
+    if (p.scale_mode == kScalePerToken) {
+      const uint32_t sc = kst + (uint32_t)p.off_scale;
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int row = rr * 32 + lane;
+        if (row < TTC && ((mask[rr] >> lane) & 1u)) {
+          cp_async4(sc + row * 4, p.k_scale + yv[rr]);
+          cp_async4(sc + TTC * 4 + row * 4, p.v_scale + yv[rr]);
+        }
+      }
+    }
+  }
+
   __device__ __forceinline__ void emit_sparse(StageHdr h) {
     int s;
     if (!acquire_stage(s)) return;
     const int TT = p.TT;
     const uint32_t kst = sm.stage(s, p);
     const uint32_t vst = kst + (uint32_t)TT * 128u * NCH;
-    const bool ktok = p.scale_mode == kScalePerToken;
     const bool empty = !(h.t1 > h.t0);
     int idx[4], phys[4];
 #pragma unroll
@@ -613,7 +662,6 @@ struct Producer {
     int yv[4];
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) {
-      const int row = rr * 32 + lane;
       const int t = empty ? -1 : idx[rr];
       const bool valid = t >= 0 && t < h.L;
       int y = 0;
@@ -627,47 +675,15 @@ struct Producer {
       }
       yv[rr] = y;
       h.mask[rr] = __ballot_sync(0xffffffffu, valid);
-      if (ktok && valid) {
-        const uint32_t sc = kst + p.off_scale;
-        const float kv = __ldg(p.k_scale + y), vv = __ldg(p.v_scale + y);
-        asm volatile("st.shared.f32 [%0], %1;" ::"r"(sc + row * 4), "f"(kv) : "memory");
-        asm volatile("st.shared.f32 [%0], %1;" ::"r"(sc + TT * 4 + row * 4), "f"(vv) : "memory");
-      }
-    }
-    // a stage none of whose index positions holds a token of [0, L) moves no bytes
-    const bool skip = empty || (h.mask[0] | h.mask[1] | h.mask[2] | h.mask[3]) == 0u;
-    const uint32_t bytes = skip ? 0u : (uint32_t)TT * 128u * NCH * 2u;
-    __syncwarp();
-    if (lane == 0) {
-      *sm.hdr(s, p) = h;
-      if (bytes)
-        mbar_arrive_tx(sm.full(s, p), bytes);
-      else
-        mbar_arrive(sm.full(s, p));
     }
     __syncwarp();
-    if (!skip) {
-      // lane q gathers stage rows 4q .. 4q+3 (round 4q / 32 of the y registers)
-      int y4[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int src = (4 * lane + i) & 31;
-        const int v0 = __shfl_sync(0xffffffffu, yv[0], src);
-        const int v1 = __shfl_sync(0xffffffffu, yv[1], src);
-        const int v2 = __shfl_sync(0xffffffffu, yv[2], src);
-        const int v3 = __shfl_sync(0xffffffffu, yv[3], src);
-        const int rnd = (4 * lane + i) >> 5;
-        y4[i] = rnd == 0 ? v0 : (rnd == 1 ? v1 : (rnd == 2 ? v2 : v3));
-      }
-      if (lane < TT / 4) {
-        const uint32_t bar = sm.full(s, p);
-#pragma unroll
-        for (int cb = 0; cb < NCH; ++cb) {
-          tma_gather4(kst + (uint32_t)(cb * TT + 4 * lane) * 128u, tmK, cb * (128 / ELT), y4[0], y4[1], y4[2], y4[3], bar);
-          tma_gather4(vst + (uint32_t)(cb * TT + 4 * lane) * 128u, tmV, cb * (128 / ELT), y4[0], y4[1], y4[2], y4[3], bar);
-        }
-      }
-    }
+    if (lane == 0) *sm.hdr(s, p) = h;
+    if (!empty) gather_rows(kst, vst, yv, h.mask);
+    // The stage is full once lane 0 has published the header and every
+    // lane's copies have landed (one noinc arrival per lane).
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.full(s, p));
+    cp_async_arrive(sm.full(s, p));
     // look ahead: page ids of the next stage, indices of the one after
     la_b = -1;
     const int next = h.tbase + TT;
@@ -718,6 +734,7 @@ struct Producer {
       sm.hdr(s, p)->kind_flags = kEnd;
       mbar_arrive(sm.full(s, p));
     }
+    if (p.topk > 0) mbar_arrive(sm.full(s, p));  // sparse stages count one arrival per lane too
     __syncwarp();
     ++n;
   }
@@ -877,6 +894,7 @@ struct Producer {
     if (ok) emit_end();
     if (!ok) {
       // Wait (bounded) for copies this warp issued that may still be in flight.
+      if (p.topk > 0) cp_async_wait_all();
       const int first = max(0, n - p.NS);
       for (int m = first; m < n; ++m) (void)mbar_wait(sm.full(m % p.NS, p), (m / p.NS) & 1);
       for (int m = max(0, nq - p.NQ); m < nq; ++m) (void)mbar_wait(sm.qfull(m % p.NQ, p), (m / p.NQ) & 1);
@@ -1010,7 +1028,7 @@ struct Consumer {
     if (FP8 && p.scale_mode == kScalePerTensor) kscale = __ldg(p.k_scale);
     vscale = per_tensor_vscale(p);
     // Swizzled shared-memory offsets: row r's 16-byte chunk c sits at chunk
-    // c ^ (r & 7) (128-byte swizzle; sparse stages are unswizzled).
+    // c ^ (r & 7) (128-byte swizzle, dense and sparse stages alike).
 #pragma unroll
     for (int cb = 0; cb < NCH; ++cb) {
 #pragma unroll
@@ -1018,12 +1036,12 @@ struct Consumer {
         const int row = g4 + 8 * ab;
 #pragma unroll
         for (int hl = 0; hl < 2; ++hl)
-          koff[cb][ab][hl] = (uint32_t)(cb * p.TT + row) * 128u + (uint32_t)(((2 * t4 + hl) ^ (row & p.swz)) << 4);
+          koff[cb][ab][hl] = (uint32_t)(cb * p.TT + row) * 128u + (uint32_t)(((2 * t4 + hl) ^ (row & 7)) << 4);
       }
       const int vr[4] = {2 * t4, 2 * t4 + 1, 2 * t4 + 8, 2 * t4 + 9};
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        voff[cb][k] = (uint32_t)(cb * p.TT + vr[k]) * 128u + (uint32_t)((g4 ^ (vr[k] & p.swz)) << 4);
+        voff[cb][k] = (uint32_t)(cb * p.TT + vr[k]) * 128u + (uint32_t)((g4 ^ (vr[k] & 7)) << 4);
     }
   }
 
@@ -1649,7 +1667,8 @@ __global__ void __launch_bounds__(MAXW * 32, (D == 128 && MAXW == 5) ? 2 : 1) pa
   if (warp == 0) prefetch_params(p);
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
-      mbar_init(sm.full(s, p), 1);
+      // sparse stages: the header arrival and one copy arrival per producer lane
+      mbar_init(sm.full(s, p), p.topk > 0 ? 33 : 1);
       mbar_init(sm.empty(s, p), p.NCW);
     }
     for (int i = 0; i < 2; ++i) {
