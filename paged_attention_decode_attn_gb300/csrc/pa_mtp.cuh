@@ -242,6 +242,7 @@ struct MtpSoftmax {
   __device__ __forceinline__ uint32_t row_c_u32(int r) const { return sm.base_u32 + p.off_rows + 4u * (uint32_t)r; }
   __device__ __forceinline__ uint32_t row_m_u32(int r) const { return sm.base_u32 + p.off_rows + 256u + 4u * (uint32_t)r; }
   __device__ __forceinline__ uint32_t row_pos_u32(int r) const { return sm.base_u32 + p.off_rows + 512u + 4u * (uint32_t)r; }
+  __device__ __forceinline__ uint32_t row_alpha_u32(int r) const { return sm.base_u32 + p.off_rows + 768u + 4u * (uint32_t)r; }
   __device__ __forceinline__ uint32_t q16() const { return sm.base_u32 + p.off_q16; }
   __device__ __forceinline__ uint32_t pslot(int i) const { return sm.base_u32 + p.off_p16 + (uint32_t)i * (TT * 128u); }
 
@@ -629,64 +630,74 @@ struct MtpSoftmax {
     const bool cluster = p.merge == kMergeCluster;
     float* cp_o = reinterpret_cast<float*>(sm.base + p.off_cpart);
     float* cp_ml = cp_o + (size_t)p.Rpad * D;
-    // per row: the reference max M, the sum L, and the factor that turns O
-    // into the output (whole units: sink-adjusted 1/L times the V scale) or
-    // into the partial (the per-token V unit)
-    float Mr[RH], Lr[RH], f[RH];
-    {
+    // Per row, the factor that turns O into the output (whole units:
+    // sink-adjusted 1/L times the V scale) or into the partial (the per-token
+    // V unit), into row_alpha; lane r of the warpgroup's first warp computes
+    // row r's factor and writes a partial's (max, sum) pair.
+    if (quarter == 0) {
       uint32_t v[RH];
       if (o_valid) {
         tmem_ld_cols<RH>(tmem + lane_addr + C::kColL + (uint32_t)(wg * RH), v);
         tmem_wait_ld();
       }
-#pragma unroll
-      for (int i = 0; i < RH; i += 4) {
-        const float4 m4 = lds128f(row_m_u32(wg * RH + i));
-        Mr[i] = m4.x;
-        Mr[i + 1] = m4.y;
-        Mr[i + 2] = m4.z;
-        Mr[i + 3] = m4.w;
-      }
+      float Lv = 0.f;
 #pragma unroll
       for (int i = 0; i < RH; ++i) {
         // L^T rows are identical; lanes 0-15 of each quarter hold them (M = 64 layout)
         const float l = __shfl_sync(0xffffffffu, __uint_as_float(o_valid ? v[i] : 0u), lane & 15);
-        Lr[i] = o_valid ? l : 0.f;
+        if (lane == i) Lv = o_valid ? l : 0.f;
       }
-    }
-    const float ounit = VTOK ? 1.f / kVtokUnit : 1.f;
-#pragma unroll
-    for (int i = 0; i < RH; ++i) {
-      if (whole) {
-        const int r = wg * RH + i;
-        float L = Lr[i], a = 1.f;
-        if (p.has_sinks && r < p.R) {
-          const float s2 = __ldg(p.sinks + h.g * p.G + r % p.G) * kLog2e;
-          const float M2 = fmaxf(Mr[i], s2);
-          a = (Mr[i] == -INFINITY) ? 0.f : ex2(Mr[i] - M2);
-          L = fmaf(L, a, ex2(s2 - M2));
+      if (lane < RH) {
+        const int r = wg * RH + lane;
+        const float M = row_m()[r];
+        float fr = VTOK ? 1.f / kVtokUnit : 1.f;
+        if (whole) {
+          float L = Lv, a = 1.f;
+          if (p.has_sinks && r < p.R) {
+            const float s2 = __ldg(p.sinks + h.g * p.G + r % p.G) * kLog2e;
+            const float M2 = fmaxf(M, s2);
+            a = (M == -INFINITY) ? 0.f : ex2(M - M2);
+            L = fmaf(L, a, ex2(s2 - M2));
+          }
+          fr = (L > 0.f) ? a * ((1.f / L) * vscale) : 0.f;
+        } else if (r < p.R) {
+          const float2 ml = make_float2(M, Lv);
+          if (cluster)
+            *reinterpret_cast<float2*>(cp_ml + 2 * r) = ml;
+          else
+            *reinterpret_cast<float2*>(p.part_ml + ((size_t)slot * p.Rpad + r) * 2) = ml;
         }
-        f[i] = (L > 0.f) ? a * ((1.f / L) * vscale) : 0.f;
-      } else {
-        f[i] = ounit;
+        row_alpha()[r] = fr;
       }
     }
+    named_bar(kBarWg0 + wg, 128);
     // O * f through shared memory (the P slots, idle once the last PV is
     // done: [RN rows][D] f32), then every softmax thread writes 16-byte
     // pieces of whole rows: fewer, wider stores than one float per row.
     const uint32_t stg = sm.base_u32 + p.off_p16;
 #pragma unroll 1
     for (int cblk = 0; cblk < C::DCH; ++cblk) {
-      uint32_t v[RH];
-      if (o_valid) {
-        tmem_ld_cols<RH>(tmem + lane_addr + C::kColO + (uint32_t)(cblk * RN + wg * RH), v);
-        tmem_wait_ld();
-      }
       const int d = cblk * 128 + tok;  // lane quarter q, lane l -> dim 32q + l of this block
+      // 16 columns at a time keeps the live registers low
 #pragma unroll
-      for (int i = 0; i < RH; ++i) {
-        const float o = (o_valid ? __uint_as_float(v[i]) : 0.f) * f[i];
-        asm volatile("st.shared.f32 [%0], %1;" ::"r"(stg + 4u * (uint32_t)((wg * RH + i) * D + d)), "f"(o) : "memory");
+      for (int hh = 0; hh < RH / 16; ++hh) {
+        uint32_t v[16];
+        if (o_valid) {
+          tmem_ld16(tmem + lane_addr + C::kColO + (uint32_t)(cblk * RN + wg * RH + 16 * hh), v);
+          tmem_wait_ld();
+        }
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+          const float4 f4 = lds128f(row_alpha_u32(wg * RH + 16 * hh + i));
+          const float fq[4] = {f4.x, f4.y, f4.z, f4.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float o = (o_valid ? __uint_as_float(v[i + j]) : 0.f) * fq[j];
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(stg + 4u * (uint32_t)((wg * RH + 16 * hh + i + j) * D + d)),
+                         "f"(o)
+                         : "memory");
+          }
+        }
       }
     }
     named_bar(kBarStage, kMtpSoftThreads);
@@ -706,20 +717,6 @@ struct MtpSoftmax {
         } else {
           *reinterpret_cast<float4*>(p.part_o + ((size_t)slot * p.Rpad + r) * D + d) = o;
         }
-      }
-    }
-    // (max, sum) of the rows: one lane writes them all (compile-time indices
-    // keep them in registers)
-    if (!whole && quarter == 0 && lane == 0) {
-#pragma unroll
-      for (int i = 0; i < RH; ++i) {
-        const int r = wg * RH + i;
-        if (r >= p.R) break;
-        const float2 ml = make_float2(Mr[i], Lr[i]);
-        if (cluster)
-          *reinterpret_cast<float2*>(cp_ml + 2 * r) = ml;
-        else
-          *reinterpret_cast<float2*>(p.part_ml + ((size_t)slot * p.Rpad + r) * 2) = ml;
       }
     }
     // O and L are read; the next segment's first PV may overwrite them
