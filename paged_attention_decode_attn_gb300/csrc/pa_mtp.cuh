@@ -88,6 +88,11 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&v)
   else
     tmem_st16(taddr, v);
 }
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ float4 lds128f(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
@@ -318,12 +323,14 @@ struct MtpSoftmax {
       }
       const float sc = __uint_as_float((uint32_t)(ex + 127) << 23);
       const float inv = __uint_as_float((uint32_t)(127 - ex) << 23);
-      // four elements at a time: three e4m3 terms, one 32-bit word each
-#pragma unroll
+      // four elements at a time: three e4m3 terms, one 32-bit word each (a
+      // rolled loop: this runs once per segment, and short code misses the
+      // instruction cache less often than it saves in issue slots)
+#pragma unroll 1
       for (int g4 = 0; g4 < EPT / 4; ++g4) {
         // elements 4*g4 .. 4*g4+3: words 0-1 or 2-3 of 16-byte unit g4 / 2
-        const uint4 rw = raw[g4 / 2];
-        const uint32_t words[2] = {(g4 & 1) ? rw.z : rw.x, (g4 & 1) ? rw.w : rw.y};
+        const uint32_t words[2] = {valid ? lds32(qrow + 8u * (uint32_t)g4) : 0u,
+                                   valid ? lds32(qrow + 8u * (uint32_t)g4 + 4u) : 0u};
         float x[4], t0[4], t1[4], t2[4];
         x[0] = bf16_bits_to_f32(words[0] & 0xFFFFu) * sc;
         x[1] = bf16_bits_to_f32(words[0] >> 16) * sc;
@@ -577,16 +584,16 @@ struct MtpSoftmax {
     // PV(k - 1).
     if constexpr (FP8) {
       // FP16 V over the stage's K and V bytes, before waiting on the P slot.
-      // A token's FP8 V row is read, and its FP16 chunk rows written, only by
-      // the eight lanes of one warp that convert it, unit by unit: reading
-      // the unit before the warp writes is enough ordering for the in-place
-      // copy.
+      // Each FP16 chunk row of a token lies over that token's K bytes (which
+      // S has consumed) or over its own FP8 V bytes, and all of a token's V
+      // units are converted by lanes of one warp: every unit of the warp is
+      // read before the warp writes any, which orders the in-place copy.
+      uint4 wv[kVUnits];
 #pragma unroll
-      for (int j = 0; j < kVUnits; ++j) {
-        const uint4 w = load_v_unit(vst, j);
-        __syncwarp();
-        store_v16_unit(kst, sst, h, j, w);
-      }
+      for (int j = 0; j < kVUnits; ++j) wv[j] = load_v_unit(vst, j);
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < kVUnits; ++j) store_v16_unit(kst, sst, h, j, wv[j]);
     } else if (!interior) {
       clear_v_row(vst, h);
     }
