@@ -44,6 +44,7 @@ class Shape(ctypes.Structure):
         ("has_sinks", ctypes.c_int),
         ("topk", ctypes.c_int),
         ("sm_scale", ctypes.c_double),
+        ("q_dtype", ctypes.c_int),
     ]
 
 
@@ -77,6 +78,8 @@ class Oracle:
         lib.pa_oracle_e4m3_to_double.restype = ctypes.c_double
         lib.pa_oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
         lib.pa_oracle_bf16_to_double.restype = ctypes.c_double
+        lib.pa_oracle_f16_to_double.argtypes = [ctypes.c_uint16]
+        lib.pa_oracle_f16_to_double.restype = ctypes.c_double
         lib.pa_oracle_round_bf16.argtypes = [ctypes.c_double]
         lib.pa_oracle_round_bf16.restype = ctypes.c_uint16
         lib.pa_oracle_round_bf16_array.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t]
@@ -98,6 +101,9 @@ class Oracle:
     def bf16_to_double(self, bits) -> np.ndarray:
         return np.array([self.lib.pa_oracle_bf16_to_double(int(b)) for b in np.ravel(bits)])
 
+    def f16_to_double(self, bits) -> np.ndarray:
+        return np.array([self.lib.pa_oracle_f16_to_double(int(b)) for b in np.ravel(bits)])
+
     def round_bf16(self, x) -> np.ndarray:
         x = np.ascontiguousarray(np.ravel(x), dtype=np.float64)
         out = np.empty(x.shape, dtype=np.uint16)
@@ -114,7 +120,7 @@ class Oracle:
         return Shape(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.query_len,
                      w.page_size, w.max_pages_per_seq, w.num_pages, w.kv_dtype, w.scale_mode,
                      int(w.causal), int(w.window), int(w.sinks is not None), int(w.topk),
-                     sm_scale)
+                     sm_scale, int(getattr(w, "q_dtype", 0)))
 
     @staticmethod
     def _arrays(w):

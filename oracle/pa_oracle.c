@@ -23,7 +23,10 @@
  *       dequantised exactly (FP8 e4m3fn code times its per-tensor or per-token
  *       scale; BF16 widened), PR "Add paged-attention Tile kernel" (scales are
  *       a scalar or [num_blocks, num_kv_heads, block_size]).
- *     x_t = sm_scale * sum_d q[d] * k[d]
+ *     x_t = sm_scale * sum_d q[d] * k[d]  (q widened exactly from BF16 or FP16:
+ *       PR "Extend packed D256 PA decode pipe ...", Validation, and PR "Merge
+ *       gfx1250 PA decode partitions ...", Validation, run BF16 and FP16
+ *       queries)
  *     with sink s_h: m = max(max_t x_t, s_h), den = sum_t e^(x_t-m) + e^(s_h-m)
  *     without:        m = max_t x_t,          den = sum_t e^(x_t-m)
  *     out = sum_t e^(x_t-m) v_t / den; out = 0 when T is empty.
@@ -49,6 +52,7 @@
 #define PA_ORACLE_NO_MEM 3
 
 enum { ORACLE_KV_FP8 = 0, ORACLE_KV_BF16 = 1 };
+enum { ORACLE_Q_BF16 = 0, ORACLE_Q_FP16 = 1 };
 enum { ORACLE_SCALE_NONE = 0, ORACLE_SCALE_PER_TENSOR = 1, ORACLE_SCALE_PER_TOKEN = 2 };
 
 typedef struct {
@@ -67,6 +71,7 @@ typedef struct {
   int has_sinks;
   int topk; /* 0 = dense decode; > 0 = sparse index-list decode (QL must be 1) */
   double sm_scale;
+  int q_dtype; /* ORACLE_Q_BF16 or ORACLE_Q_FP16 (the query's element type) */
 } pa_oracle_shape;
 
 /* OCP 8-bit floating point, E4M3 ("fn": no infinities, S.1111.111 is NaN):
@@ -90,6 +95,27 @@ double pa_oracle_bf16_to_double(uint16_t bits) {
   float f;
   memcpy(&f, &w, sizeof f);
   return (double)f;
+}
+
+/* IEEE 754 binary16: sign, 5 exponent bits (bias 15), 10 fraction bits;
+ * exponent field 0 holds the subnormals f * 2^-24, 31 the infinities and
+ * NaNs. Widening is exact. */
+double pa_oracle_f16_to_double(uint16_t bits) {
+  int sign = (bits >> 15) & 1;
+  int e = (bits >> 10) & 0x1F;
+  int f = bits & 0x3FF;
+  double mag;
+  if (e == 0x1F)
+    mag = f ? NAN : INFINITY;
+  else if (e == 0)
+    mag = ldexp((double)f, -24);
+  else
+    mag = ldexp(1024.0 + (double)f, e - 25);
+  return sign ? -mag : mag;
+}
+
+static double q_element(const pa_oracle_shape* sh, const uint16_t* qrow, int d) {
+  return sh->q_dtype == ORACLE_Q_FP16 ? pa_oracle_f16_to_double(qrow[d]) : pa_oracle_bf16_to_double(qrow[d]);
 }
 
 /* Round a double to BF16 (8 significant bits, exponent range of binary32),
@@ -186,8 +212,7 @@ int pa_oracle_row_partial(const pa_oracle_shape* sh, const uint16_t* q, const vo
       return PA_ORACLE_BAD_PAGE;
     }
     for (int d = 0; d < D; ++d)
-      s += pa_oracle_bf16_to_double(qrow[d]) *
-           kv_element(sh, k_cache, k_scale, page, g, t % sh->page_size, d);
+      s += q_element(sh, qrow, d) * kv_element(sh, k_cache, k_scale, page, g, t % sh->page_size, d);
     x[j] = sh->sm_scale * s;
     if (x[j] > m) m = x[j];
   }
@@ -236,6 +261,7 @@ static int check_shape(const pa_oracle_shape* sh) {
   if (sh->num_q_heads % sh->num_kv_heads != 0) return PA_ORACLE_BAD_ARG;
   if (sh->topk > 0 && sh->query_len != 1) return PA_ORACLE_BAD_ARG;
   if (sh->window < 0) return PA_ORACLE_BAD_ARG;
+  if (sh->q_dtype != ORACLE_Q_BF16 && sh->q_dtype != ORACLE_Q_FP16) return PA_ORACLE_BAD_ARG;
   return PA_ORACLE_OK;
 }
 

@@ -47,6 +47,8 @@ KV_BF16 = 1
 SCALE_NONE = 0
 SCALE_PER_TENSOR = 1
 SCALE_PER_TOKEN = 2
+Q_BF16 = 0
+Q_FP16 = 1
 
 FP8_MAX = 448.0
 FP8_NAN = 0x7F
@@ -68,7 +70,7 @@ class Workload:
     max_pages_per_seq: int
     kv_dtype: int
     scale_mode: int
-    q: np.ndarray  # uint16 [B*QL, Hq, D] BF16 bits
+    q: np.ndarray  # uint16 [B*QL, Hq, D] BF16 or FP16 bits (q_dtype)
     k_cache: np.ndarray  # uint8 [P, Hkv, S, D] codes, or uint16 BF16 bits
     v_cache: np.ndarray
     block_table: np.ndarray  # int32 [B, max_pages_per_seq]
@@ -81,6 +83,7 @@ class Workload:
     topk: int = 0
     topk_idx: Optional[np.ndarray] = None  # int32 [B, topk]
     seed: int = 0
+    q_dtype: int = Q_BF16  # element type of q and of the output
 
     @property
     def group(self) -> int:
@@ -92,6 +95,16 @@ class Workload:
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
+
+
+def f16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to IEEE binary16 (torch's RNE cast) and return the bits."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+
+
+def q_bits(x: np.ndarray, q_dtype: int) -> np.ndarray:
+    return f16_bits(x) if q_dtype == Q_FP16 else bf16_bits(x)
 
 
 def bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -179,12 +192,13 @@ def _fill_cache(rng, num_pages, hkv, S, D, used_pages, valid_slots, kv_dtype,
 def make_dense(name, *, batch, hkv, group, head_dim, query_len, page_size,
                ctx_lens, kv_dtype, scale_mode, seed, pool_pages=None,
                causal=1, window=0, with_sinks=False, max_pages=None,
-               v_amplitude=1.0, vfun=None, q_amplitude=1.0, token_sigma=0.0):
+               v_amplitude=1.0, vfun=None, q_amplitude=1.0, token_sigma=0.0, q_dtype=Q_BF16):
     """Build a dense paged-decode workload with the given context lengths.
 
-    ``q_amplitude`` scales the N(0,1) query values before BF16 rounding (large
-    logits); ``token_sigma`` > 0 varies K and V token magnitudes by
-    e^(token_sigma * N(0,1)); ``v_amplitude`` scales V."""
+    ``q_amplitude`` scales the N(0,1) query values before rounding to the
+    query type ``q_dtype`` (BF16 or FP16; large logits); ``token_sigma`` > 0
+    varies K and V token magnitudes by e^(token_sigma * N(0,1));
+    ``v_amplitude`` scales V."""
     rng = np.random.default_rng(seed)
     ctx_lens = np.asarray(ctx_lens, dtype=np.int32)
     need = (ctx_lens.astype(np.int64) + page_size - 1) // page_size
@@ -202,7 +216,7 @@ def make_dense(name, *, batch, hkv, group, head_dim, query_len, page_size,
     qv = rng.standard_normal((batch * query_len, hq, head_dim), dtype=np.float32)
     if q_amplitude != 1.0:
         qv *= np.float32(q_amplitude)
-    q = bf16_bits(qv)
+    q = q_bits(qv, q_dtype)
     kc, ks = _fill_cache(rng, pool_pages, hkv, page_size, head_dim, used, valid,
                          kv_dtype, scale_mode, token_sigma=token_sigma)
     vc, vs = _fill_cache(rng, pool_pages, hkv, page_size, head_dim, used, valid,
@@ -217,7 +231,7 @@ def make_dense(name, *, batch, hkv, group, head_dim, query_len, page_size,
                     kv_dtype=kv_dtype, scale_mode=scale_mode, q=q, k_cache=kc,
                     v_cache=vc, block_table=table, ctx_lens=ctx_lens, k_scale=ks,
                     v_scale=vs, causal=causal, window=window, sinks=sinks,
-                    seed=seed)
+                    seed=seed, q_dtype=q_dtype)
 
 
 # --- the five workloads -----------------------------------------------------
@@ -285,7 +299,8 @@ def mtp4(seed: int = 1005, kv_dtype: int = KV_FP8, batch: int = 32,
 
 def sparse(seed: int = 1004, kv_dtype: int = KV_FP8, rows: int = 64,
            topk: int = 2048, context: int = 131072, pool_pages: int = 4096,
-           page_size: int = 16, head_dim: int = 128, group: int = 16) -> Workload:
+           page_size: int = 16, head_dim: int = 128, group: int = 16,
+           q_dtype: int = Q_BF16) -> Workload:
     """64 rows (QL1), 16 query heads, 1 KV head, D128, page 16, top-2048 of 131072."""
     rng = np.random.default_rng(seed)
     hkv = 1
@@ -300,7 +315,7 @@ def sparse(seed: int = 1004, kv_dtype: int = KV_FP8, rows: int = 64,
     used = np.arange(pool_pages)
     valid = np.full(pool_pages, page_size, dtype=np.int64)
     hq = hkv * group
-    q = bf16_bits(rng.standard_normal((rows, hq, head_dim), dtype=np.float32))
+    q = q_bits(rng.standard_normal((rows, hq, head_dim), dtype=np.float32), q_dtype)
     smode = SCALE_PER_TENSOR if kv_dtype == KV_FP8 else SCALE_NONE
     kc, ks = _fill_cache(rng, pool_pages, hkv, page_size, head_dim, used, valid, kv_dtype, smode)
     vc, vs = _fill_cache(rng, pool_pages, hkv, page_size, head_dim, used, valid, kv_dtype, smode)
@@ -310,7 +325,7 @@ def sparse(seed: int = 1004, kv_dtype: int = KV_FP8, rows: int = 64,
                     kv_dtype=kv_dtype, scale_mode=smode, q=q, k_cache=kc,
                     v_cache=vc, block_table=table, ctx_lens=ctx, k_scale=ks,
                     v_scale=vs, causal=0, window=0, sinks=None, topk=topk,
-                    topk_idx=idx, seed=seed)
+                    topk_idx=idx, seed=seed, q_dtype=q_dtype)
 
 
 def sparse_prefill(seed: int = 1006, kv_dtype: int = KV_FP8, rows: int = 1024,

@@ -48,7 +48,8 @@ def dequant(w, which: str) -> np.ndarray:
 
 
 def q_double(w) -> np.ndarray:
-    t = torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).view(torch.bfloat16)
+    qt = torch.float16 if getattr(w, "q_dtype", pw.Q_BF16) == pw.Q_FP16 else torch.bfloat16
+    t = torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).view(qt)
     return t.double().numpy()
 
 
@@ -148,6 +149,23 @@ def pin_bf16_widen(orc):
     assert np.array_equal(mine[ok], lib[ok]), "bf16 widening differs from torch"
 
 
+def pin_f16_widen(orc):
+    """All 65536 binary16 patterns against torch's float16 cast, plus values
+    that follow from the format's definition (IEEE 754 binary16: bias 15,
+    10 fraction bits, subnormals f * 2^-24)."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    mine = orc.f16_to_double(bits)
+    lib = torch.from_numpy(bits.view(np.int16)).view(torch.float16).double().numpy()
+    nan = np.isnan(lib)
+    assert np.array_equal(np.isnan(mine), nan), "f16 NaN patterns differ from torch"
+    assert np.array_equal(mine[~nan], lib[~nan]), "f16 widening differs from torch"
+    spot = {0x3C00: 1.0, 0xC000: -2.0, 0x7BFF: 65504.0, 0x0400: 2.0 ** -14, 0x0001: 2.0 ** -24,
+            0x03FF: 1023 * 2.0 ** -24, 0x3555: 0.333251953125, 0x7C00: np.inf, 0xFC00: -np.inf, 0x8000: -0.0}
+    for b, v in spot.items():
+        got = orc.f16_to_double([b])[0]
+        assert got == v and np.signbit(got) == np.signbit(v), (hex(b), got, v)
+
+
 def pin_bf16_round(orc):
     rng = np.random.default_rng(5)
     x = np.concatenate([
@@ -173,6 +191,8 @@ def pin_brute_force(orc):
         dict(seed=14, QL=2, causal=0, sinks=True, S=64, lens=(1, 70, 130)),
         dict(seed=15, scale=pw.SCALE_PER_TOKEN, QL=4, window=1, group=8, lens=(3, 33, 50)),
         dict(seed=16, hkv=3, group=1, QL=1, window=5, lens=(7, 16, 17, 45)),
+        dict(seed=17, q_dtype=pw.Q_FP16, QL=2, window=9, lens=(4, 31, 66)),
+        dict(seed=18, q_dtype=pw.Q_FP16, kv=pw.KV_BF16, group=8, sinks=True, lens=(2, 47)),
     ]
     for c in cases:
         w = small(**c)
@@ -396,7 +416,7 @@ def pin_poison_unread(orc):
 
 
 ALL_PINS = [
-    pin_e4m3_all_codes, pin_e4m3_golden, pin_bf16_widen, pin_bf16_round, pin_brute_force,
+    pin_e4m3_all_codes, pin_e4m3_golden, pin_bf16_widen, pin_f16_widen, pin_bf16_round, pin_brute_force,
     pin_one_token, pin_two_tokens, pin_constant_v, pin_window_one_position, pin_causal_prefix,
     pin_relocation, pin_empty, pin_merge_any_split, pin_sparse, pin_per_token_uniform,
     pin_gqa_heads, pin_poison_unread,

@@ -27,7 +27,12 @@ MUTANTS = [
     ("e4m3 subnormal", "ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
     ("per-token scale slot", "* sh->page_size + slot];", "* sh->page_size];"),
     ("V uses K scale", "kv_element(sh, v_cache, v_scale,", "kv_element(sh, v_cache, k_scale,"),
-    ("q operand reversed", "pa_oracle_bf16_to_double(qrow[d]) *", "pa_oracle_bf16_to_double(qrow[D - 1 - d]) *"),
+    ("q operand reversed", "s += q_element(sh, qrow, d) *", "s += q_element(sh, qrow, D - 1 - d) *"),
+    ("f16 bias", "ldexp(1024.0 + (double)f, e - 25)", "ldexp(1024.0 + (double)f, e - 24)"),
+    ("f16 subnormal", "mag = ldexp((double)f, -24);", "mag = ldexp((double)f, -25);"),
+    ("f16 queries read as bf16",
+     "return sh->q_dtype == ORACLE_Q_FP16 ? pa_oracle_f16_to_double(qrow[d]) : pa_oracle_bf16_to_double(qrow[d]);",
+     "return pa_oracle_bf16_to_double(qrow[d]);"),
     ("sparse context filter", "if (t >= 0 && t < L) tokens[n++] = t;", "if (t >= 0) tokens[n++] = t;"),
     ("merge without rescale", "out[d] += o[(size_t)j * D + d] * a;", "out[d] += o[(size_t)j * D + d];"),
     ("merge without sink", "if (has_sink) L += exp(sink - M);", "if (0) L += exp(sink - M);"),
