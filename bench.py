@@ -65,7 +65,8 @@ def measured_peak_gbs():
 # Sources that define each kernel: its own translation units and headers,
 # plus the shared header and the host code that sets its launch.
 KERNEL_SOURCES = {
-    "pa_tile": ("pa_tile.cuh", "pa_tile_fp8_d128.cu", "pa_tile_fp8_d256.cu", "pa_tile_bf16.cu"),
+    "pa_tile": ("pa_tile.cuh", "pa_tile_fp8_d128.cu", "pa_tile_fp8_d256.cu", "pa_tile_bf16.cu",
+                "pa_tile_bf16_q16.cu"),
     "pa_mtp": ("pa_tile.cuh", "pa_tc.cuh", "pa_mtp.cuh", "pa_mtp_fp8.cu", "pa_mtp_bf16.cu"),
     "pa_reduce": ("pa_tile.cuh", "pa_reduce.cu"),
 }

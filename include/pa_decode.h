@@ -86,6 +86,11 @@ typedef enum pa_status {
 } pa_status;
 
 enum { PA_KV_FP8_E4M3 = 0, PA_KV_BF16 = 1 };
+/* Element type of the queries and of the output (PR "Extend packed D256 PA
+ * decode pipe to page16, transposed V and sliding windows", Validation, and PR
+ * "Merge gfx1250 PA decode partitions in the tile kernel and speed up dense
+ * decode", Validation, run BF16 and FP16 queries). */
+enum { PA_Q_BF16 = 0, PA_Q_FP16 = 1 };
 enum { PA_SCALE_NONE = 0, PA_SCALE_PER_TENSOR = 1, PA_SCALE_PER_TOKEN = 2 };
 
 /* How partitions of one (sequence, KV head) are merged. */
@@ -136,6 +141,7 @@ typedef struct pa_plan_desc {
   int ctas_per_sm_override; /* 0 => occupancy query */
   int device;            /* CUDA device ordinal the plan is for */
   int consumer;          /* PA_CONSUMER_*; TMEM on an unsupported shape is PA_ERR_UNSUPPORTED */
+  int q_dtype;           /* PA_Q_*: element type of q and out (0 = BF16) */
 } pa_plan_desc;
 
 typedef struct pa_plan_info {
@@ -215,7 +221,9 @@ PA_API void pa_plan_destroy(pa_plan_t* plan);
  * value_scale, ...)), with the sliding window and sinks of PR "Extend packed
  * D256 PA decode pipe to page16, transposed V and sliding windows" and PR
  * "Merge gfx1250 PA decode partitions in the tile kernel and speed up dense
- * decode". window: 0 = off, else W >= 1 (requires causal or query_len 1).
+ * decode". q and out: device [batch * query_len, num_q_heads, head_dim]
+ * elements of the plan's q_dtype (BF16 or FP16), row-major; out is written
+ * in that type. window: 0 = off, else W >= 1 (requires causal or query_len 1).
  * Scales: required (device float32) when the plan's scale_mode is not NONE.
  * Errors: PA_ERR_INVALID_ARG (NULL or misaligned pointer, negative window,
  * sparse plan), PA_ERR_UNSUPPORTED (window with non-causal multi-token

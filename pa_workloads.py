@@ -374,11 +374,11 @@ def sparse_prefill(seed: int = 1006, kv_dtype: int = KV_FP8, rows: int = 1024,
 
 def small_sparse(seed: int = 2004, kv_dtype: int = KV_FP8, rows: int = 3,
                  topk: int = 200, context: int = 1000, pool_pages: int = 40,
-                 group: int = 16, head_dim: int = 128) -> Workload:
+                 group: int = 16, head_dim: int = 128, q_dtype: int = Q_BF16) -> Workload:
     """A few sparse rows small enough for per-element oracle parity."""
     w = sparse(seed=seed, kv_dtype=kv_dtype, rows=rows, topk=topk,
                context=context + (-context) % 16, pool_pages=pool_pages,
-               group=group, head_dim=head_dim)
+               group=group, head_dim=head_dim, q_dtype=q_dtype)
     ctx = np.asarray([context, context // 2, 0][:rows] + [context] * max(0, rows - 3),
                      dtype=np.int32)
     return w.with_(ctx_lens=ctx)

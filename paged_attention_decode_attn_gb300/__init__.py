@@ -22,7 +22,8 @@ __all__ = [
     "PA_ERR_DEVICE_STATUS", "PA_KV_FP8_E4M3", "PA_KV_BF16", "PA_SCALE_NONE", "PA_SCALE_PER_TENSOR",
     "PA_SCALE_PER_TOKEN", "PA_MERGE_AUTO", "PA_MERGE_DIRECT", "PA_MERGE_CLUSTER",
     "PA_MERGE_LAST_ARRIVER", "PA_MERGE_REDUCER", "PA_SCHED_AUTO", "PA_SCHED_BALANCED",
-    "PA_SCHED_PER_UNIT", "PA_CONSUMER_AUTO", "PA_CONSUMER_TILE", "PA_CONSUMER_TMEM", "PaError", "PlanDesc", "PlanInfo", "Plan", "library", "library_path",
+    "PA_SCHED_PER_UNIT", "PA_CONSUMER_AUTO", "PA_CONSUMER_TILE", "PA_CONSUMER_TMEM", "PA_Q_BF16",
+    "PA_Q_FP16", "PaError", "PlanDesc", "PlanInfo", "Plan", "library", "library_path",
     "pa_plan_create", "pa_plan_workspace_bytes", "pa_plan_set_workspace", "pa_plan_get_info",
     "pa_plan_destroy", "pa_decode", "pa_decode_sparse", "pa_decode_noalloc", "pa_strerror",
     "pa_last_error", "EXPORTED_SYMBOLS",
@@ -34,6 +35,7 @@ PA_SCALE_NONE, PA_SCALE_PER_TENSOR, PA_SCALE_PER_TOKEN = 0, 1, 2
 PA_MERGE_AUTO, PA_MERGE_DIRECT, PA_MERGE_CLUSTER, PA_MERGE_LAST_ARRIVER, PA_MERGE_REDUCER = range(5)
 PA_SCHED_AUTO, PA_SCHED_BALANCED, PA_SCHED_PER_UNIT = 0, 1, 2
 PA_CONSUMER_AUTO, PA_CONSUMER_TILE, PA_CONSUMER_TMEM = 0, 1, 2
+PA_Q_BF16, PA_Q_FP16 = 0, 1
 
 EXPORTED_SYMBOLS = [
     "pa_plan_create", "pa_plan_workspace_bytes", "pa_plan_set_workspace", "pa_plan_get_info",
@@ -58,7 +60,7 @@ class PlanDesc(ctypes.Structure):
         "has_sinks", "sparse_topk")] + [("sm_scale", ctypes.c_float)] + [
         (name, ctypes.c_int) for name in (
             "max_partitions", "merge_mode", "schedule", "sm_count_override",
-            "ctas_per_sm_override", "device", "consumer")]
+            "ctas_per_sm_override", "device", "consumer", "q_dtype")]
 
 
 class PlanInfo(ctypes.Structure):

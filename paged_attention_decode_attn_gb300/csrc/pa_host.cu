@@ -84,6 +84,9 @@ struct KernelShape {
 // MMA-issue warp.
 bool umma_supported(const pa_plan_desc& d, int R) {
   if (d.sparse_topk > 0 || R <= 16) return false;
+  // BF16 caches are read in place by BF16 MMAs, whose other operand (Q) must
+  // be BF16 too: FP16 queries there take the tile consumer.
+  if (d.kv_dtype == PA_KV_BF16 && d.q_dtype == PA_Q_FP16) return false;
   if (d.kv_dtype == PA_KV_FP8_E4M3) return d.head_dim == 128 || d.head_dim == 256;
   return d.head_dim == 128;
 }
@@ -190,7 +193,7 @@ const void* pick_tile_kernel(const pa_plan_desc& d, const KernelShape& k) {
     if (d.head_dim == 128) return pa::tile_kernel_fp8_d128(k.vtok, k.ncw > 4);
     return k.ncw > 4 ? nullptr : pa::tile_kernel_fp8_d256(k.vtok);
   }
-  return pa::tile_kernel_bf16(d.head_dim, k.ncw > 4);
+  return pa::tile_kernel_bf16(d.head_dim, k.ncw > 4, d.q_dtype == PA_Q_FP16);
 }
 
 pa_status validate_desc(const pa_plan_desc& d) {
@@ -220,6 +223,8 @@ pa_status validate_desc(const pa_plan_desc& d) {
     return fail(PA_ERR_INVALID_ARG, "unknown kv_dtype %d", d.kv_dtype);
   if (d.scale_mode < PA_SCALE_NONE || d.scale_mode > PA_SCALE_PER_TOKEN)
     return fail(PA_ERR_INVALID_ARG, "unknown scale_mode %d", d.scale_mode);
+  if (d.q_dtype != PA_Q_BF16 && d.q_dtype != PA_Q_FP16)
+    return fail(PA_ERR_INVALID_ARG, "unknown q_dtype %d", d.q_dtype);
   if (d.kv_dtype == PA_KV_BF16 && d.scale_mode != PA_SCALE_NONE)
     return fail(PA_ERR_INVALID_ARG, "BF16 caches take no K/V scales");
   if (d.sparse_topk < 0) return fail(PA_ERR_INVALID_ARG, "sparse_topk must be >= 0");
@@ -412,6 +417,7 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   p.topk = d.sparse_topk;
   p.has_sinks = d.has_sinks ? 1 : 0;
   p.scale_mode = d.kv_dtype == PA_KV_FP8_E4M3 ? d.scale_mode : pa::kScaleNone;
+  p.q_f16 = d.q_dtype == PA_Q_FP16;
   const float sm_scale = d.sm_scale > 0.f ? d.sm_scale : 1.0f / std::sqrt((float)d.head_dim);
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   p.sched = sched;

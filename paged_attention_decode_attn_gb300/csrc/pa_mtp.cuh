@@ -303,14 +303,15 @@ struct MtpSoftmax {
     for (int u = 0; u < EPT / 8; ++u) raw[u] = valid ? lds128(qrow + 16u * u) : make_uint4(0, 0, 0, 0);
     float cr = 0.f;
     if constexpr (FP8) {
+      const bool qh = p.q_f16 != 0;  // FP16 queries (else BF16), widened exactly either way
       float amax = 0.f;
 #pragma unroll
       for (int u = 0; u < EPT / 8; ++u) {
         const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[e] & 0xFFFFu)));
-          amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[e] >> 16)));
+          amax = fmaxf(amax, fabsf(q_bits_to_f32(w[e] & 0xFFFFu, qh)));
+          amax = fmaxf(amax, fabsf(q_bits_to_f32(w[e] >> 16, qh)));
         }
       }
 #pragma unroll
@@ -332,10 +333,10 @@ struct MtpSoftmax {
         const uint32_t words[2] = {valid ? lds32(qrow + 8u * (uint32_t)g4) : 0u,
                                    valid ? lds32(qrow + 8u * (uint32_t)g4 + 4u) : 0u};
         float x[4], t0[4], t1[4], t2[4];
-        x[0] = bf16_bits_to_f32(words[0] & 0xFFFFu) * sc;
-        x[1] = bf16_bits_to_f32(words[0] >> 16) * sc;
-        x[2] = bf16_bits_to_f32(words[1] & 0xFFFFu) * sc;
-        x[3] = bf16_bits_to_f32(words[1] >> 16) * sc;
+        x[0] = q_bits_to_f32(words[0] & 0xFFFFu, qh) * sc;
+        x[1] = q_bits_to_f32(words[0] >> 16, qh) * sc;
+        x[2] = q_bits_to_f32(words[1] & 0xFFFFu, qh) * sc;
+        x[3] = q_bits_to_f32(words[1] >> 16, qh) * sc;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           t0[e] = e4m3_lead(x[e]);
@@ -716,8 +717,8 @@ struct MtpSoftmax {
         if (whole) {
           const int qi = r / p.G, head = h.g * p.G + r % p.G;
           uint2 st;
-          st.x = pack_bf16(o.x, o.y);
-          st.y = pack_bf16(o.z, o.w);
+          st.x = pack_out(o.x, o.y, p.q_f16 != 0);
+          st.y = pack_out(o.z, o.w, p.q_f16 != 0);
           *reinterpret_cast<uint2*>(p.out + ((size_t)(h.b * p.QL + qi) * p.Hq + head) * D + d) = st;
         } else if (cluster) {
           *reinterpret_cast<float4*>(cp_o + (size_t)r * D + d) = o;

@@ -187,6 +187,17 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
   }
 }
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+__device__ __forceinline__ float f16_bits_to_f32(uint32_t bits16) {
+  return __half2float(__ushort_as_half((unsigned short)bits16));
+}
+// A query element (BF16 or FP16 bits in the low half of the word), widened exactly.
+__device__ __forceinline__ float q_bits_to_f32(uint32_t bits16, bool f16) {
+  return f16 ? f16_bits_to_f32(bits16) : bf16_bits_to_f32(bits16);
+}
+// Two output elements in the queries' type (round to nearest even).
+__device__ __forceinline__ uint32_t pack_out(float lo, float hi, bool f16) {
+  return f16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
+}
 
 // ------------------------------------------------------- schedule arithmetic
 // Visible token range of sequence b as a chunk range (union over the QL rows).
@@ -361,8 +372,8 @@ __device__ __forceinline__ void finalize_store(const PaParams& p, float vscale, 
   }
   const float inv = (L > 0.f) ? (1.f / L) * vscale : 0.f;
   uint2 st;
-  st.x = pack_bf16(O.x * inv, O.y * inv);
-  st.y = pack_bf16(O.z * inv, O.w * inv);
+  st.x = pack_out(O.x * inv, O.y * inv, p.q_f16 != 0);
+  st.y = pack_out(O.z * inv, O.w * inv, p.q_f16 != 0);
   *reinterpret_cast<uint2*>(p.out + ((size_t)(b * p.QL + i) * p.Hq + head) * D + d) = st;
 }
 
@@ -990,7 +1001,11 @@ struct StageView {
   }
 };
 
-template <bool FP8, int D, int NT, bool VTOK, int TW>
+// QF16 (BF16 caches only): the queries are FP16; each is split exactly into
+// BF16 hi + lo (an FP16 value's 11 significant bits leave at most 4 for lo)
+// and S takes one BF16 MMA per term. FP8 caches convert any query type to
+// FP16 operands at the segment start (a runtime flag).
+template <bool FP8, int D, int NT, bool VTOK, int TW, bool QF16 = false>
 struct Consumer {
   static constexpr int ELT = FP8 ? 1 : 2;
   static constexpr int NCH = D * ELT / 128;  // 128-byte column blocks per token row
@@ -1010,6 +1025,7 @@ struct Consumer {
   float kscale = 1.f, vscale = 1.f;
   // per segment
   uint32_t qf[NT][KSTEPS][2];
+  uint32_t qlo[QF16 ? NT : 1][QF16 ? KSTEPS : 1][2];  // FP16 queries on BF16 caches: the lo terms
   float crow[NT][2];
   int prow[NT][2];  // query position of the thread's two rows per n-tile
   float mrun[NT][2], lrun[NT][2];
@@ -1078,6 +1094,7 @@ struct Consumer {
       float crow_n = 0.f;
       if constexpr (FP8) {
         // 32 values per block: d in [cb*128 + 32*t4, +32)
+        const bool qh = p.q_f16 != 0;
         float amax = 0.f;
         uint4 raw[NCH][4];
 #pragma unroll
@@ -1092,8 +1109,8 @@ struct Consumer {
             const uint32_t w[4] = {raw[cb][v].x, raw[cb][v].y, raw[cb][v].z, raw[cb][v].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[e] & 0xFFFFu)));
-              amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[e] >> 16)));
+              amax = fmaxf(amax, fabsf(q_bits_to_f32(w[e] & 0xFFFFu, qh)));
+              amax = fmaxf(amax, fabsf(q_bits_to_f32(w[e] >> 16, qh)));
             }
           }
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
@@ -1116,9 +1133,10 @@ struct Consumer {
 #pragma unroll
             for (int hw = 0; hw < 2; ++hw) {
               const int s = cb * KS_BLK + 2 * v + hw;
-              qf[j][s][0] = pack_f16(bf16_bits_to_f32(w[2 * hw] & 0xFFFFu) * sc, bf16_bits_to_f32(w[2 * hw] >> 16) * sc);
-              qf[j][s][1] =
-                  pack_f16(bf16_bits_to_f32(w[2 * hw + 1] & 0xFFFFu) * sc, bf16_bits_to_f32(w[2 * hw + 1] >> 16) * sc);
+              qf[j][s][0] =
+                  pack_f16(q_bits_to_f32(w[2 * hw] & 0xFFFFu, qh) * sc, q_bits_to_f32(w[2 * hw] >> 16, qh) * sc);
+              qf[j][s][1] = pack_f16(q_bits_to_f32(w[2 * hw + 1] & 0xFFFFu, qh) * sc,
+                                     q_bits_to_f32(w[2 * hw + 1] >> 16, qh) * sc);
             }
           }
         crow_n = valid ? inv * p.sm_scale_log2 * (p.scale_mode == kScalePerTensor ? kscale : 1.f) : 0.f;
@@ -1130,10 +1148,22 @@ struct Consumer {
           for (int v = 0; v < 2; ++v) {
             const uint4 w = valid ? lds128(qrow + (uint32_t)(cb * 64 + 16 * t4) * 2u + 16u * v) : make_uint4(0, 0, 0, 0);
             const int s0 = cb * KS_BLK + 2 * v;
-            qf[j][s0][0] = w.x;
-            qf[j][s0][1] = w.y;
-            qf[j][s0 + 1][0] = w.z;
-            qf[j][s0 + 1][1] = w.w;
+            if constexpr (QF16) {
+              const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float a = f16_bits_to_f32(ww[e] & 0xFFFFu), b = f16_bits_to_f32(ww[e] >> 16);
+                const uint32_t hi = pack_bf16(a, b);
+                const uint32_t lo = pack_bf16(a - bf16_bits_to_f32(hi & 0xFFFFu), b - bf16_bits_to_f32(hi >> 16));
+                qf[j][s0 + e / 2][e & 1] = hi;
+                qlo[j][s0 + e / 2][e & 1] = lo;
+              }
+            } else {
+              qf[j][s0][0] = w.x;
+              qf[j][s0][1] = w.y;
+              qf[j][s0 + 1][0] = w.z;
+              qf[j][s0 + 1][1] = w.w;
+            }
           }
         crow_n = valid ? p.sm_scale_log2 : 0.f;
       }
@@ -1237,6 +1267,12 @@ struct Consumer {
               for (int j = 0; j < NT; ++j)
                 mma16816<false>(sacc[u][j], wa[2 * w2], wb[2 * w2], wa[2 * w2 + 1], wb[2 * w2 + 1], qf[j][s][0],
                                 qf[j][s][1]);
+              if constexpr (QF16) {
+#pragma unroll
+                for (int j = 0; j < NT; ++j)
+                  mma16816<false>(sacc[u][j], wa[2 * w2], wb[2 * w2], wa[2 * w2 + 1], wb[2 * w2 + 1], qlo[j][s][0],
+                                  qlo[j][s][1]);
+              }
             }
           }
         }
@@ -1651,7 +1687,7 @@ __device__ __forceinline__ void cluster_sync_all() {
 
 // MAXW: warps per CTA the instantiation is built for (5: up to 4 consumer
 // warps, two CTAs per SM at head_dim 128; 9: up to 8 row-slice warps).
-template <bool FP8, int D, int NT, bool VTOK, int TW, int MAXW>
+template <bool FP8, int D, int NT, bool VTOK, int TW, int MAXW, bool QF16 = false>
 __global__ void __launch_bounds__(MAXW * 32, (D == 128 && MAXW == 5) ? 2 : 1) pa_tile_kernel(const __grid_constant__ PaParams p,
                                                                       const __grid_constant__ CUtensorMap tmK,
                                                                       const __grid_constant__ CUtensorMap tmV) {
@@ -1689,7 +1725,7 @@ __global__ void __launch_bounds__(MAXW * 32, (D == 128 && MAXW == 5) ? 2 : 1) pa
       cluster_sync_all();
     }
   } else {
-    Consumer<FP8, D, NT, VTOK, TW> cons(p, sm);
+    Consumer<FP8, D, NT, VTOK, TW, QF16> cons(p, sm);
     cons.run();
     if (p.merge == kMergeCluster) {
       cluster_sync_all();

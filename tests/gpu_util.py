@@ -19,7 +19,8 @@ class DeviceWorkload:
     def __init__(self, w: pw.Workload, device="cuda"):
         self.w = w
         t = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a)).to(device)
-        self.q = t(w.q.view(np.int16)).view(torch.bfloat16)
+        qt = torch.float16 if w.q_dtype == pw.Q_FP16 else torch.bfloat16
+        self.q = t(w.q.view(np.int16)).view(qt)
         if w.kv_dtype == pw.KV_BF16:
             self.k = t(w.k_cache.view(np.int16)).view(torch.bfloat16)
             self.v = t(w.v_cache.view(np.int16)).view(torch.bfloat16)
@@ -41,12 +42,12 @@ class DeviceWorkload:
                  max_pages_per_seq=w.max_pages_per_seq, num_pages=w.num_pages,
                  max_context_len=int(w.ctx_lens.max()) if w.batch else 0, kv_dtype=w.kv_dtype,
                  scale_mode=w.scale_mode, causal=int(w.causal), has_sinks=int(w.sinks is not None),
-                 sparse_topk=int(w.topk))
+                 sparse_topk=int(w.topk), q_dtype=int(w.q_dtype))
         f.update(kw)
         return f
 
     def poison_out(self):
-        self.out.view(torch.int16).fill_(0x7FC0)  # BF16 NaN
+        self.out.view(torch.int16).fill_(0x7FC0)  # NaN in BF16 and in FP16
 
     def run(self, plan: pa.Plan, window=None, stream=None):
         w = self.w

@@ -92,6 +92,11 @@ PLAN_CASES = [
          consumer=pa.PA_CONSUMER_TMEM),
     desc(num_q_heads=24, num_kv_heads=8, query_len=4, kv_dtype=1, scale_mode=0, consumer=pa.PA_CONSUMER_TILE),
     desc(batch=32, num_q_heads=64, num_kv_heads=4, query_len=4, page_size=128, consumer=pa.PA_CONSUMER_TILE),
+    # FP16 queries: FP8 caches keep the tensor-memory consumer, BF16 caches take the tile consumer
+    desc(batch=32, num_q_heads=64, num_kv_heads=4, query_len=4, page_size=128, q_dtype=pa.PA_Q_FP16),
+    desc(batch=32, num_q_heads=64, num_kv_heads=4, query_len=4, page_size=128, kv_dtype=1, scale_mode=0,
+         q_dtype=pa.PA_Q_FP16),
+    desc(num_q_heads=8, num_kv_heads=8, kv_dtype=1, scale_mode=0, head_dim=256, q_dtype=pa.PA_Q_FP16),
     desc(batch=8, num_q_heads=32, num_kv_heads=2, query_len=2, scale_mode=2),  # FP8 per-token, 32 rows: auto
 ]
 
@@ -127,6 +132,9 @@ BAD = [
     (dict(max_partitions=300), pa.PA_ERR_INVALID_ARG),
     (dict(head_dim=256, num_q_heads=64, num_kv_heads=1), pa.PA_ERR_UNSUPPORTED),
     (dict(consumer=3), pa.PA_ERR_INVALID_ARG),
+    (dict(q_dtype=2), pa.PA_ERR_INVALID_ARG),
+    (dict(consumer=pa.PA_CONSUMER_TMEM, num_q_heads=64, num_kv_heads=4, kv_dtype=1, scale_mode=0,
+          q_dtype=pa.PA_Q_FP16), pa.PA_ERR_UNSUPPORTED),  # BF16 MMAs need BF16 queries
     (dict(consumer=pa.PA_CONSUMER_TMEM), pa.PA_ERR_UNSUPPORTED),  # 8 rows: tile consumer only
     (dict(consumer=pa.PA_CONSUMER_TMEM, num_q_heads=64, num_kv_heads=4, sparse_topk=64), pa.PA_ERR_UNSUPPORTED),
     (dict(consumer=pa.PA_CONSUMER_TMEM, num_q_heads=32, num_kv_heads=2, head_dim=256, kv_dtype=1, scale_mode=0),

@@ -192,3 +192,55 @@ def test_sparse_prefill_small(orc, kv):
         assert_parity(gpu, ref, what=f"sparse prefill {m}")
     gpu, plan = decode(dw)
     assert plan.info["merge_mode"] == pa.PA_MERGE_DIRECT  # rows >> SMs: one slot per row
+
+
+# FP16 queries (and FP16 output) on every consumer and cache format, with
+# whole and split units through the merge paths. FP8 caches convert the
+# queries exactly; BF16 caches split each into BF16 hi + lo (two MMAs).
+FP16_CASES = [
+    # id, kv, scale, group, query_len, head_dim, page, window, sinks, consumer the plan must take
+    ("fp8-gqa8", pw.KV_FP8, pw.SCALE_PER_TENSOR, 8, 1, 128, 16, 0, False, pa.PA_CONSUMER_TILE),
+    ("bf16-gqa8-mtp2-win", pw.KV_BF16, pw.SCALE_NONE, 8, 2, 128, 32, 37, True, pa.PA_CONSUMER_TILE),
+    ("fp8-gqa16-mtp4", pw.KV_FP8, pw.SCALE_PER_TENSOR, 16, 4, 128, 128, 0, False, pa.PA_CONSUMER_TMEM),
+    ("fp8-tok-gqa8-mtp4", pw.KV_FP8, pw.SCALE_PER_TOKEN, 8, 4, 128, 64, 0, True, pa.PA_CONSUMER_TMEM),
+    ("bf16-gqa16-mtp4", pw.KV_BF16, pw.SCALE_NONE, 16, 4, 128, 64, 0, False, pa.PA_CONSUMER_TILE),
+    ("bf16-gqa16-mtp2", pw.KV_BF16, pw.SCALE_NONE, 16, 2, 128, 16, 0, False, pa.PA_CONSUMER_TILE),
+    ("fp8-d256-tok-mtp4", pw.KV_FP8, pw.SCALE_PER_TOKEN, 8, 4, 256, 64, 17, True, pa.PA_CONSUMER_TMEM),
+    ("bf16-d256", pw.KV_BF16, pw.SCALE_NONE, 8, 1, 256, 64, 0, False, pa.PA_CONSUMER_TILE),
+]
+FP16_MODES = [
+    dict(),
+    dict(sm_count_override=5, ctas_per_sm_override=1, merge_mode=pa.PA_MERGE_REDUCER),
+    dict(schedule=pa.PA_SCHED_PER_UNIT, max_partitions=4, merge_mode=pa.PA_MERGE_CLUSTER),
+]
+
+
+@pytest.mark.parametrize("case", FP16_CASES, ids=[c[0] for c in FP16_CASES])
+def test_fp16_queries(orc, case):
+    name, kv, scale, group, ql, D, page, window, sinks, consumer = case
+    lens = [0, 1, 17, 130, 1000, 2300]
+    w = pw.make_dense("f16q-" + name, batch=len(lens), hkv=2, group=group, head_dim=D, query_len=ql,
+                      page_size=page, ctx_lens=lens, kv_dtype=kv, scale_mode=scale,
+                      seed=300 + FP16_CASES.index(case), causal=1, window=window, with_sinks=sinks,
+                      q_dtype=pw.Q_FP16)
+    # most query values need FP16's extra fraction bits (the BF16 lo term is exercised)
+    q32 = w.q.view(np.float16).astype(np.float32)
+    back = (pw.bf16_bits(q32).astype(np.uint32) << 16).view(np.float32)
+    assert np.mean(back != q32) > 0.5
+    ref = orc.decode(w)
+    dw = DeviceWorkload(w)
+    assert dw.out.dtype == torch.float16
+    for m in FP16_MODES:
+        gpu, plan = decode(dw, **m)
+        assert plan.info["consumer"] == consumer, (name, plan.info)
+        assert_parity(gpu, ref, what=f"fp16 queries {name} {m}")
+
+
+@pytest.mark.parametrize("kv", [pw.KV_FP8, pw.KV_BF16], ids=["fp8", "bf16"])
+def test_fp16_queries_sparse(orc, kv):
+    w = pw.small_sparse(kv_dtype=kv, rows=5, topk=300, context=1000, q_dtype=pw.Q_FP16)
+    ref = orc.decode(w)
+    dw = DeviceWorkload(w)
+    for m in SPARSE_MODES:
+        gpu, _ = decode(dw, **m)
+        assert_parity(gpu, ref, what=f"sparse fp16 queries {m}")
