@@ -31,7 +31,8 @@
  *
  * Layouts (all tensors are caller-owned device memory, row-major, contiguous)
  * --------------------------------------------------------------------------
- *   q, out        [batch*query_len, num_q_heads, head_dim]     BF16
+ *   q, out        [batch*query_len, num_q_heads, head_dim]     BF16 or FP16
+ *                 (the plan's q_dtype)
  *   k_cache,
  *   v_cache       [num_pages, num_kv_heads, page_size, head_dim]
  *                 FP8 e4m3fn bytes (OCP) or BF16
@@ -122,8 +123,8 @@ typedef struct pa_plan_desc {
   int batch;
   int num_q_heads;
   int num_kv_heads;      /* num_q_heads % num_kv_heads == 0 */
-  int head_dim;          /* 128 or 256 (PA_ERR_UNSUPPORTED otherwise) */
-  int query_len;         /* 1..4 (MTP rows); rows = query_len * group <= 64 */
+  int head_dim;          /* 128 or 256; 64 with BF16 caches (PA_ERR_UNSUPPORTED otherwise) */
+  int query_len;         /* >= 1 (MTP rows); rows = query_len * group <= 64 (32 at head_dim 256) */
   int page_size;         /* 16, 32, 64, 128 or 256 tokens */
   int max_pages_per_seq; /* block-table row stride (int32 elements) */
   int num_pages;         /* pages in the cache pool */

@@ -203,8 +203,8 @@ pa_status validate_desc(const pa_plan_desc& d) {
   if (d.num_q_heads % d.num_kv_heads != 0)
     return fail(PA_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", d.num_q_heads,
                 d.num_kv_heads);
-  if (d.head_dim != 128 && d.head_dim != 256)
-    return fail(PA_ERR_UNSUPPORTED, "head_dim %d unsupported (128 or 256)", d.head_dim);
+  if (d.head_dim != 128 && d.head_dim != 256 && !(d.head_dim == 64 && d.kv_dtype == PA_KV_BF16))
+    return fail(PA_ERR_UNSUPPORTED, "head_dim %d unsupported (128 or 256; 64 with BF16 caches)", d.head_dim);
   if (d.query_len < 1) return fail(PA_ERR_INVALID_ARG, "query_len must be >= 1 (got %d)", d.query_len);
   const long long rows = (long long)(d.num_q_heads / d.num_kv_heads) * d.query_len;
   if (rows > pa::kMaxRows)
@@ -320,7 +320,7 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   // least 3); the others one CTA per SM and up to 226 KiB.
   // The Q ring has two slots (the next segment's rows load while the current
   // one streams) unless that costs the third stage; one slot then.
-  const bool two_per_sm = !k.umma && d.head_dim == 128 && k.ncw <= 4;
+  const bool two_per_sm = !k.umma && d.head_dim <= 128 && k.ncw <= 4;
   int ns = 0, nq = 2;
   int budget = kSmemTwoPerSm;
   for (int attempt = two_per_sm ? 0 : 1; attempt < 2 && ns < 3; ++attempt) {

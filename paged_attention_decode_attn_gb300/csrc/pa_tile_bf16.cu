@@ -8,6 +8,9 @@ const void* tile_kernel_bf16(int d, int wide, int q_f16) {
   if (d == 128 && !wide) return reinterpret_cast<const void*>(&dev::pa_tile_kernel<false, 128, 1, false, 1, 5>);
   if (d == 128 && wide) return reinterpret_cast<const void*>(&dev::pa_tile_kernel<false, 128, 1, false, 1, 9>);
   if (d == 256 && !wide) return reinterpret_cast<const void*>(&dev::pa_tile_kernel<false, 256, 1, false, 1, 5>);
+  // head_dim 64: one 128-byte block per token row, like FP8 head_dim 128
+  if (d == 64 && !wide) return reinterpret_cast<const void*>(&dev::pa_tile_kernel<false, 64, 1, false, 1, 5>);
+  if (d == 64 && wide) return reinterpret_cast<const void*>(&dev::pa_tile_kernel<false, 64, 1, false, 1, 9>);
   return nullptr;
 }
 }  // namespace pa

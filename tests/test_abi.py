@@ -97,6 +97,9 @@ PLAN_CASES = [
     desc(batch=32, num_q_heads=64, num_kv_heads=4, query_len=4, page_size=128, kv_dtype=1, scale_mode=0,
          q_dtype=pa.PA_Q_FP16),
     desc(num_q_heads=8, num_kv_heads=8, kv_dtype=1, scale_mode=0, head_dim=256, q_dtype=pa.PA_Q_FP16),
+    # BF16 head_dim 64 (one 128-byte block per token row)
+    desc(num_q_heads=64, num_kv_heads=8, kv_dtype=1, scale_mode=0, head_dim=64),
+    desc(num_q_heads=64, num_kv_heads=1, kv_dtype=1, scale_mode=0, head_dim=64, q_dtype=pa.PA_Q_FP16),
     desc(batch=8, num_q_heads=32, num_kv_heads=2, query_len=2, scale_mode=2),  # FP8 per-token, 32 rows: auto
 ]
 
@@ -112,7 +115,8 @@ def test_plan_matches_rule(lib, d):
 
 
 BAD = [
-    (dict(head_dim=64), pa.PA_ERR_UNSUPPORTED),
+    (dict(head_dim=64), pa.PA_ERR_UNSUPPORTED),  # FP8 caches: 128 or 256 only
+    (dict(head_dim=96, kv_dtype=1, scale_mode=0), pa.PA_ERR_UNSUPPORTED),
     (dict(num_q_heads=60), pa.PA_ERR_INVALID_ARG),
     (dict(kv_dtype=1, scale_mode=1), pa.PA_ERR_INVALID_ARG),
     (dict(num_q_heads=64, num_kv_heads=1), pa.PA_ERR_UNSUPPORTED),  # 64 rows * QL1 ok? -> 64 ok

@@ -244,3 +244,31 @@ def test_fp16_queries_sparse(orc, kv):
     for m in SPARSE_MODES:
         gpu, _ = decode(dw, **m)
         assert_parity(gpu, ref, what=f"sparse fp16 queries {m}")
+
+
+# BF16 caches at head_dim 64 (one 128-byte block per token row), every merge
+# path, with BF16 and FP16 queries.
+@pytest.mark.parametrize("group,ql,window,sinks", [(8, 1, 0, False), (4, 3, 17, True), (16, 4, 0, False),
+                                                   (64, 1, 0, True)], ids=["gqa8", "gqa4-mtp3-win", "gqa16-mtp4",
+                                                                           "gqa64"])
+@pytest.mark.parametrize("q_dtype", [pw.Q_BF16, pw.Q_FP16], ids=["qbf16", "qfp16"])
+def test_bf16_head_dim_64(orc, group, ql, window, sinks, q_dtype):
+    lens = [0, 1, 65, 300, 1777]
+    w = pw.make_dense("d64", batch=len(lens), hkv=2, group=group, head_dim=64, query_len=ql, page_size=16,
+                      ctx_lens=lens, kv_dtype=pw.KV_BF16, scale_mode=pw.SCALE_NONE, seed=400 + group + ql,
+                      causal=1, window=window, with_sinks=sinks, q_dtype=q_dtype)
+    ref = orc.decode(w)
+    dw = DeviceWorkload(w)
+    for m in MODES:
+        gpu, plan = decode(dw, **m)
+        assert plan.info["consumer"] == pa.PA_CONSUMER_TILE
+        assert_parity(gpu, ref, what=f"head_dim 64 {m}")
+
+
+def test_bf16_head_dim_64_sparse(orc):
+    w = pw.small_sparse(kv_dtype=pw.KV_BF16, rows=5, topk=300, context=1000, head_dim=64)
+    ref = orc.decode(w)
+    dw = DeviceWorkload(w)
+    for m in SPARSE_MODES:
+        gpu, _ = decode(dw, **m)
+        assert_parity(gpu, ref, what=f"sparse head_dim 64 {m}")
