@@ -32,6 +32,7 @@ import re
 import subprocess
 import sys
 import time
+from typing import Optional
 
 import numpy as np
 
@@ -90,11 +91,27 @@ def kernel_source_hash(kernel: str = "pa_tile") -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str = "dense", kernel: str = "pa_tile"):
-    """DRAM bytes per launch from the committed ncu summary of this kernel on
-    this workload (profiles/<kernel>_<workload>.md), if it was taken on the
-    current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+def profile_name(args, kernel: str) -> Optional[str]:
+    """Name of the committed ncu summary for this bench line's kernel and
+    workload (<kernel>_<workload>[_bf16][_ql<N>]), or None when the line runs
+    a non-default size or variant (no summary covers it)."""
+    if args.batch or args.page != 16 or args.window or args.sinks or args.partitions or args.merge != "auto" \
+            or args.consumer != "auto" or (args.workload == "sparse_prefill" and args.rows != 1024):
+        return None
+    name = f"{kernel}_{args.workload}"
+    if args.kv == "bf16" and args.workload in ("sparse", "mtp4", "sparse_prefill"):
+        name += "_bf16"
+    if args.workload == "d256" and args.ql != 1:
+        name += f"_ql{args.ql}"
+    return name
+
+
+def profiled_traffic(name: Optional[str], kernel: str = "pa_tile"):
+    """DRAM bytes per launch from the committed ncu summary profiles/<name>.md,
+    if it was taken on the current sources of `kernel`; else None."""
+    if name is None:
+        return None
+    path = os.path.join(ROOT, "profiles", f"{name}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -259,13 +276,13 @@ CONSUMERS = {"auto": 0, "tile": 1, "tmem": 2}
 def make_workload(args, rank):
     kv = pw.KV_BF16 if args.kv == "bf16" else pw.KV_FP8
     if args.workload == "dense":
-        return pw.dense(seed=1002 + rank, page_size=args.page)
+        return pw.dense(seed=1002 + rank, page_size=args.page, batch=args.batch or 64)
     if args.workload == "tiny":
         return pw.tiny()
     if args.workload == "d256":
         return pw.d256(query_len=args.ql, window=args.window, with_sinks=args.sinks, batch=args.batch or 16)
     if args.workload == "sparse":
-        return pw.sparse(kv_dtype=kv)
+        return pw.sparse(kv_dtype=kv, rows=args.batch or 64)
     if args.workload == "mtp4":
         return pw.mtp4(kv_dtype=kv, batch=args.batch or 32)
     if args.workload == "sparse_prefill":
@@ -483,7 +500,8 @@ def main():
                                                          "ctas_per_sm", "launches_per_call")}},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
-                         "traffic": profiled_traffic(args.workload, kernel_name.replace("_kernel", "")),
+                         "traffic": profiled_traffic(profile_name(args, kernel_name.replace("_kernel", "")),
+                                                     kernel_name.replace("_kernel", "")),
                          "algorithmic_bytes_per_launch": alg, "kernel": kernel_name},
             "e2e": {"value": e2e_bytes / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "steps": e2e_steps},

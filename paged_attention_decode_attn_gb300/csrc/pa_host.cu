@@ -314,13 +314,16 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   pl->reduce_fn = pa::reduce_kernel(d.head_dim);
   if (!pl->tile_fn || !pl->reduce_fn) return fail(PA_ERR_UNSUPPORTED, "no kernel for this configuration");
 
-  // Ring depth. Kernels light enough for two CTAs per SM (head_dim 128 with
-  // 8-row warp tiles: at most 168 registers, so three warps share an SM
-  // sub-partition's register file) get as many stages as fit 112 KiB (at
-  // least 3); the others one CTA per SM and up to 226 KiB.
-  // The Q ring has two slots (the next segment's rows load while the current
-  // one streams) unless that costs the third stage; one slot then.
-  const bool two_per_sm = !k.umma && d.head_dim <= 128 && k.ncw <= 4;
+  // Ring depth. Kernels light enough for two CTAs per SM (at most four
+  // consumer warps and 168 registers, so three warps share an SM
+  // sub-partition's register file: head_dim 64/128, and FP8 head_dim 256,
+  // measured 16 % faster than one CTA per SM on the long-context D256 decode)
+  // get as many stages as fit 112 KiB (at least 3); the others one CTA per SM
+  // and up to 226 KiB. The Q ring has two slots (the next segment's rows load
+  // while the current one streams) unless that costs the third stage; one
+  // slot then.
+  const bool two_per_sm =
+      !k.umma && k.ncw <= 4 && (d.head_dim <= 128 || d.kv_dtype == PA_KV_FP8_E4M3);
   int ns = 0, nq = 2;
   int budget = kSmemTwoPerSm;
   for (int attempt = two_per_sm ? 0 : 1; attempt < 2 && ns < 3; ++attempt) {

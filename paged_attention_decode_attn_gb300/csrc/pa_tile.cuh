@@ -1686,9 +1686,10 @@ __device__ __forceinline__ void cluster_sync_all() {
 }
 
 // MAXW: warps per CTA the instantiation is built for (5: up to 4 consumer
-// warps, two CTAs per SM at head_dim 128; 9: up to 8 row-slice warps).
+// warps, two CTAs per SM at head_dim 64/128 and FP8 head_dim 256; 9: up to 8
+// row-slice warps).
 template <bool FP8, int D, int NT, bool VTOK, int TW, int MAXW, bool QF16 = false>
-__global__ void __launch_bounds__(MAXW * 32, (D <= 128 && MAXW == 5) ? 2 : 1) pa_tile_kernel(const __grid_constant__ PaParams p,
+__global__ void __launch_bounds__(MAXW * 32, (MAXW == 5 && (D <= 128 || FP8)) ? 2 : 1) pa_tile_kernel(const __grid_constant__ PaParams p,
                                                                       const __grid_constant__ CUtensorMap tmK,
                                                                       const __grid_constant__ CUtensorMap tmV) {
   extern __shared__ uint8_t smem_raw[];

@@ -65,7 +65,7 @@ def smem_total(d, k, ns, cluster, nq):
 def plan(d):
     """Expected pa_plan_info fields for a descriptor dict with overrides set."""
     k = kernel_shape(d)
-    two = not k["umma"] and d["head_dim"] <= 128 and k["ncw"] <= 4
+    two = not k["umma"] and k["ncw"] <= 4 and (d["head_dim"] <= 128 or d["kv_dtype"] == 0)
     ns, budget = 0, SMEM_TWO
     cl0 = d.get("sparse_topk", 0) > 0 or d.get("merge_mode", 0) == 2
     for attempt in range(0 if two else 1, 2):
