@@ -107,7 +107,8 @@ enum {
  * (any shape); the tensor-memory consumer issues tcgen05.mma from a dedicated
  * warp with accumulators in TMEM, two softmax warpgroups splitting the rows
  * (dense decode with 17..64 rows per KV head, FP8 head_dim 128/256 or BF16
- * head_dim 128; head_dim 256 up to 32 rows). AUTO takes the tensor-memory
+ * head_dim 128 with BF16 queries; head_dim 256 with 9..32 rows). AUTO takes
+ * the tensor-memory
  * consumer wherever it covers the shape (measured faster on every such
  * shape), else the tile consumer. */
 enum { PA_CONSUMER_AUTO = 0, PA_CONSUMER_TILE = 1, PA_CONSUMER_TMEM = 2 };

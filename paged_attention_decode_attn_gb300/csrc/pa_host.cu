@@ -81,9 +81,11 @@ struct KernelShape {
 // Groups of more than 16 query rows per KV head (MTP verify, wide GQA) on
 // dense decode can run the tensor-memory (tcgen05) consumer: two softmax
 // warpgroups over one MMA block of up to 64 rows, a producer warp and an
-// MMA-issue warp.
+// MMA-issue warp. At head_dim 256 it also takes 9-16 rows (measured 9 %
+// faster than the tile consumer on the long-context D256 decode at query
+// length 2; at head_dim 128 the tile consumer stays ahead up to 16 rows).
 bool umma_supported(const pa_plan_desc& d, int R) {
-  if (d.sparse_topk > 0 || R <= 16) return false;
+  if (d.sparse_topk > 0 || R <= (d.head_dim == 256 ? 8 : 16)) return false;
   // BF16 caches are read in place by BF16 MMAs, whose other operand (Q) must
   // be BF16 too: FP16 queries there take the tile consumer.
   if (d.kv_dtype == PA_KV_BF16 && d.q_dtype == PA_Q_FP16) return false;
@@ -243,8 +245,8 @@ pa_status validate_desc(const pa_plan_desc& d) {
   if (d.consumer == PA_CONSUMER_TMEM &&
       !umma_supported(d, d.query_len * (d.num_kv_heads > 0 ? d.num_q_heads / d.num_kv_heads : 0)))
     return fail(PA_ERR_UNSUPPORTED,
-                "the tensor-memory consumer needs dense decode, 17..64 rows per KV head, FP8 head_dim 128/256 or "
-                "BF16 head_dim 128");
+                "the tensor-memory consumer needs dense decode, 17..64 rows per KV head (9..32 at head_dim 256), "
+                "FP8 head_dim 128/256 or BF16 head_dim 128 with BF16 queries");
   if (d.sm_count_override < 0 || d.ctas_per_sm_override < 0)
     return fail(PA_ERR_INVALID_ARG, "overrides must be >= 0");
   return PA_OK;

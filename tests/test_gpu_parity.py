@@ -79,7 +79,7 @@ def test_d256_per_token_mtp_windows(orc, ql, window):
     ref = orc.decode(w)
     dw = DeviceWorkload(w)
     modes = [dict(), dict(sm_count_override=4, ctas_per_sm_override=1)]
-    if 8 * ql > 16:  # tensor-memory consumer
+    if 8 * ql > 8:  # tensor-memory consumer (head_dim 256: more than 8 rows)
         modes += [dict(consumer=pa.PA_CONSUMER_TMEM),
                   dict(consumer=pa.PA_CONSUMER_TMEM, sm_count_override=4, ctas_per_sm_override=1)]
     for m in modes:

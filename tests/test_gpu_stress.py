@@ -56,7 +56,7 @@ CONDITIONS = ["q_x8", "q_x16", "planted_key", "zero_q_rows", "token_magnitudes",
 def _consumers(group, ql, head_dim, kv):
     out = [pa.PA_CONSUMER_TILE]
     R = group * ql
-    if R > 16 and (head_dim == 128 or kv == pw.KV_FP8):
+    if R > (8 if head_dim == 256 else 16) and (head_dim == 128 or kv == pw.KV_FP8):
         out.append(pa.PA_CONSUMER_TMEM)
     return out
 
