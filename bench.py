@@ -514,9 +514,11 @@ def main():
             line["warm_protocol"] = "10-call CUDA graph x 5 replays, min of 5 runs, median of 3 rounds, no L2 eviction"
         if world == 1 and not args.no_cpu_baseline and args.workload == "dense":
             cores = host_cores()
-            cb = cpu_baseline(w, units=max(CPU_SAMPLE_UNITS, 4 * cores), threads=cores)
+            # all host cores over every unit of the workload (a few seconds on
+            # 16 cores), and one thread over a sample of 64 units
+            cb = cpu_baseline(w, units=w.batch * w.num_kv_heads, threads=cores)
             cb.pop("seconds")
-            single = cpu_baseline(w, units=CPU_SAMPLE_UNITS // 2, seed=1)
+            single = cpu_baseline(w, units=64, seed=1)
             single.pop("seconds")
             cb["single_thread"] = single
             line["cpu_baseline"] = cb
