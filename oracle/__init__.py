@@ -93,6 +93,8 @@ class Oracle:
         lib.pa_oracle_merge.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp, ctypes.c_int,
                                         ctypes.c_double, vp]
         lib.pa_oracle_merge.restype = None
+        lib.pa_oracle_mqa_logits.argtypes = [ctypes.c_int] * 4 + [vp] * 6 + [ctypes.c_int] + [vp] * 4
+        lib.pa_oracle_mqa_logits.restype = ctypes.c_int
 
     # --- element codecs ---------------------------------------------------
     def e4m3_to_double(self, codes) -> np.ndarray:
@@ -175,6 +177,42 @@ class Oracle:
         self.lib.pa_oracle_merge(n, D, _ptr(m), _ptr(l), _ptr(o), int(sink is not None),
                                  float(sink) if sink is not None else 0.0, _ptr(out))
         return out
+
+
+class LogitsCase:
+    """Indexer-logits inputs as host arrays (see pa_oracle_mqa_logits)."""
+
+    def __init__(self, q, kv, kv_scale, weights, ks, ke):
+        self.q = np.ascontiguousarray(q, dtype=np.uint8)  # [rows, heads, dim] e4m3 codes
+        self.kv = np.ascontiguousarray(kv, dtype=np.uint8)  # [num_kv, dim]
+        self.kv_scale = np.ascontiguousarray(kv_scale, dtype=np.float32)
+        self.weights = np.ascontiguousarray(weights, dtype=np.float32)  # [rows, heads]
+        self.ks = np.ascontiguousarray(ks, dtype=np.int32)
+        self.ke = np.ascontiguousarray(ke, dtype=np.int32)
+
+
+def mqa_logits(orc: Oracle, case: LogitsCase, rows_idx, cols_idx):
+    """(logits, bound) at the listed (row, token) pairs, float64; -inf outside windows."""
+    r = np.ascontiguousarray(rows_idx, dtype=np.int32).ravel()
+    j = np.ascontiguousarray(cols_idx, dtype=np.int32).ravel()
+    out = np.empty(r.size)
+    bound = np.empty(r.size)
+    rows, heads, dim = case.q.shape
+    rc = orc.lib.pa_oracle_mqa_logits(rows, heads, dim, case.kv.shape[0], _ptr(case.q), _ptr(case.kv),
+                                      _ptr(case.kv_scale), _ptr(case.weights), _ptr(case.ks), _ptr(case.ke),
+                                      r.size, _ptr(r), _ptr(j), _ptr(out), _ptr(bound))
+    if rc != 0:
+        raise RuntimeError(f"oracle logits failed with code {rc}")
+    return out, bound
+
+
+def mqa_logits_full(orc: Oracle, case: LogitsCase):
+    """The whole [rows, num_kv] logits matrix and its bounds (small cases)."""
+    rows = case.q.shape[0]
+    n = case.kv.shape[0]
+    rr, jj = np.meshgrid(np.arange(rows), np.arange(n), indexing="ij")
+    out, bound = mqa_logits(orc, case, rr, jj)
+    return out.reshape(rows, n), bound.reshape(rows, n)
 
 
 def get() -> Oracle:

@@ -329,3 +329,52 @@ int pa_oracle_decode(const pa_oracle_shape* sh, const uint16_t* q, const void* k
 void pa_oracle_round_bf16_array(const double* x, uint16_t* bits, size_t n) {
   for (size_t k = 0; k < n; ++k) bits[k] = pa_oracle_round_bf16(x[k]);
 }
+
+/*
+ * Indexer logits (PR "[FlyDSL] fp8_mqa_logits gfx942: add LDS-staged variant,
+ * use it by default", Summary and Changes: FP8 queries and KV, a ReLU x
+ * weight epilogue reduced over the heads, per-row KV windows, -inf written
+ * outside them when clean_logits is set). For query row r and KV token j:
+ *
+ *   inside the window (ks[r] <= j < ke[r], 0 <= j < num_kv):
+ *     logit = sum_h w[r][h] * max(0, kv_scale[j] * sum_d q[r][h][d] * kv[j][d])
+ *   outside: -inf
+ *
+ * with q and kv e4m3 codes decoded exactly. The reading where the page is
+ * silent: the per-token KV scale multiplies the dot product before the ReLU.
+ * Computed for the n listed (r, j) pairs; bound[i] receives
+ * sum_h |w| * |kv_scale| * sum_d |q * kv| (the magnitude an FP32 evaluation's
+ * rounding is proportional to), 0 outside the window.
+ */
+int pa_oracle_mqa_logits(int rows, int heads, int dim, int num_kv, const uint8_t* q, const uint8_t* kv,
+                         const float* kv_scale, const float* weights, const int32_t* ks, const int32_t* ke,
+                         int n, const int32_t* pr, const int32_t* pj, double* out, double* bound) {
+  if (rows < 0 || heads <= 0 || dim <= 0 || num_kv < 0 || n < 0) return PA_ORACLE_BAD_ARG;
+  for (int i = 0; i < n; ++i) {
+    int r = pr[i], j = pj[i];
+    if (r < 0 || r >= rows || j < 0 || j >= num_kv) return PA_ORACLE_BAD_ARG;
+    if (!(j >= ks[r] && j < ke[r])) {
+      out[i] = -INFINITY;
+      bound[i] = 0.0;
+      continue;
+    }
+    {
+      double sc = (double)kv_scale[j], acc = 0.0, mag = 0.0;
+      for (int h = 0; h < heads; ++h) {
+        double s = 0.0, a = 0.0, w = (double)weights[(size_t)r * heads + h];
+        for (int d = 0; d < dim; ++d) {
+          double x = pa_oracle_e4m3_to_double(q[((size_t)r * heads + h) * dim + d]) *
+                     pa_oracle_e4m3_to_double(kv[(size_t)j * dim + d]);
+          s += x;
+          a += fabs(x);
+        }
+        s *= sc;
+        acc += w * (s > 0.0 ? s : 0.0);
+        mag += fabs(w) * fabs(sc) * a;
+      }
+      out[i] = acc;
+      bound[i] = mag;
+    }
+  }
+  return PA_ORACLE_OK;
+}

@@ -419,3 +419,69 @@ def algorithmic_bytes(w: Workload, visible_tokens: Optional[np.ndarray] = None) 
     if w.sinks is not None:
         total += w.num_q_heads * 4
     return int(total)
+
+
+# --- indexer logits ------------------------------------------------------------
+
+@dataclasses.dataclass
+class LogitsWorkload:
+    """Inputs of the indexer-logits op (host arrays)."""
+
+    name: str
+    q: np.ndarray         # uint8 e4m3 [rows, heads, dim]
+    kv: np.ndarray        # uint8 e4m3 [num_kv, dim]
+    kv_scale: np.ndarray  # float32 [num_kv]
+    weights: np.ndarray   # float32 [rows, heads]
+    ks: np.ndarray        # int32 [rows] window start
+    ke: np.ndarray        # int32 [rows] window end (exclusive)
+    seed: int = 0
+
+    @property
+    def rows(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def heads(self) -> int:
+        return self.q.shape[1]
+
+    @property
+    def num_kv(self) -> int:
+        return self.kv.shape[0]
+
+    def window_tokens(self) -> int:
+        a = np.clip(self.ks.astype(np.int64), 0, self.num_kv)
+        e = np.clip(self.ke.astype(np.int64), 0, self.num_kv)
+        return int(np.maximum(0, e - a).sum())
+
+    def flops(self) -> int:
+        """Multiply-adds of the scores inside the windows, 2 FLOPs each."""
+        return 2 * self.window_tokens() * self.heads * self.q.shape[2]
+
+
+def indexer(seed: int = 1007, rows: int = 1024, heads: int = 64, num_kv: int = 131072, dim: int = 128,
+            window: str = "chunk") -> LogitsWorkload:
+    """Indexer logits over a prompt chunk: `rows` query rows, `heads` heads,
+    FP8 queries and an FP8 KV list of `num_kv` tokens with per-token scales.
+    window "chunk": the chunk's rows are the last `rows` positions of the KV
+    list (a cached prefix before them), row r sees [0, num_kv - rows + r + 1);
+    "random": each row sees a random interval (empty ones included)."""
+    rng = np.random.default_rng(seed)
+    qv = rng.standard_normal((rows, heads, dim), dtype=np.float32)
+    q = fp8_codes(qv)
+    kvv = rng.standard_normal((num_kv, dim), dtype=np.float32)
+    amax = np.abs(kvv).max(axis=1)
+    scale = np.where(amax > 0, amax / FP8_MAX, 1.0).astype(np.float32)
+    kv = fp8_codes(kvv / scale[:, None])
+    weights = (rng.standard_normal((rows, heads), dtype=np.float32) / np.sqrt(heads)).astype(np.float32)
+    if window == "chunk":
+        ks = np.zeros(rows, dtype=np.int32)
+        ke = (num_kv - rows + np.arange(rows) + 1).clip(0, num_kv).astype(np.int32)
+    elif window == "random":
+        a = rng.integers(-5, num_kv, size=rows)
+        b = a + rng.integers(-3, num_kv // 2 + 3, size=rows)
+        ks = a.astype(np.int32)
+        ke = b.clip(-10, num_kv + 10).astype(np.int32)
+    else:
+        raise ValueError(window)
+    return LogitsWorkload(name=f"indexer-{window}", q=q, kv=kv, kv_scale=scale, weights=weights, ks=ks, ke=ke,
+                          seed=seed)

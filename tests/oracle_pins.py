@@ -415,9 +415,71 @@ def pin_poison_unread(orc):
         assert np.all(np.isfinite(out)), w.name
 
 
+# --- indexer-logits pins ------------------------------------------------------------
+
+def _logits_case(w):
+    import oracle
+
+    return oracle.LogitsCase(w.q, w.kv, w.kv_scale, w.weights, w.ks, w.ke)
+
+
+def logits_brute_force(w) -> np.ndarray:
+    """Float64 logits from torch's e4m3 casts and NumPy einsums, with an explicit window mask."""
+    qf = torch.from_numpy(np.ascontiguousarray(w.q)).view(torch.float8_e4m3fn).double().numpy()
+    kf = torch.from_numpy(np.ascontiguousarray(w.kv)).view(torch.float8_e4m3fn).double().numpy()
+    s = np.einsum("rhd,jd->rhj", qf, kf) * w.kv_scale.astype(np.float64)[None, None, :]
+    out = np.einsum("rh,rhj->rj", w.weights.astype(np.float64), np.maximum(s, 0.0))
+    j = np.arange(w.num_kv)[None, :]
+    inside = (j >= w.ks[:, None]) & (j < w.ke[:, None])
+    return np.where(inside, out, -np.inf)
+
+
+def pin_logits_brute_force(orc):
+    import oracle
+
+    for seed, rows, heads, n, win in [(21, 5, 16, 300, "random"), (22, 7, 32, 260, "chunk"),
+                                      (23, 3, 64, 129, "random")]:
+        w = pw.indexer(seed=seed, rows=rows, heads=heads, num_kv=n, window=win)
+        mine, _ = oracle.mqa_logits_full(orc, _logits_case(w))
+        ref = logits_brute_force(w)
+        assert np.array_equal(np.isneginf(mine), np.isneginf(ref)), f"window mask differs ({seed})"
+        fin = np.isfinite(ref)
+        assert_close(mine[fin], ref[fin], rtol=1e-11, atol=1e-9, what=f"logits brute force {seed}")
+
+
+def pin_logits_closed_forms(orc):
+    """One head, weight 1: the logit is max(0, scale * q . k); negative scores
+    contribute nothing (ReLU); the window is half-open [ks, ke)."""
+    import oracle
+
+    dim = 8
+    q = np.zeros((1, 1, dim), dtype=np.uint8)
+    q[0, 0, 3] = 0x40  # e4m3 2.0
+    kv = np.zeros((4, dim), dtype=np.uint8)
+    kv[0, 3] = 0x38   # 1.0   -> 2 * 1 * scale
+    kv[1, 3] = 0xB8   # -1.0  -> relu -> 0
+    kv[2, 3] = 0x44   # 3.0   -> 6 * scale
+    kv[3, 3] = 0x38
+    scale = np.array([0.5, 2.0, 0.25, 1.0], dtype=np.float32)
+    case = oracle.LogitsCase(q, kv, scale, np.ones((1, 1), np.float32), np.array([0], np.int32),
+                             np.array([3], np.int32))
+    out, bound = oracle.mqa_logits_full(orc, case)
+    assert out[0, 0] == 1.0 and out[0, 1] == 0.0 and out[0, 2] == 1.5, out
+    assert np.isneginf(out[0, 3]), "ke is exclusive"
+    assert bound[0, 1] == 4.0 and bound[0, 3] == 0.0, bound
+    # two heads with weights w1, w2: a weighted sum of the per-head ReLUs
+    q2 = np.zeros((1, 2, dim), dtype=np.uint8)
+    q2[0, 0, 3] = 0x40   # 2.0
+    q2[0, 1, 3] = 0xC0   # -2.0
+    case2 = oracle.LogitsCase(q2, kv, np.ones(4, np.float32), np.array([[0.75, -0.5]], np.float32),
+                              np.array([0], np.int32), np.array([4], np.int32))
+    out2, _ = oracle.mqa_logits_full(orc, case2)
+    assert out2[0, 0] == 0.75 * 2.0 and out2[0, 1] == -0.5 * 2.0 and out2[0, 2] == 0.75 * 6.0, out2
+
+
 ALL_PINS = [
     pin_e4m3_all_codes, pin_e4m3_golden, pin_bf16_widen, pin_f16_widen, pin_bf16_round, pin_brute_force,
     pin_one_token, pin_two_tokens, pin_constant_v, pin_window_one_position, pin_causal_prefix,
     pin_relocation, pin_empty, pin_merge_any_split, pin_sparse, pin_per_token_uniform,
-    pin_gqa_heads, pin_poison_unread,
+    pin_gqa_heads, pin_poison_unread, pin_logits_brute_force, pin_logits_closed_forms,
 ]

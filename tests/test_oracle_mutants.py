@@ -41,6 +41,13 @@ MUTANTS = [
     ("no empty-row guard", "if (ntok == 0) {", "if (ntok < 0) {"),
     ("exp sign", "double w = exp(x[j] - m);", "double w = exp(m - x[j]);"),
     ("window ignored", "if (sh->window > 0 && t <= p - sh->window) continue;", ""),
+    ("logits without ReLU", "acc += w * (s > 0.0 ? s : 0.0);", "acc += w * s;"),
+    ("logits window end inclusive", "if (!(j >= ks[r] && j < ke[r])) {", "if (!(j >= ks[r] && j <= ke[r])) {"),
+    ("logits scale dropped", "      s *= sc;\n", "      (void)sc;\n"),
+    ("logits head weight of the wrong head", "double s = 0.0, a = 0.0, w = (double)weights[(size_t)r * heads + h];",
+     "double s = 0.0, a = 0.0, w = (double)weights[(size_t)r * heads + (heads - 1 - h)];"),
+    ("logits kv row off by one", "pa_oracle_e4m3_to_double(kv[(size_t)j * dim + d]);",
+     "pa_oracle_e4m3_to_double(kv[(size_t)(j + 1 < num_kv ? j + 1 : j) * dim + d]);"),
 ]
 
 
