@@ -264,10 +264,13 @@ WORKLOADS = {
              "contexts U[4096, 65536]"),
     "sparse_prefill": ("sparse prefill: one prompt of N rows (--rows, default 1024), 16 query heads, 1 KV head, "
                        "head_dim 128, page 16, row r attends to min(r + 1, 2048) tokens, 4096-page pool"),
+    "indexer": ("indexer logits: a 1024-row prompt chunk against 131072 KV tokens (cached prefix + chunk, row r "
+                "sees [0, 130049 + r)), 64 heads, head_dim 128, FP8 Q and KV with per-token KV scales, "
+                "-inf written outside the windows"),
 }
 
 
-SEQ_LEN = {"dense": "U[1024,8192]", "tiny": "{37,100}", "d256": "{0, 8K+tail, 128K+tail}",
+SEQ_LEN = {"indexer": "131072 KV tokens", "dense": "U[1024,8192]", "tiny": "{37,100}", "d256": "{0, 8K+tail, 128K+tail}",
            "sparse": "2048 of 131072", "mtp4": "U[4096,65536]", "sparse_prefill": "min(r + 1, 2048) of r + 1"}
 MERGES = {"auto": 0, "direct": 1, "cluster": 2, "last-arriver": 3, "reducer": 4}
 CONSUMERS = {"auto": 0, "tile": 1, "tmem": 2}
@@ -288,6 +291,114 @@ def make_workload(args, rank):
     if args.workload == "sparse_prefill":
         return pw.sparse_prefill(kv_dtype=kv, rows=args.rows)
     raise ValueError(args.workload)
+
+
+def run_indexer(args):
+    """The indexer-logits line: FP8 tensor-core throughput (TFLOP/s of the
+    scores inside the windows) with the same timing protocol as the decode."""
+    import torch
+    import torch.distributed as dist
+
+    import paged_attention_decode_attn_gb300 as pa
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    w = pw.indexer(seed=1007 + rank, rows=args.batch or 1024)
+    flops = w.flops()
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    host = {"q": pin(w.q), "kv": pin(w.kv), "sc": pin(w.kv_scale), "w": pin(w.weights), "ks": pin(w.ks),
+            "ke": pin(w.ke)}
+    d = {k: v.to(dev) for k, v in host.items()}
+    stride = (w.num_kv + 3) // 4 * 4
+    logits = torch.empty((w.rows, stride), dtype=torch.float32, device=dev)
+    status = torch.zeros(4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def step(on=None):
+        pa.pa_mqa_logits(logits, d["q"], d["kv"], d["sc"], d["w"], d["ks"], d["ke"], clean_logits=True,
+                         status=status, stream=stream if on is None else on)
+
+    for _ in range(max(3, args.warmup)):
+        flush.sum(dtype=torch.int64)
+        step()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with Clocks(dev.index) as clk:
+        torch.cuda._sleep(int(3e8))
+        for i in range(K):
+            flush.sum(dtype=torch.int64)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    per_call_ms = np.array([s_.elapsed_time(e) for s_, e in zip(starts, ends)])
+    tot_s, tot_flops = aggregate(float(per_call_ms.sum()) / 1000.0, flops * K)
+    st = int(status[0].item())
+    warm_us = None if args.no_warm else warm_us_per_call(step, torch.cuda.Stream(dev))
+    out_host = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = logits.numel() * logits.element_size()
+    e2e_steps = args.e2e_steps
+    for i in range(e2e_steps + 2):
+        if i == 2:
+            torch.cuda.synchronize(dev)
+            if world > 1:
+                dist.barrier()
+            t0 = time.perf_counter()
+        for k_, v_ in host.items():
+            d[k_].copy_(v_, non_blocking=True)
+        step()
+        out_host.copy_(logits, non_blocking=True)
+        torch.cuda.synchronize(dev)
+    e2e_s, e2e_flops = aggregate(time.perf_counter() - t0, flops * e2e_steps)
+    if rank == 0:
+        peaks = {}
+        try:
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+                peaks = json.load(f)
+        except (OSError, ValueError):
+            pass
+        # FP8 dense peak: the measured BF16 burst figure times the nominal FP8/BF16 ratio (2)
+        bf16 = float(peaks.get("bf16_tflops", 0) or 0)
+        peak, kind = (2.0 * bf16, "measured bf16 burst x 2 (nominal fp8/bf16)") if bf16 > 0 else \
+            (2.0 * 1900.0, "fallback bf16 1.9 PFLOP/s x 2")
+        per_us = float(np.mean(per_call_ms)) * 1000.0
+        achieved = flops / (per_us * 1e-6) / 1e12
+        line = {
+            "metric": "TFLOP/s of FP8 indexer logits (scores inside the windows, 2 FLOPs per multiply-add)",
+            "value": tot_flops / tot_s / 1e12, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": float(np.mean(per_call_ms)), "us_per_call": per_us,
+            "us_per_call_median": float(np.median(per_call_ms)) * 1000.0, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 (Q, KV), f32 accumulate and logits",
+            "data": "synthetic (seeded pa_workloads.indexer)",
+            "config": {"workload": WORKLOADS["indexer"], "global_batch": w.rows * world, "seq_len": SEQ_LEN["indexer"],
+                       "heads": w.heads, "parallelism": "replicas" if world > 1 else "single GPU",
+                       "l2": "512 MiB read-only pass before every timed call"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "peak_kind": kind, "traffic": None,
+                         "flops_per_launch": flops, "kernel": "pa_logits_kernel"},
+            "e2e": {"value": e2e_flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h), "steps": e2e_steps},
+            "gpu_launches": K, "clocks": clk.summary(), "device_status": st,
+        }
+        if warm_us is not None:
+            line["us_per_call_warm"] = warm_us
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
 
 
 def run_reference(args):
@@ -377,6 +488,8 @@ def main():
     args.warmup_ref = 1 if args.warmup > 0 else 0
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "indexer":
+        return run_indexer(args)
 
     import torch
     import torch.distributed as dist

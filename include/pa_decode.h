@@ -273,6 +273,35 @@ PA_API pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache
                                    const float* v_scale, int window, const float* sinks, const pa_plan_t* plan,
                                    void* stream);
 
+/* Indexer logits: the scoring step upstream of sparse decode, which ranks KV
+ * tokens for each query row (PR "[FlyDSL] fp8_mqa_logits gfx942: add
+ * LDS-staged variant, use it by default": FP8 Q and KV, a ReLU x weight
+ * epilogue reduced over the heads, per-row KV windows, and -inf written
+ * outside them by the kernel itself when clean_logits is set). For query row
+ * r and KV token j in its window [ks[r], ke[r]) (clipped to [0, num_kv)):
+ *
+ *   logits[r * logits_stride + j] =
+ *       sum_h weights[r * num_heads + h] * max(0, kv_scale[j] * sum_d q[r][h][d] * kv[j][d])
+ *
+ * with q and kv decoded exactly from OCP e4m3fn bytes; every other j in
+ * [0, num_kv) is set to -inf when clean_logits != 0 and left untouched
+ * otherwise. Arguments (device memory, 16-byte aligned, caller-owned):
+ *   logits   float32 [rows, logits_stride] (logits_stride >= num_kv, a multiple of 4)
+ *   q        e4m3 bytes [rows, num_heads, head_dim]
+ *   kv       e4m3 bytes [num_kv, head_dim]
+ *   kv_scale float32 [num_kv], >= 0 (the per-token dequantisation scale)
+ *   weights  float32 [rows, num_heads] (any head weighting, softmax scale included)
+ *   ks, ke   int32 [rows] window bounds
+ *   status   int32 device word or NULL: a bounded wait that ran out sets a bit
+ * num_heads: 16, 32, 64 or 128; head_dim: 128. One kernel launch on `stream`
+ * (tcgen05 FP8 MMAs, FP32 accumulation); nothing is allocated.
+ * Errors: PA_ERR_INVALID_ARG (null or misaligned pointer, bad size),
+ * PA_ERR_UNSUPPORTED (head count or head_dim), PA_ERR_CUDA (launch). */
+PA_API pa_status pa_mqa_logits(float* logits, int logits_stride, const void* q, const void* kv,
+                               const float* kv_scale, const float* weights, const int32_t* ks,
+                               const int32_t* ke, int rows, int num_heads, int head_dim, int num_kv,
+                               int clean_logits, int32_t* status, int device, void* stream);
+
 PA_API const char* pa_strerror(pa_status status);
 
 /* Message of the last failure on this thread ("" if none). */

@@ -25,7 +25,7 @@ __all__ = [
     "PA_SCHED_PER_UNIT", "PA_CONSUMER_AUTO", "PA_CONSUMER_TILE", "PA_CONSUMER_TMEM", "PA_Q_BF16",
     "PA_Q_FP16", "PaError", "PlanDesc", "PlanInfo", "Plan", "library", "library_path",
     "pa_plan_create", "pa_plan_workspace_bytes", "pa_plan_set_workspace", "pa_plan_get_info",
-    "pa_plan_destroy", "pa_decode", "pa_decode_sparse", "pa_decode_noalloc", "pa_strerror",
+    "pa_plan_destroy", "pa_decode", "pa_decode_sparse", "pa_decode_noalloc", "pa_mqa_logits", "pa_strerror",
     "pa_last_error", "EXPORTED_SYMBOLS",
 ]
 
@@ -39,7 +39,7 @@ PA_Q_BF16, PA_Q_FP16 = 0, 1
 
 EXPORTED_SYMBOLS = [
     "pa_plan_create", "pa_plan_workspace_bytes", "pa_plan_set_workspace", "pa_plan_get_info",
-    "pa_plan_destroy", "pa_decode", "pa_decode_sparse", "pa_decode_noalloc", "pa_strerror",
+    "pa_plan_destroy", "pa_decode", "pa_decode_sparse", "pa_decode_noalloc", "pa_mqa_logits", "pa_strerror",
     "pa_last_error",
 ]
 
@@ -104,6 +104,9 @@ def library():
         lib.pa_decode_sparse.restype = st
         lib.pa_decode_noalloc.argtypes = [vp] * 8 + [i, vp, vp, vp]
         lib.pa_decode_noalloc.restype = st
+        # logits, stride, q, kv, kv_scale, weights, ks, ke, rows, heads, dim, num_kv, clean, status, device, stream
+        lib.pa_mqa_logits.argtypes = [vp, i, vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp, i, vp]
+        lib.pa_mqa_logits.restype = st
         lib.pa_strerror.argtypes = [st]
         lib.pa_strerror.restype = ctypes.c_char_p
         lib.pa_last_error.argtypes = []
@@ -196,6 +199,18 @@ def pa_decode_sparse(out, q, k_cache, v_cache, block_table, ctx_lens, topk_idx, 
                                       _ptr(block_table), _ptr(ctx_lens), _ptr(topk_idx),
                                       _ptr(k_scale), _ptr(v_scale), _ptr(sinks), plan,
                                       _stream(stream)))
+
+
+def pa_mqa_logits(logits, q, kv, kv_scale, weights, ks, ke, clean_logits=True, status=None, stream=None):
+    """Indexer logits (FP8 q [rows, heads, 128], FP8 kv [num_kv, 128]) into the
+    float32 logits [rows, >= num_kv] tensor; see include/pa_decode.h."""
+    rows, heads, dim = q.shape
+    num_kv = kv.shape[0]
+    _check(library().pa_mqa_logits(_ptr(logits), int(logits.stride(0)), _ptr(q), _ptr(kv), _ptr(kv_scale),
+                                   _ptr(weights), _ptr(ks), _ptr(ke), int(rows), int(heads), int(dim), int(num_kv),
+                                   int(bool(clean_logits)), _ptr(status), int(logits.device.index or 0),
+                                   _stream(stream)))
+    return logits
 
 
 class Plan:
