@@ -70,6 +70,7 @@ KERNEL_SOURCES = {
                 "pa_tile_bf16_q16.cu"),
     "pa_mtp": ("pa_tile.cuh", "pa_tc.cuh", "pa_mtp.cuh", "pa_mtp_fp8.cu", "pa_mtp_bf16.cu"),
     "pa_reduce": ("pa_tile.cuh", "pa_reduce.cu"),
+    "pa_logits": ("pa_tile.cuh", "pa_tc.cuh", "pa_logits.cu"),
 }
 SHARED_SOURCES = ("pa_internal.h", "pa_host.cu")
 
@@ -387,7 +388,8 @@ def run_indexer(args):
                        "heads": w.heads, "parallelism": "replicas" if world > 1 else "single GPU",
                        "l2": "512 MiB read-only pass before every timed call"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "peak_kind": kind, "traffic": None,
+                         "frac": achieved / peak, "peak_kind": kind,
+                         "traffic": profiled_traffic(None if args.batch else "pa_logits_indexer", "pa_logits"),
                          "flops_per_launch": flops, "kernel": "pa_logits_kernel"},
             "e2e": {"value": e2e_flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "steps": e2e_steps},
