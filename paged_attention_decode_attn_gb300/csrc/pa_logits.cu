@@ -76,16 +76,34 @@ __device__ __forceinline__ void lg_tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) 
         "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
       : "r"(taddr));
 }
-// acc += sum over n of w[n] * max(0, s[n]) (s: tensor-memory words)
+// Two FP32 lanes in one 64-bit register, and their packed FMA (fma.rn.f32x2):
+// one instruction for two products.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ float f32x2_sum(uint64_t a) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
+  return lo + hi;
+}
+// acc += sum over n of w[n] * max(0, s[n]) (s: tensor-memory words), even
+// and odd n in the two lanes of acc
 template <int NV>
-__device__ __forceinline__ float lg_relu_dot(const uint32_t (&v)[NV], const float* w, float acc) {
+__device__ __forceinline__ uint64_t lg_relu_dot(const uint32_t (&v)[NV], const float* w, uint64_t acc) {
 #pragma unroll
   for (int x = 0; x < NV; x += 4) {
     const float4 w4 = *reinterpret_cast<const float4*>(w + x);
-    acc = fmaf(w4.x, fmaxf(__uint_as_float(v[x]), 0.f), acc);
-    acc = fmaf(w4.y, fmaxf(__uint_as_float(v[x + 1]), 0.f), acc);
-    acc = fmaf(w4.z, fmaxf(__uint_as_float(v[x + 2]), 0.f), acc);
-    acc = fmaf(w4.w, fmaxf(__uint_as_float(v[x + 3]), 0.f), acc);
+    acc = fma_f32x2(f32x2(w4.x, w4.y),
+                    f32x2(fmaxf(__uint_as_float(v[x]), 0.f), fmaxf(__uint_as_float(v[x + 1]), 0.f)), acc);
+    acc = fma_f32x2(f32x2(w4.z, w4.w),
+                    f32x2(fmaxf(__uint_as_float(v[x + 2]), 0.f), fmaxf(__uint_as_float(v[x + 3]), 0.f)), acc);
   }
   return acc;
 }
@@ -276,14 +294,14 @@ __global__ void __launch_bounds__(lg_threads(H), 1)
       float acc[RPW];
 #pragma unroll
       for (int i = 0; i < RPW; ++i) {
-        acc[i] = 0.f;
+        uint64_t a2 = f32x2(0.f, 0.f);
         const int col0 = b * kLgN + (half * RPW + i) * H;
         const float* w = wsm + (half * RPW + i) * H;
         if constexpr (H == 16) {
           uint32_t v[16];
           lg_tmem_ld16(tmem + lane_addr + (uint32_t)col0, v);
           tmem_wait_ld();
-          acc[i] = lg_relu_dot<16>(v, w, acc[i]);
+          a2 = lg_relu_dot<16>(v, w, a2);
         } else {
           // 64 columns (two loads) per wait
 #pragma unroll
@@ -292,10 +310,11 @@ __global__ void __launch_bounds__(lg_threads(H), 1)
             tmem_ld32(tmem + lane_addr + (uint32_t)(col0 + h0), va);
             if (h0 + 32 < H) tmem_ld32(tmem + lane_addr + (uint32_t)(col0 + h0 + 32), vb);
             tmem_wait_ld();
-            acc[i] = lg_relu_dot<32>(va, w + h0, acc[i]);
-            if (h0 + 32 < H) acc[i] = lg_relu_dot<32>(vb, w + h0 + 32, acc[i]);
+            a2 = lg_relu_dot<32>(va, w + h0, a2);
+            if (h0 + 32 < H) a2 = lg_relu_dot<32>(vb, w + h0 + 32, a2);
           }
         }
+        acc[i] = f32x2_sum(a2);
       }
       // S buffer b is read: the MMA of tile k + 2 may overwrite it
       tc_fence_before();
