@@ -83,8 +83,9 @@ const void* tile_kernel_bf16(int d, int wide, int q_f16);
 const void* tile_kernel_bf16_q16(int d, int wide);
 const void* reduce_kernel(int d);
 // Tensor-memory consumer instantiations (FP8 head_dim 128/256, BF16 head_dim
-// 128; rh = query rows per softmax warpgroup, 16 or 32).
-const void* mtp_kernel(int fp8, int d, int vtok, int rh);
+// 128; rh = query rows per softmax warpgroup, 16 or 32; nwg = softmax
+// warpgroups, 2 or 4).
+const void* mtp_kernel(int fp8, int d, int vtok, int rh, int nwg);
 
 }  // namespace pa
 

@@ -1,12 +1,15 @@
 // Pipelined tensor-memory (tcgen05) consumer for query-row groups of 17..64
 // rows per KV head (MTP verify rows x GQA), dense paged decode on sm_103a.
 //
-// Warp roles (320 threads, one CTA per SM):
-//  * warps 0-7: two softmax warpgroups. TMEM lane quarter q = warp % 4 holds
-//    stage tokens 32q..32q+31, so thread (warp, lane) owns token 32q + lane;
-//    warpgroup w = warp / 4 owns query rows [w*RH, (w+1)*RH);
-//  * warp 8: the producer of the tile kernel (page ids, TMA ring, Q ring);
-//  * warp 9: one thread issues every tcgen05.mma and commit.
+// Warp roles (one CTA per SM; NWG = 2 or 4 softmax warpgroups):
+//  * warps 0 .. 4 NWG - 1: the softmax warpgroups. TMEM lane quarter
+//    q = warp % 4 holds stage tokens 32q..32q+31, so thread (warp, lane) owns
+//    token 32q + lane; warpgroup w = warp / 4 owns query rows [w*RH, (w+1)*RH);
+//  * warp 4 NWG: the producer of the tile kernel (page ids, TMA ring, Q ring);
+//  * warp 4 NWG + 1: one thread issues every tcgen05.mma and commit.
+// Four warpgroups of 16 rows put four softmax warps on each SM sub-partition
+// (better latency hiding than two warpgroups of 32 rows) at 96 registers a
+// thread.
 //
 // Per stage k (128 tokens), accumulators in tensor memory:
 //   S^T[128 tok x RN]  = K . Q^T          (double-buffered: S(k+1) runs while
@@ -49,12 +52,8 @@ namespace pa {
 namespace dev {
 
 constexpr int kMtpTT = 128;            // tokens per stage (M of S^T)
-constexpr int kMtpSoftThreads = 256;   // softmax warps 0-7
-constexpr int kMtpThreads = 320;       // + producer warp 8 + MMA warp 9
-constexpr int kMtpProducerWarp = 8;
-constexpr int kMtpMmaWarp = 9;
-constexpr int kBarStage = 2;           // named barrier of the 256 softmax threads (1 = merges)
-constexpr int kBarWg0 = 3;             // 3, 4: named barriers of one softmax warpgroup (128 threads)
+constexpr int kBarStage = 2;           // named barrier of all softmax threads (1 = merges)
+constexpr int kBarWg0 = 3;             // 3, 4, ...: named barriers of one softmax warpgroup (128 threads)
 constexpr float kVtokUnit = 0.0625f;   // per-token V scales enter FP16 V as vs * 2^-4
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
@@ -168,10 +167,17 @@ struct MtpBars {
   __device__ __forceinline__ uint32_t drained() const { return base + 80u; }  // every MMA complete
 };
 
-template <bool FP8, int D, bool VTOK, int RH>
+// NWG softmax warpgroups (warps 0 .. 4 NWG - 1) of RH rows each, then the
+// producer warp and the MMA warp.
+template <bool FP8, int D, bool VTOK, int RH, int NWG>
 struct MtpCfg {
   static constexpr int TT = kMtpTT;
-  static constexpr int RN = 2 * RH;              // rows of the MMA block (N of S^T and O^T)
+  static constexpr int RN = NWG * RH;            // rows of the MMA block (N of S^T and O^T)
+  static constexpr int kSoftWarps = 4 * NWG;
+  static constexpr int kSoft = 32 * kSoftWarps;  // softmax threads
+  static constexpr int kThreads = kSoft + 64;
+  static constexpr int kProducerWarp = kSoftWarps;
+  static constexpr int kMmaWarp = kSoftWarps + 1;
   static constexpr int ELT = FP8 ? 1 : 2;
   static constexpr int NCH = D * ELT / 128;      // 128-byte chunks per token row of a stage
   static constexpr int DCH = D / 128;            // O^T blocks of 128 dims
@@ -203,9 +209,9 @@ struct MtpCfg {
 //   p.off_p16  P^T: NP slots of [128 tokens][128 B] (rows of warpgroup w at
 //              bytes [w*RH*2, (w+1)*RH*2)), then the ones operand (2 KiB)
 //   p.off_rows row state: c[64], m[64], pos[64], alpha[64], red[4][64]
-template <bool FP8, int D, bool VTOK, int RH>
+template <bool FP8, int D, bool VTOK, int RH, int NWG>
 struct MtpSoftmax {
-  using C = MtpCfg<FP8, D, VTOK, RH>;
+  using C = MtpCfg<FP8, D, VTOK, RH, NWG>;
   static constexpr int TT = C::TT;
   static constexpr int RN = C::RN;
 
@@ -281,7 +287,7 @@ struct MtpSoftmax {
   __device__ __forceinline__ bool begin_segment(int L, bool has_tokens) {
     // every softmax thread is done with the previous segment's row state
     // (its epilogue reads row_m) before it is reset here
-    named_bar(kBarStage, kMtpSoftThreads);
+    named_bar(kBarStage, C::kSoft);
     const int qs = nq % p.NQ;
     bool got = mbar_wait(sm.qfull(qs, p), (nq / p.NQ) & 1);
     got = __all_sync(0xffffffffu, got);
@@ -291,7 +297,7 @@ struct MtpSoftmax {
     }
     ++nq;
     Lseg = L;
-    constexpr int TPR = kMtpSoftThreads / RN;  // threads per row
+    constexpr int TPR = C::kSoft / RN;  // threads per row
     constexpr int EPT = D / TPR;               // elements per thread
     static_assert(EPT % 16 == 0, "Q split granularity");
     const int tid = threadIdx.x;
@@ -368,7 +374,7 @@ struct MtpSoftmax {
       row_pos()[r] = valid ? L - p.QL + r / p.G : 0;
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    named_bar(kBarStage, kMtpSoftThreads);
+    named_bar(kBarStage, C::kSoft);
     __syncwarp();
     if (lane == 0) {
       if (has_tokens) mbar_arrive(bars.q_ready());
@@ -493,9 +499,9 @@ struct MtpSoftmax {
   // This thread's FP8 V units (16 bytes each) of the stage: unit j is e =
   // threadIdx.x + 256 j, token e / (8 NCH), 128-byte chunk (e / 8) % NCH,
   // 16-byte column e % 8.
-  static constexpr int kVUnits = TT * C::NCH * 8 / kMtpSoftThreads;
+  static constexpr int kVUnits = TT * C::NCH * 8 / C::kSoft;
   __device__ __forceinline__ uint4 load_v_unit(uint32_t vst, int j) const {
-    const int e = threadIdx.x + j * kMtpSoftThreads;
+    const int e = threadIdx.x + j * C::kSoft;
     const int t = e / (8 * C::NCH), cb = (e / 8) % C::NCH, cc = e % 8;
     return lds128(vst + (uint32_t)(cb * TT + t) * 128u + (uint32_t)((cc ^ (t & 7)) << 4));
   }
@@ -505,7 +511,7 @@ struct MtpSoftmax {
   // folded in.
   __device__ __forceinline__ void store_v16_unit(uint32_t kst, uint32_t sst, const StageView& h, int j,
                                                  uint4 w) const {
-    const int e = threadIdx.x + j * kMtpSoftThreads;
+    const int e = threadIdx.x + j * C::kSoft;
     const int t = e / (8 * C::NCH), cb = (e / 8) % C::NCH, cc = e % 8;
     const bool in = h.tbase + t >= h.t0 && h.tbase + t < h.t1;
     const int dim0 = cb * 128 + 16 * cc;
@@ -708,10 +714,10 @@ struct MtpSoftmax {
         }
       }
     }
-    named_bar(kBarStage, kMtpSoftThreads);
+    named_bar(kBarStage, C::kSoft);
     {
       const int E = p.R * (D / 4);  // float4 pieces of the R rows
-      for (int e = threadIdx.x; e < E; e += kMtpSoftThreads) {
+      for (int e = threadIdx.x; e < E; e += C::kSoft) {
         const int r = e / (D / 4), d = (e % (D / 4)) * 4;
         const float4 o = lds128f(stg + 4u * (uint32_t)(r * D + d));
         if (whole) {
@@ -734,10 +740,10 @@ struct MtpSoftmax {
       if (threadIdx.x == 0 && slot == md.s0) p.unit_desc[h.unit] = make_int4(md.nseg, md.s0, md.sbase, md.sstride);
     } else if (p.merge == kMergeLastArriver) {
       __threadfence();
-      named_bar(1, kMtpSoftThreads);
+      named_bar(1, C::kSoft);
       if (threadIdx.x == 0) la_arrive(p, sm, h.b, h.g, h.unit, md);
-      named_bar(1, kMtpSoftThreads);
-      la_run_queue<D>(p, sm, per_tensor_vscale(p), kMtpSoftThreads);
+      named_bar(1, C::kSoft);
+      la_run_queue<D>(p, sm, per_tensor_vscale(p), C::kSoft);
     }
   }
 
@@ -785,10 +791,10 @@ struct MtpSoftmax {
   }
 };
 
-// The MMA-issuing thread (lane 0 of warp 9).
-template <bool FP8, int D, bool VTOK, int RH>
+// The MMA-issuing thread (lane 0 of the warp after the producer).
+template <bool FP8, int D, bool VTOK, int RH, int NWG>
 struct MtpIssuer {
-  using C = MtpCfg<FP8, D, VTOK, RH>;
+  using C = MtpCfg<FP8, D, VTOK, RH, NWG>;
   static constexpr int TT = C::TT;
   static constexpr int RN = C::RN;
   const PaParams& p;
@@ -986,12 +992,12 @@ struct MtpIssuer {
   }
 };
 
-// Softmax warps 0-7, producer warp 8, MMA warp 9.
-template <bool FP8, int D, bool VTOK, int RH>
-__global__ void __launch_bounds__(kMtpThreads, 1) pa_mtp_kernel(const __grid_constant__ PaParams p,
-                                                                const __grid_constant__ CUtensorMap tmK,
-                                                                const __grid_constant__ CUtensorMap tmV) {
-  using Cfg = MtpCfg<FP8, D, VTOK, RH>;
+// Softmax warps 0 .. 4 NWG - 1, then the producer warp and the MMA warp.
+template <bool FP8, int D, bool VTOK, int RH, int NWG>
+__global__ void __launch_bounds__(MtpCfg<FP8, D, VTOK, RH, NWG>::kThreads, 1)
+    pa_mtp_kernel(const __grid_constant__ PaParams p, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV) {
+  using Cfg = MtpCfg<FP8, D, VTOK, RH, NWG>;
   extern __shared__ uint8_t smem_raw[];
   Smem sm;
   {
@@ -1006,19 +1012,19 @@ __global__ void __launch_bounds__(kMtpThreads, 1) pa_mtp_kernel(const __grid_con
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
       mbar_init(sm.full(s, p), 1);
-      mbar_init(sm.empty(s, p), 9);  // eight softmax warps + the MMA commit (or the MMA thread)
+      mbar_init(sm.empty(s, p), Cfg::kSoftWarps + 1);  // softmax warps + the MMA commit (or the MMA thread)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(sm.qfull(i, p), 1);
-      mbar_init(sm.qempty(i, p), 8);
+      mbar_init(sm.qempty(i, p), Cfg::kSoftWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar0 + 8u * i, 1);          // s_full: MMA commit
-      mbar_init(bar0 + 16u + 8u * i, 8);    // s_free: softmax warps
-      mbar_init(bar0 + 32u + 8u * i, 8);    // p_full: softmax warps
+      mbar_init(bar0 + 16u + 8u * i, Cfg::kSoftWarps);  // s_free: softmax warps
+      mbar_init(bar0 + 32u + 8u * i, Cfg::kSoftWarps);  // p_full: softmax warps
     }
     for (int i = 0; i < 3; ++i) mbar_init(bar0 + 48u + 8u * i, 1);  // pv_done: MMA commit
-    mbar_init(bar0 + 72u, 8);  // q_ready
+    mbar_init(bar0 + 72u, Cfg::kSoftWarps);  // q_ready
     mbar_init(bar0 + 80u, 1);  // drained
     for (int i = 0; i < 16; ++i) sm.misc(p)[i] = 0;
     fence_barrier_init();
@@ -1027,7 +1033,7 @@ __global__ void __launch_bounds__(kMtpThreads, 1) pa_mtp_kernel(const __grid_con
   {
     const uint32_t one2 = FP8 ? 0x3C003C00u : 0x3F803F80u;
     const uint32_t ones = sm.base_u32 + p.off_p16 + (uint32_t)Cfg::NP * kMtpTT * 128u;
-    for (uint32_t o = threadIdx.x * 16u; o < 2048u; o += kMtpThreads * 16u) sts128(ones + o, make_uint4(one2, one2, one2, one2));
+    for (uint32_t o = threadIdx.x * 16u; o < 2048u; o += Cfg::kThreads * 16u) sts128(ones + o, make_uint4(one2, one2, one2, one2));
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sm.base_u32 + p.off_tslot),
@@ -1042,16 +1048,16 @@ __global__ void __launch_bounds__(kMtpThreads, 1) pa_mtp_kernel(const __grid_con
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm.base + p.off_tslot);
   constexpr int ELT = FP8 ? 1 : 2;
   constexpr int NCH = D * ELT / 128;
-  if (warp == kMtpProducerWarp) {
+  if (warp == Cfg::kProducerWarp) {
     Producer<ELT, NCH> prod(p, &tmK, &tmV, sm);
     prod.run();
     if (p.merge == kMergeCluster) {
       cluster_sync_all();
       cluster_sync_all();
     }
-  } else if (warp == kMtpMmaWarp) {
+  } else if (warp == Cfg::kMmaWarp) {
     if ((threadIdx.x & 31) == 0) {
-      MtpIssuer<FP8, D, VTOK, RH> mma(p, sm, tmem);
+      MtpIssuer<FP8, D, VTOK, RH, NWG> mma(p, sm, tmem);
       mma.run();
     }
     __syncwarp();
@@ -1060,11 +1066,11 @@ __global__ void __launch_bounds__(kMtpThreads, 1) pa_mtp_kernel(const __grid_con
       cluster_sync_all();
     }
   } else {
-    MtpSoftmax<FP8, D, VTOK, RH> cons(p, sm, tmem);
+    MtpSoftmax<FP8, D, VTOK, RH, NWG> cons(p, sm, tmem);
     cons.run();
     if (p.merge == kMergeCluster) {
       cluster_sync_all();
-      cluster_merge_unit<D>(p, sm, per_tensor_vscale(p), blockIdx.x / p.P, threadIdx.x, kMtpSoftThreads);
+      cluster_merge_unit<D>(p, sm, per_tensor_vscale(p), blockIdx.x / p.P, threadIdx.x, Cfg::kSoft);
       cluster_sync_all();
     }
   }

@@ -36,8 +36,10 @@ def kernel_shape(d):
         d["kv_dtype"] == 1 and d.get("q_dtype", 0) == 1)
     consumer = d.get("consumer", 0)
     if supported and consumer in (0, 2):
-        rh = 16 if R <= 32 else 32
-        k.update(umma=True, rh=rh, nt=2, rw=rh, wr=2, wt=4, ncw=8, rpad=-(-R // 8) * 8, tt=128,
+        four = R > 32 and 0 < d.get("max_context_len", 0) <= 16384
+        rh = 16 if (R <= 32 or four) else 32
+        nwg = 4 if four else 2
+        k.update(umma=True, rh=rh, nwg=nwg, nt=2, rw=rh, wr=nwg, wt=4, ncw=8, rpad=-(-R // 8) * 8, tt=128,
                  bh=min(d["page_size"], 128))
     return k
 
@@ -46,7 +48,7 @@ def smem_total(d, k, ns, cluster, nq):
     stage = 2 * k["tt"] * k["rb"] + (1024 if d["scale_mode"] == 2 else 0)
     off = ns * stage
     if k["umma"]:
-        rn = 2 * k["rh"]
+        rn = k["nwg"] * k["rh"]
         off += (3 if d["kv_dtype"] == 0 else 2) * d["head_dim"] * rn  # Q operand
         off = align(off, 1024)
         off += (3 if d["kv_dtype"] == 0 else 2) * k["tt"] * 128 + 2048  # P^T slots, the ones operand
@@ -124,7 +126,7 @@ def plan(d):
     off += 256
     return dict(merge_mode=merge, schedule=sched, num_partitions=P if sched == 2 else 0,
                 stage_tokens=k["tt"], num_stages=ns, rows=k["R"], rows_per_warp=k["rw"],
-                row_warps=k["wr"], token_warps=k["wt"], block_threads=320 if k["umma"] else (k["ncw"] + 1) * 32,
+                row_warps=k["wr"], token_warps=k["wt"], block_threads=32 * (4 * k["nwg"] + 2) if k["umma"] else (k["ncw"] + 1) * 32,
                 grid=grid, cluster=P if cluster else 1, ctas_per_sm=cps, sm_count=sm,
                 launches_per_call=2 if merge == 4 else 1, units=units, consumer=2 if k["umma"] else 1,
                 smem_bytes=smem,
