@@ -175,7 +175,7 @@ pa::SmemLayout smem_layout(const pa_plan_desc& d, const KernelShape& k, int ns, 
   off += (size_t)ns * 128;
   L.off_bar = (int)off;
   off += (size_t)ns * 16 + 32;  // full/empty per stage, then full/empty per Q slot
-  L.off_ubar = (int)off;  // tensor-memory consumer: its eleven pipeline barriers
+  L.off_ubar = (int)off;  // tensor-memory consumer: its fourteen pipeline barriers
   off += k.umma ? 128 : 16;
   L.off_tslot = (int)off;  // tensor-memory address written by tcgen05.alloc
   off += 16;

@@ -156,15 +156,17 @@ struct Max3Tree<1> {
 // Pipeline barriers of the consumer (eight bytes each, from p.off_ubar).
 struct MtpBars {
   uint32_t base;
-  __device__ __forceinline__ uint32_t s_full(int i) const { return base + 8u * i; }   // S(k) in TMEM
-  __device__ __forceinline__ uint32_t s_free(int i) const { return base + 16u + 8u * i; }  // S(k) read
-  __device__ __forceinline__ uint32_t p_full(int i) const { return base + 32u + 8u * i; }  // P(k), V(k) ready
+  // S(k) in TMEM / S(k) read / P(k) and V(k) ready: one barrier per S^T
+  // buffer, indexed k % SB
+  __device__ __forceinline__ uint32_t s_full(int i) const { return base + 8u * i; }
+  __device__ __forceinline__ uint32_t s_free(int i) const { return base + 24u + 8u * i; }
+  __device__ __forceinline__ uint32_t p_full(int i) const { return base + 48u + 8u * i; }
   // PV(k) complete, three barriers indexed k % 3: between two observations
   // the softmax warps leave up to three PVs unobserved (their P buffers), so
   // no barrier may complete twice in that window
-  __device__ __forceinline__ uint32_t pv_done(int i) const { return base + 48u + 8u * i; }
-  __device__ __forceinline__ uint32_t q_ready() const { return base + 72u; }  // segment's Q operand written
-  __device__ __forceinline__ uint32_t drained() const { return base + 80u; }  // every MMA complete
+  __device__ __forceinline__ uint32_t pv_done(int i) const { return base + 72u + 8u * i; }
+  __device__ __forceinline__ uint32_t q_ready() const { return base + 96u; }  // segment's Q operand written
+  __device__ __forceinline__ uint32_t drained() const { return base + 104u; }  // every MMA complete
 };
 
 // NWG softmax warpgroups (warps 0 .. 4 NWG - 1) of RH rows each, then the
@@ -191,11 +193,14 @@ struct MtpCfg {
   static constexpr int PT = FP8 ? 1 : 2;  // terms
   static constexpr int PB = FP8 ? 3 : 1;  // buffers
   static constexpr int NP = PT * PB;      // slots
+  // S^T buffers: S(k) goes to buffer k % SB, so the MMA thread runs S up to
+  // SB stages ahead of the slowest softmax warpgroup
+  static constexpr int SB = 3;
   // tensor-memory columns
-  static constexpr uint32_t kColS = 0;           // S^T buffers: [0, RN) and [RN, 2 RN)
-  static constexpr uint32_t kColO = 2 * RN;      // O^T: DCH blocks of RN columns
-  static constexpr uint32_t kColL = 2 * RN + DCH * RN;  // L^T (M = 64 layout: lanes 0-15 of each quarter)
-  static constexpr uint32_t kCols = 256;
+  static constexpr uint32_t kColS = 0;                   // S^T buffers: SB blocks of RN columns
+  static constexpr uint32_t kColO = SB * RN;             // O^T: DCH blocks of RN columns
+  static constexpr uint32_t kColL = (SB + DCH) * RN;     // L^T (M = 64 layout: lanes 0-15 of each quarter)
+  static constexpr uint32_t kCols = kColL + RN <= 256 ? 256 : 512;  // a power of two (one CTA per SM)
   static_assert(kColL + RN <= kCols, "tensor memory budget");
   static_assert(!(D == 256 && RN > 32), "head_dim 256 takes at most 32 rows");
   // instruction descriptors (FP8 caches: S e4m3 x e4m3, PV and L FP16; BF16 caches: BF16)
@@ -560,8 +565,8 @@ struct MtpSoftmax {
 
   // One stage with tokens: scores -> P^T (and the FP16 V operand).
   __device__ __forceinline__ bool stage(const StageView& h, int s) {
-    const int buf = k & 1;
-    if (!mbar_wait(bars.s_full(buf), (k >> 1) & 1)) {
+    const int buf = k % C::SB;
+    if (!mbar_wait(bars.s_full(buf), (k / C::SB) & 1)) {
       fail();
       return false;
     }
@@ -581,12 +586,12 @@ struct MtpSoftmax {
     if (named_bar_or(kBarWg0 + wg, 128, mx > 8.f)) {
       if (!raise_max(h, interior, ks, buf, o_valid, y)) return false;
     }
-    // S(k) is read: its buffer may take S(k + 2)
+    // S(k) is read: its buffer may take S(k + SB)
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars.s_free(buf));
     // P^T row of this token (this warpgroup's RH rows), eight rows per 16-byte
-    // store. FP8 caches: FP16 P in buffer k & 1, last read by PV(k - 2). BF16
+    // store. FP8 caches: FP16 P in slot k % 3, last read by PV(k - 3). BF16
     // caches: hi = bf16(p), lo = bf16(p - hi) in the one buffer, last read by
     // PV(k - 1).
     if constexpr (FP8) {
@@ -821,7 +826,7 @@ struct MtpIssuer {
     return false;
   }
 
-  // S^T(k) = K . Q^T into buffer k & 1
+  // S^T(k) = K . Q^T into buffer k % SB
   __device__ __forceinline__ void issue_s(int buf, uint32_t kst) {
     const uint64_t dk = umma_sdesc(kst, 16, 1024);
     const uint32_t d = tmem + C::kColS + (uint32_t)(buf * RN);
@@ -895,7 +900,7 @@ struct MtpIssuer {
   }
 
   // Event loop: S(k) is issued as soon as stage k's bytes, the segment's Q
-  // operand and S buffer k & 1 are ready; PV(j) as soon as P(j) is, in order.
+  // operand and S buffer k % SB are ready; PV(j) as soon as P(j) is, in order.
   // The two streams interleave freely, so a stage is released right after
   // its PV and never waits for the next stage's data.
   __device__ __forceinline__ void run() {
@@ -908,15 +913,21 @@ struct MtpIssuer {
     bool hdr_ok = false, need_q = false;  // stage n's header read (and its Q wait pending)
     int hflags = 0;
     bool htok = false;
-    // pending PVs (at most two: S runs at most two stages ahead of the softmax)
-    int pv_stage0 = 0, pv_stage1 = 0;
-    bool pv_acc0 = false, pv_acc1 = false;
+    // pending PVs in issue order (at most SB: S runs at most SB stages ahead
+    // of the softmax): ring stage and whether O accumulates
+    int pv_st0 = 0, pv_st1 = 0, pv_st2 = 0;
+    bool pv_ac0 = false, pv_ac1 = false, pv_ac2 = false;
+    static_assert(C::SB <= 3, "pending-PV queue depth");
     unsigned long long idle_since = 0;
     while (ok) {
       bool progress = false;
       // PV(kp) as soon as P(kp) is ready
-      if (kp < ks && ready(bars.p_full(kp & 1), (kp >> 1) & 1)) {
-        issue_pv(kp, (kp & 1) ? pv_stage1 : pv_stage0, (kp & 1) ? pv_acc1 : pv_acc0);
+      if (kp < ks && ready(bars.p_full(kp % C::SB), (kp / C::SB) & 1)) {
+        issue_pv(kp, pv_st0, pv_ac0);
+        pv_st0 = pv_st1;
+        pv_ac0 = pv_ac1;
+        pv_st1 = pv_st2;
+        pv_ac1 = pv_ac2;
         ++kp;
         progress = true;
       } else if (!done) {
@@ -943,15 +954,19 @@ struct MtpIssuer {
               hdr_ok = false;
               ++n;
               progress = true;
-            } else if (ks - kp < 2 && (ks < 2 || ready(bars.s_free(ks & 1), ((ks >> 1) - 1) & 1))) {
+            } else if (ks - kp < C::SB && (ks < C::SB || ready(bars.s_free(ks % C::SB), (ks / C::SB - 1) & 1))) {
               tc_fence_after();
-              issue_s(ks & 1, sm.stage(s, p));
-              if (ks & 1) {
-                pv_stage1 = s;
-                pv_acc1 = seg_acc;
+              issue_s(ks % C::SB, sm.stage(s, p));
+              const int q = ks - kp;  // queue position of PV(ks)
+              if (q == 0) {
+                pv_st0 = s;
+                pv_ac0 = seg_acc;
+              } else if (q == 1) {
+                pv_st1 = s;
+                pv_ac1 = seg_acc;
               } else {
-                pv_stage0 = s;
-                pv_acc0 = seg_acc;
+                pv_st2 = s;
+                pv_ac2 = seg_acc;
               }
               seg_acc = true;
               ++ks;
@@ -970,13 +985,13 @@ struct MtpIssuer {
         // come next instead of spinning on the issue slots the softmax warps
         // of this sub-partition need.
         if (kp < ks)
-          (void)wait_hint(bars.p_full(kp & 1), (kp >> 1) & 1);
+          (void)wait_hint(bars.p_full(kp % C::SB), (kp / C::SB) & 1);
         else if (!done && !hdr_ok)
           (void)wait_hint(sm.full(n % p.NS, p), (n / p.NS) & 1);
         else if (!done && need_q)
           (void)wait_hint(bars.q_ready(), qn & 1);
-        else if (!done && ks >= 2)
-          (void)wait_hint(bars.s_free(ks & 1), ((ks >> 1) - 1) & 1);
+        else if (!done && ks >= C::SB)
+          (void)wait_hint(bars.s_free(ks % C::SB), (ks / C::SB - 1) & 1);
         const unsigned long long t = global_timer();
         if (idle_since == 0) {
           idle_since = t;
@@ -1018,14 +1033,14 @@ __global__ void __launch_bounds__(MtpCfg<FP8, D, VTOK, RH, NWG>::kThreads, 1)
       mbar_init(sm.qfull(i, p), 1);
       mbar_init(sm.qempty(i, p), Cfg::kSoftWarps);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar0 + 8u * i, 1);          // s_full: MMA commit
-      mbar_init(bar0 + 16u + 8u * i, Cfg::kSoftWarps);  // s_free: softmax warps
-      mbar_init(bar0 + 32u + 8u * i, Cfg::kSoftWarps);  // p_full: softmax warps
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(bar0 + 8u * i, 1);                      // s_full: MMA commit
+      mbar_init(bar0 + 24u + 8u * i, Cfg::kSoftWarps);  // s_free: softmax warps
+      mbar_init(bar0 + 48u + 8u * i, Cfg::kSoftWarps);  // p_full: softmax warps
+      mbar_init(bar0 + 72u + 8u * i, 1);                // pv_done: MMA commit
     }
-    for (int i = 0; i < 3; ++i) mbar_init(bar0 + 48u + 8u * i, 1);  // pv_done: MMA commit
-    mbar_init(bar0 + 72u, Cfg::kSoftWarps);  // q_ready
-    mbar_init(bar0 + 80u, 1);  // drained
+    mbar_init(bar0 + 96u, Cfg::kSoftWarps);  // q_ready
+    mbar_init(bar0 + 104u, 1);               // drained
     for (int i = 0; i < 16; ++i) sm.misc(p)[i] = 0;
     fence_barrier_init();
   }
