@@ -206,7 +206,7 @@ def aggregate(local_seconds: float, local_bytes: int, group=None):
 def _unit_bytes(w, units):
     """Algorithmic bytes of the sampled (sequence, KV head) units."""
     L = w.ctx_lens.astype(np.int64)
-    per_tok = w.head_dim * w.elt_bytes * 2
+    per_tok = w.row_bytes * 2
     total = 0
     for u in units:
         b = int(u) // w.num_kv_heads

@@ -80,6 +80,10 @@ class Oracle:
         lib.pa_oracle_bf16_to_double.restype = ctypes.c_double
         lib.pa_oracle_f16_to_double.argtypes = [ctypes.c_uint16]
         lib.pa_oracle_f16_to_double.restype = ctypes.c_double
+        lib.pa_oracle_e2m1_to_double.argtypes = [ctypes.c_uint8]
+        lib.pa_oracle_e2m1_to_double.restype = ctypes.c_double
+        lib.pa_oracle_e8m0_to_double.argtypes = [ctypes.c_uint8]
+        lib.pa_oracle_e8m0_to_double.restype = ctypes.c_double
         lib.pa_oracle_round_bf16.argtypes = [ctypes.c_double]
         lib.pa_oracle_round_bf16.restype = ctypes.c_uint16
         lib.pa_oracle_round_bf16_array.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t]
@@ -99,6 +103,12 @@ class Oracle:
     # --- element codecs ---------------------------------------------------
     def e4m3_to_double(self, codes) -> np.ndarray:
         return np.array([self.lib.pa_oracle_e4m3_to_double(int(c)) for c in np.ravel(codes)])
+
+    def e2m1_to_double(self, codes) -> np.ndarray:
+        return np.array([self.lib.pa_oracle_e2m1_to_double(int(c)) for c in np.ravel(codes)])
+
+    def e8m0_to_double(self, codes) -> np.ndarray:
+        return np.array([self.lib.pa_oracle_e8m0_to_double(int(c)) for c in np.ravel(codes)])
 
     def bf16_to_double(self, bits) -> np.ndarray:
         return np.array([self.lib.pa_oracle_bf16_to_double(int(b)) for b in np.ravel(bits)])
@@ -127,8 +137,9 @@ class Oracle:
     @staticmethod
     def _arrays(w):
         c = np.ascontiguousarray
-        ks = c(w.k_scale, dtype=np.float32) if w.k_scale is not None else None
-        vs = c(w.v_scale, dtype=np.float32) if w.v_scale is not None else None
+        sdt = np.uint8 if w.kv_dtype == 2 else np.float32  # MXFP4: E8M0 scale bytes
+        ks = c(w.k_scale, dtype=sdt) if w.k_scale is not None else None
+        vs = c(w.v_scale, dtype=sdt) if w.v_scale is not None else None
         sinks = c(w.sinks, dtype=np.float32) if w.sinks is not None else None
         idx = c(w.topk_idx, dtype=np.int32) if w.topk_idx is not None else None
         return (c(w.q), c(w.k_cache), c(w.v_cache), c(w.block_table, dtype=np.int32),

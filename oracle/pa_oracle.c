@@ -22,7 +22,11 @@
  *     K/V row of token t: page = block_table[b][t / S], slot = t % S,
  *       dequantised exactly (FP8 e4m3fn code times its per-tensor or per-token
  *       scale; BF16 widened), PR "Add paged-attention Tile kernel" (scales are
- *       a scalar or [num_blocks, num_kv_heads, block_size]).
+ *       a scalar or [num_blocks, num_kv_heads, block_size]); MXFP4 (PR "Merge
+ *       gfx1250 PA decode partitions ...", the merge-resolution notes name
+ *       MXFP4 K/V without a layout): the OCP Microscaling (MX) v1.0 format,
+ *       blocks of 32 consecutive head dims of one token row, each an E8M0
+ *       scale times 32 FP4 E2M1 elements (see kv_element for the layout).
  *     x_t = sm_scale * sum_d q[d] * k[d]  (q widened exactly from BF16 or FP16:
  *       PR "Extend packed D256 PA decode pipe ...", Validation, and PR "Merge
  *       gfx1250 PA decode partitions ...", Validation, run BF16 and FP16
@@ -51,9 +55,10 @@
 #define PA_ORACLE_BAD_PAGE 2
 #define PA_ORACLE_NO_MEM 3
 
-enum { ORACLE_KV_FP8 = 0, ORACLE_KV_BF16 = 1 };
+enum { ORACLE_KV_FP8 = 0, ORACLE_KV_BF16 = 1, ORACLE_KV_MXFP4 = 2 };
 enum { ORACLE_Q_BF16 = 0, ORACLE_Q_FP16 = 1 };
-enum { ORACLE_SCALE_NONE = 0, ORACLE_SCALE_PER_TENSOR = 1, ORACLE_SCALE_PER_TOKEN = 2 };
+enum { ORACLE_SCALE_NONE = 0, ORACLE_SCALE_PER_TENSOR = 1, ORACLE_SCALE_PER_TOKEN = 2, ORACLE_SCALE_MX_BLOCK = 3 };
+#define ORACLE_MX_BLOCK 32
 
 typedef struct {
   int batch;
@@ -64,8 +69,8 @@ typedef struct {
   int page_size;
   int max_pages_per_seq;
   int num_pages;
-  int kv_dtype;   /* ORACLE_KV_FP8 or ORACLE_KV_BF16 */
-  int scale_mode; /* ORACLE_SCALE_* (FP8 only) */
+  int kv_dtype;   /* ORACLE_KV_FP8, ORACLE_KV_BF16 or ORACLE_KV_MXFP4 */
+  int scale_mode; /* ORACLE_SCALE_* (FP8: NONE/PER_TENSOR/PER_TOKEN; MXFP4: MX_BLOCK) */
   int causal;
   int window; /* 0 = off */
   int has_sinks;
@@ -87,6 +92,24 @@ double pa_oracle_e4m3_to_double(uint8_t code) {
   else
     mag = ldexp(1.0 + (double)m / 8.0, e - 7);
   return sign ? -mag : mag;
+}
+
+/* OCP MX v1.0 FP4 element, E2M1: sign bit 3, exponent bits 2..1 (bias 1),
+ * mantissa bit 0; normal value (1 + m/2) * 2^(e-1), subnormal (e = 0) m/2.
+ * No infinities or NaNs. */
+double pa_oracle_e2m1_to_double(uint8_t code) {
+  int sign = (code >> 3) & 1;
+  int e = (code >> 1) & 0x3;
+  int m = code & 0x1;
+  double mag = e == 0 ? 0.5 * (double)m : ldexp(1.0 + 0.5 * (double)m, e - 1);
+  return sign ? -mag : mag;
+}
+
+/* OCP MX v1.0 shared scale, E8M0: an unsigned biased exponent, value
+ * 2^(code - 127); 0xFF is NaN. */
+double pa_oracle_e8m0_to_double(uint8_t code) {
+  if (code == 0xFF) return NAN;
+  return ldexp(1.0, (int)code - 127);
 }
 
 /* BF16 is the upper half of an IEEE binary32: widening is exact. */
@@ -144,16 +167,29 @@ uint16_t pa_oracle_round_bf16(double x) {
   return (uint16_t)(w >> 16);
 }
 
-static double kv_element(const pa_oracle_shape* sh, const void* cache, const float* scale,
+/* Element d of the K or V row (page, g, slot). `scale` holds binary32 scales
+ * (FP8: one, or one per token row) or, for MXFP4, the E8M0 bytes.
+ * MXFP4 layout (this library's reading; the pages give none): the row's D
+ * elements are D/2 bytes, element d in the low nibble of byte d/2 when d is
+ * even and in the high nibble when odd; its D/32 scale bytes sit at
+ * scale[row * D/32 + d/32], row = (page * Hkv + g) * page_size + slot. */
+static double kv_element(const pa_oracle_shape* sh, const void* cache, const void* scale,
                          int page, int g, int slot, int d) {
-  size_t idx = (((size_t)page * sh->num_kv_heads + g) * sh->page_size + slot) * sh->head_dim + d;
+  size_t row = ((size_t)page * sh->num_kv_heads + g) * sh->page_size + slot;
+  size_t idx = row * sh->head_dim + d;
   if (sh->kv_dtype == ORACLE_KV_BF16) return pa_oracle_bf16_to_double(((const uint16_t*)cache)[idx]);
+  if (sh->kv_dtype == ORACLE_KV_MXFP4) {
+    uint8_t byte = ((const uint8_t*)cache)[row * (size_t)(sh->head_dim / 2) + (size_t)(d / 2)];
+    uint8_t code = (d & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);
+    uint8_t x = ((const uint8_t*)scale)[row * (size_t)(sh->head_dim / ORACLE_MX_BLOCK) + (size_t)(d / ORACLE_MX_BLOCK)];
+    return pa_oracle_e2m1_to_double(code) * pa_oracle_e8m0_to_double(x);
+  }
   {
     double v = pa_oracle_e4m3_to_double(((const uint8_t*)cache)[idx]);
     if (sh->scale_mode == ORACLE_SCALE_PER_TENSOR)
-      v *= (double)scale[0];
+      v *= (double)((const float*)scale)[0];
     else if (sh->scale_mode == ORACLE_SCALE_PER_TOKEN)
-      v *= (double)scale[((size_t)page * sh->num_kv_heads + g) * sh->page_size + slot];
+      v *= (double)((const float*)scale)[row];
     return v;
   }
 }
@@ -192,8 +228,8 @@ static int visible_tokens(const pa_oracle_shape* sh, const int32_t* ctx_lens, co
 /* Partial (m, l, O[D]) of query row (b, i, h) over an explicit token list,
  * natural-log units. Empty list: m = -inf, l = 0, O = 0. */
 int pa_oracle_row_partial(const pa_oracle_shape* sh, const uint16_t* q, const void* k_cache,
-                          const void* v_cache, const int32_t* block_table, const float* k_scale,
-                          const float* v_scale, int b, int i, int h, const int32_t* tokens,
+                          const void* v_cache, const int32_t* block_table, const void* k_scale,
+                          const void* v_scale, int b, int i, int h, const int32_t* tokens,
                           int ntok, double* m_out, double* l_out, double* o_out) {
   int D = sh->head_dim;
   int G = sh->num_q_heads / sh->num_kv_heads;
@@ -262,6 +298,10 @@ static int check_shape(const pa_oracle_shape* sh) {
   if (sh->topk > 0 && sh->query_len != 1) return PA_ORACLE_BAD_ARG;
   if (sh->window < 0) return PA_ORACLE_BAD_ARG;
   if (sh->q_dtype != ORACLE_Q_BF16 && sh->q_dtype != ORACLE_Q_FP16) return PA_ORACLE_BAD_ARG;
+  if (sh->kv_dtype != ORACLE_KV_FP8 && sh->kv_dtype != ORACLE_KV_BF16 && sh->kv_dtype != ORACLE_KV_MXFP4)
+    return PA_ORACLE_BAD_ARG;
+  if ((sh->kv_dtype == ORACLE_KV_MXFP4) != (sh->scale_mode == ORACLE_SCALE_MX_BLOCK)) return PA_ORACLE_BAD_ARG;
+  if (sh->kv_dtype == ORACLE_KV_MXFP4 && sh->head_dim % ORACLE_MX_BLOCK != 0) return PA_ORACLE_BAD_ARG;
   return PA_ORACLE_OK;
 }
 
@@ -269,7 +309,7 @@ static int check_shape(const pa_oracle_shape* sh) {
  * rows of units whose mask byte is 0 are skipped (left untouched). */
 int pa_oracle_decode(const pa_oracle_shape* sh, const uint16_t* q, const void* k_cache,
                      const void* v_cache, const int32_t* block_table, const int32_t* ctx_lens,
-                     const float* k_scale, const float* v_scale, const float* sinks,
+                     const void* k_scale, const void* v_scale, const float* sinks,
                      const int32_t* topk_idx, const uint8_t* unit_mask, double* out) {
   int rc = check_shape(sh);
   int D, G, maxL = 0;

@@ -28,9 +28,12 @@ Workloads follow the shapes the reference pages measure:
   tokens (same PR, Performance: the sparse prefill rows).
 
 Cache layout is ``[num_pages, num_kv_heads, page_size, head_dim]`` (bytes for
-FP8, BF16 bit patterns for BF16). Every pool page that no sequence uses, every
-slot past a sequence's context in its last page and every block-table entry
-past a sequence's extent is poisoned with NaN codes, so any read of them shows
+FP8, BF16 bit patterns for BF16; MXFP4: ``head_dim / 2`` bytes per row, two
+E2M1 codes per byte, the even element in the low nibble, with E8M0 scale bytes
+``[num_pages, num_kv_heads, page_size, head_dim / 32]``). Every pool page that
+no sequence uses, every slot past a sequence's context in its last page and
+every block-table entry past a sequence's extent is poisoned with NaN codes
+(MXFP4, whose elements have no NaN: NaN scale bytes), so any read of them shows
 up in the output. Per-token scale slots past the context are poisoned too.
 """
 
@@ -44,15 +47,21 @@ import torch
 
 KV_FP8 = 0
 KV_BF16 = 1
+KV_MXFP4 = 2
 SCALE_NONE = 0
 SCALE_PER_TENSOR = 1
 SCALE_PER_TOKEN = 2
+SCALE_MX_BLOCK = 3
+MX_BLOCK = 32
 Q_BF16 = 0
 Q_FP16 = 1
 
 FP8_MAX = 448.0
 FP8_NAN = 0x7F
 BF16_NAN = 0x7FC0
+E8M0_NAN = 0xFF
+# magnitudes of the eight non-negative E2M1 codes, in code order
+E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float32)
 
 
 @dataclasses.dataclass
@@ -71,11 +80,11 @@ class Workload:
     kv_dtype: int
     scale_mode: int
     q: np.ndarray  # uint16 [B*QL, Hq, D] BF16 or FP16 bits (q_dtype)
-    k_cache: np.ndarray  # uint8 [P, Hkv, S, D] codes, or uint16 BF16 bits
+    k_cache: np.ndarray  # uint8 [P, Hkv, S, D] codes (MXFP4: [.., D/2] packed), or uint16 BF16 bits
     v_cache: np.ndarray
     block_table: np.ndarray  # int32 [B, max_pages_per_seq]
     ctx_lens: np.ndarray  # int32 [B]
-    k_scale: Optional[np.ndarray]  # float32 [1] or [P, Hkv, S]
+    k_scale: Optional[np.ndarray]  # float32 [1] or [P, Hkv, S]; MXFP4: uint8 E8M0 [P, Hkv, S, D/32]
     v_scale: Optional[np.ndarray]
     causal: int = 1
     window: int = 0
@@ -90,8 +99,11 @@ class Workload:
         return self.num_q_heads // self.num_kv_heads
 
     @property
-    def elt_bytes(self) -> int:
-        return 1 if self.kv_dtype == KV_FP8 else 2
+    def row_bytes(self) -> int:
+        """Bytes of one K (or V) token row, block scales included."""
+        if self.kv_dtype == KV_MXFP4:
+            return self.head_dim // 2 + self.head_dim // MX_BLOCK
+        return self.head_dim * (1 if self.kv_dtype == KV_FP8 else 2)
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -118,6 +130,33 @@ def fp8_codes(x: np.ndarray) -> np.ndarray:
     t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
     t = t.clamp_(-FP8_MAX, FP8_MAX)
     return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def mxfp4_encode(x: np.ndarray):
+    """Encode float32 rows (last axis a multiple of 32) as MXFP4.
+
+    Per block of 32 values: shared exponent X = floor(log2(amax)) - 2 + 127
+    (the largest E2M1 exponent is 2), clamped to [0, 254] (127 for an all-zero
+    block); elements = the nearest E2M1 value of v / 2^(X - 127), ties to the
+    even code, saturated at +-6. Returns (packed codes [..., D/2] uint8 with the
+    even element in the low nibble, E8M0 scales [..., D/32] uint8).
+    """
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    D = x.shape[-1]
+    blk = x.reshape(x.shape[:-1] + (D // MX_BLOCK, MX_BLOCK))
+    amax = np.abs(blk).max(axis=-1)
+    with np.errstate(divide="ignore"):
+        ex = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2.0, 0.0)
+    X = np.clip(ex + 127.0, 0, 254).astype(np.int32)
+    scaled = blk / np.exp2((X - 127).astype(np.float32))[..., None]
+    mag = np.abs(scaled)
+    dist = np.abs(mag[..., None] - E2M1_GRID)  # [..., 32, 8]
+    dist -= 1e-6 * (np.arange(8) % 2 == 0)  # ties go to the even code
+    code = np.argmin(dist, axis=-1).astype(np.uint8)
+    code |= np.where((scaled < 0) & (code != 0), 8, 0).astype(np.uint8)
+    code = code.reshape(x.shape[:-1] + (D,))
+    packed = (code[..., 0::2] | (code[..., 1::2] << 4)).astype(np.uint8)
+    return packed, X.astype(np.uint8)
 
 
 def _pool_and_table(rng, ctx_lens, page_size, pool_pages, max_pages):
@@ -163,6 +202,14 @@ def _fill_cache(rng, num_pages, hkv, S, D, used_pages, valid_slots, kv_dtype,
     slot_ok = np.arange(S)[None, :] < valid_slots[used_pages][:, None]  # [n_used, S]
     mask4 = np.broadcast_to(slot_ok[:, None, :, None], vals.shape)
     scale = None
+    if kv_dtype == KV_MXFP4:
+        packed, X = mxfp4_encode(vals)
+        cache = np.full((num_pages, hkv, S, D // 2), 0x77, dtype=np.uint8)
+        cache[used_pages] = packed
+        scale = np.full((num_pages, hkv, S, D // MX_BLOCK), E8M0_NAN, dtype=np.uint8)
+        X[~np.broadcast_to(slot_ok[:, None, :, None], X.shape)] = E8M0_NAN
+        scale[used_pages] = X
+        return cache, scale
     if kv_dtype == KV_BF16:
         cache = np.full(shape, BF16_NAN, dtype=np.uint16)
         bits = bf16_bits(vals)
@@ -393,12 +440,12 @@ def algorithmic_bytes(w: Workload, visible_tokens: Optional[np.ndarray] = None) 
     row i of sequence b; the union over rows is what is read once.
     """
     B, QL, hkv, D = w.batch, w.query_len, w.num_kv_heads, w.head_dim
-    elt = w.elt_bytes
+    row = w.row_bytes  # one K or V token row (MXFP4: with its block scales)
     total = 0
     if w.topk:
         L = w.ctx_lens.astype(np.int64)
         n_tok = int(((w.topk_idx >= 0) & (w.topk_idx < L[:, None])).sum())
-        total += n_tok * hkv * D * elt * 2
+        total += n_tok * hkv * row * 2
         if w.scale_mode == SCALE_PER_TOKEN:
             total += n_tok * hkv * 4 * 2
         total += n_tok * 4 * 2  # index + block-table entry per gathered token
@@ -408,7 +455,7 @@ def algorithmic_bytes(w: Workload, visible_tokens: Optional[np.ndarray] = None) 
         if w.window > 0:
             lo = np.maximum(0, L - QL + 1 - w.window)
         n_tok = np.maximum(0, L - lo)
-        total += int(n_tok.sum()) * hkv * D * elt * 2
+        total += int(n_tok.sum()) * hkv * row * 2
         if w.scale_mode == SCALE_PER_TOKEN:
             total += int(n_tok.sum()) * hkv * 4 * 2
         S = w.page_size

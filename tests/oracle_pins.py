@@ -4,7 +4,8 @@ Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError
 when the oracle disagrees with
 
 * a library routine (torch's float8_e4m3fn / bfloat16 casts, scipy's softmax),
-* the published FP8 format (golden spot values),
+* the published FP8 format (golden spot values) and the OCP MX FP4/E8M0
+  tables (golden, every code),
 * an independent brute-force route (NumPy float64 dense attention on
   contiguous dequantised K/V with an explicit mask and a library softmax),
 * closed forms (one and two visible tokens, constant V, a sink with one token),
@@ -32,10 +33,40 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 
 # --- an independent second route ----------------------------------------------
 
+def mx_tables():
+    """(E2M1 value per code [16], E8M0 value per code [256]) from the golden
+    fixture of the OCP MX tables (E8M0 spot values there; the rest from its
+    stated rule 2^(code - 127), NaN at 0xFF)."""
+    e2m1 = np.full(16, np.nan)
+    e8m0 = np.ldexp(1.0, np.arange(256) - 127)
+    e8m0[0xFF] = np.nan
+    spot = {}
+    for line in open(os.path.join(HERE, "golden", "mx_fp4_e2m1_e8m0.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        kind, code, val = line.split()
+        if kind == "e2m1":
+            e2m1[int(code, 16)] = float(val)
+        else:
+            spot[int(code, 16)] = float(val)
+    for c, v in spot.items():
+        assert (np.isnan(v) and np.isnan(e8m0[c])) or e8m0[c] == v, ("E8M0 rule vs fixture", c)
+    assert not np.isnan(e2m1).any()
+    return e2m1, e8m0
+
+
 def dequant(w, which: str) -> np.ndarray:
-    """Dequantise a whole cache with torch's casts (float64 [P, Hkv, S, D])."""
+    """Dequantise a whole cache with torch's casts, or the MX tables for
+    MXFP4 (float64 [P, Hkv, S, D])."""
     cache = w.k_cache if which == "k" else w.v_cache
     scale = w.k_scale if which == "k" else w.v_scale
+    if w.kv_dtype == pw.KV_MXFP4:
+        e2m1, e8m0 = mx_tables()
+        lo = e2m1[cache & 0xF]
+        hi = e2m1[cache >> 4]
+        elems = np.stack([lo, hi], axis=-1).reshape(cache.shape[:-1] + (2 * cache.shape[-1],))
+        return elems * np.repeat(e8m0[scale], pw.MX_BLOCK, axis=-1)
     if w.kv_dtype == pw.KV_BF16:
         t = torch.from_numpy(np.ascontiguousarray(cache).view(np.int16)).view(torch.bfloat16)
         return t.double().numpy()
@@ -138,6 +169,41 @@ def pin_e4m3_golden(orc):
             assert np.isnan(got), code
         else:
             assert got == want and np.signbit(got) == np.signbit(want), (code, got, want)
+
+
+def pin_mx_codes(orc):
+    """Every E2M1 code and the E8M0 spot codes against the OCP MX tables."""
+    e2m1, e8m0 = mx_tables()
+    got = orc.e2m1_to_double(np.arange(16))
+    assert np.array_equal(got, e2m1) and np.array_equal(np.signbit(got), np.signbit(e2m1)), "E2M1 values"
+    got = orc.e8m0_to_double(np.arange(256))
+    assert np.array_equal(np.isnan(got), np.isnan(e8m0)), "E8M0 NaN code"
+    ok = ~np.isnan(e8m0)
+    assert np.array_equal(got[ok], e8m0[ok]), "E8M0 values"
+
+
+def pin_mx_brute_force(orc):
+    """MXFP4 caches: the oracle against dense attention over K/V decoded
+    with the MX tables (nibble order, block index, scale row layout)."""
+    cases = [
+        dict(seed=61, D=64, lens=(5, 23, 40)),
+        dict(seed=62, D=32, QL=3, window=17, lens=(0, 2, 19, 64), group=2),
+        dict(seed=63, D=128, QL=2, sinks=True, hkv=2, group=2, S=64, lens=(1, 70, 130)),
+        dict(seed=64, D=64, q_dtype=pw.Q_FP16, causal=0, QL=2, lens=(9, 33), token_sigma=2.0),
+    ]
+    for c in cases:
+        w = small(kv=pw.KV_MXFP4, scale=pw.SCALE_MX_BLOCK, **c)
+        assert_close(orc.decode(w), brute_force(w), what=f"mx brute force {c}")
+
+
+def pin_mx_constant_v(orc):
+    """MXFP4 V whose every element encodes 0.75 gives 0.75 (and blocks of
+    different scales in one row stay exact: 3 * 2^-2 and 1.5 * 2^-1)."""
+    def vconst(used, vals):
+        return np.full_like(vals, 0.75)
+    w = small(65, kv=pw.KV_MXFP4, scale=pw.SCALE_MX_BLOCK, D=64, QL=2, lens=(3, 40), vfun=vconst)
+    out = orc.decode(w)
+    assert_close(out, np.full_like(out, 0.75), what="mx constant V")
 
 
 def pin_bf16_widen(orc):
@@ -482,4 +548,5 @@ ALL_PINS = [
     pin_one_token, pin_two_tokens, pin_constant_v, pin_window_one_position, pin_causal_prefix,
     pin_relocation, pin_empty, pin_merge_any_split, pin_sparse, pin_per_token_uniform,
     pin_gqa_heads, pin_poison_unread, pin_logits_brute_force, pin_logits_closed_forms,
+    pin_mx_codes, pin_mx_brute_force, pin_mx_constant_v,
 ]

@@ -25,7 +25,7 @@ MUTANTS = [
     ("sink sign", "den = l * a + exp(s - M);", "den = l * a + exp(M - s);"),
     ("e4m3 bias", "ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
     ("e4m3 subnormal", "ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
-    ("per-token scale slot", "* sh->page_size + slot];", "* sh->page_size];"),
+    ("per-token scale slot", "v *= (double)((const float*)scale)[row];", "v *= (double)((const float*)scale)[row - slot];"),
     ("V uses K scale", "kv_element(sh, v_cache, v_scale,", "kv_element(sh, v_cache, k_scale,"),
     ("q operand reversed", "s += q_element(sh, qrow, d) *", "s += q_element(sh, qrow, D - 1 - d) *"),
     ("f16 bias", "ldexp(1024.0 + (double)f, e - 25)", "ldexp(1024.0 + (double)f, e - 24)"),
@@ -46,6 +46,14 @@ MUTANTS = [
     ("logits scale dropped", "      s *= sc;\n", "      (void)sc;\n"),
     ("logits head weight of the wrong head", "double s = 0.0, a = 0.0, w = (double)weights[(size_t)r * heads + h];",
      "double s = 0.0, a = 0.0, w = (double)weights[(size_t)r * heads + (heads - 1 - h)];"),
+    ("mx nibble order", "uint8_t code = (d & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);",
+     "uint8_t code = (d & 1) ? (uint8_t)(byte & 0xF) : (uint8_t)(byte >> 4);"),
+    ("mx block of 16 dims", "(size_t)(d / ORACLE_MX_BLOCK)];", "(size_t)(d / 16) % (size_t)(sh->head_dim / ORACLE_MX_BLOCK)];"),
+    ("mx scale row stride", "uint8_t x = ((const uint8_t*)scale)[row * (size_t)(sh->head_dim / ORACLE_MX_BLOCK)",
+     "uint8_t x = ((const uint8_t*)scale)[(row / 2) * (size_t)(sh->head_dim / ORACLE_MX_BLOCK)"),
+    ("e2m1 exponent bias", "ldexp(1.0 + 0.5 * (double)m, e - 1)", "ldexp(1.0 + 0.5 * (double)m, e - 2)"),
+    ("e2m1 subnormal", "e == 0 ? 0.5 * (double)m", "e == 0 ? 1.0 * (double)m"),
+    ("e8m0 bias", "return ldexp(1.0, (int)code - 127);", "return ldexp(1.0, (int)code - 126);"),
     ("logits kv row off by one", "pa_oracle_e4m3_to_double(kv[(size_t)j * dim + d]);",
      "pa_oracle_e4m3_to_double(kv[(size_t)(j + 1 < num_kv ? j + 1 : j) * dim + d]);"),
 ]
