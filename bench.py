@@ -67,7 +67,7 @@ def measured_peak_gbs():
 # plus the shared header and the host code that sets its launch.
 KERNEL_SOURCES = {
     "pa_tile": ("pa_tile.cuh", "pa_tile_fp8_d128.cu", "pa_tile_fp8_d256.cu", "pa_tile_bf16.cu",
-                "pa_tile_bf16_q16.cu"),
+                "pa_tile_bf16_q16.cu", "pa_tile_fp4.cu"),
     "pa_mtp": ("pa_tile.cuh", "pa_tc.cuh", "pa_mtp.cuh", "pa_mtp_fp8.cu", "pa_mtp_bf16.cu"),
     "pa_reduce": ("pa_tile.cuh", "pa_reduce.cu"),
     "pa_logits": ("pa_tile.cuh", "pa_tc.cuh", "pa_logits.cu"),
@@ -102,6 +102,10 @@ def profile_name(args, kernel: str) -> Optional[str]:
     name = f"{kernel}_{args.workload}"
     if args.kv == "bf16" and args.workload in ("sparse", "mtp4", "sparse_prefill"):
         name += "_bf16"
+    if args.kv == "bf16" and args.workload == "dense":
+        return None
+    if args.kv == "mxfp4":
+        name += "_mxfp4"
     if args.workload == "d256" and args.ql != 1:
         name += f"_ql{args.ql}"
     return name
@@ -277,10 +281,22 @@ MERGES = {"auto": 0, "direct": 1, "cluster": 2, "last-arriver": 3, "reducer": 4}
 CONSUMERS = {"auto": 0, "tile": 1, "tmem": 2}
 
 
+def workload_name(args) -> str:
+    name = WORKLOADS[args.workload]
+    if args.kv == "mxfp4":
+        name = name.replace("dense FP8 paged decode", "dense MXFP4 paged decode") + \
+            ", MXFP4 K/V (E2M1 elements, one E8M0 scale per 32 head dims)"
+    elif args.kv == "bf16" and args.workload in ("dense", "mtp4"):
+        name = name.replace("dense FP8 paged decode", "dense BF16 paged decode") + ", BF16 K/V"
+    return name
+
+
 def make_workload(args, rank):
-    kv = pw.KV_BF16 if args.kv == "bf16" else pw.KV_FP8
+    kv = {"fp8": pw.KV_FP8, "bf16": pw.KV_BF16, "mxfp4": pw.KV_MXFP4}[args.kv]
+    if args.kv == "mxfp4" and args.workload not in ("dense", "mtp4"):
+        raise SystemExit("--kv mxfp4 applies to the dense and mtp4 workloads")
     if args.workload == "dense":
-        return pw.dense(seed=1002 + rank, page_size=args.page, batch=args.batch or 64)
+        return pw.dense(seed=1002 + rank, page_size=args.page, batch=args.batch or 64, kv_dtype=kv)
     if args.workload == "tiny":
         return pw.tiny()
     if args.workload == "d256":
@@ -472,7 +488,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="dense", choices=sorted(WORKLOADS),
                     help="the headline line uses the default dense workload; the others are for profiling")
-    ap.add_argument("--kv", default="fp8", choices=["fp8", "bf16"], help="sparse and mtp4 cache format")
+    ap.add_argument("--kv", default="fp8", choices=["fp8", "bf16", "mxfp4"],
+                    help="cache format (dense: fp8, bf16, mxfp4; mtp4: all three; sparse workloads: fp8, bf16)")
     ap.add_argument("--rows", type=int, default=1024, help="sparse_prefill: prompt rows")
     ap.add_argument("--page", type=int, default=16, help="dense: page size (16 is the workload's)")
     ap.add_argument("--batch", type=int, default=0,
@@ -603,9 +620,10 @@ def main():
             "warmup": args.warmup, "ms_per_step": float(np.mean(per_call_ms)),
             "us_per_call": per_launch_us, "us_per_call_median": float(np.median(per_call_ms)) * 1000.0,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": ("fp8-e4m3" if w.kv_dtype == pw.KV_FP8 else "bf16") + " (KV), bf16 (Q/O), f32 accumulate",
+            "dtype": {pw.KV_FP8: "fp8-e4m3", pw.KV_BF16: "bf16", pw.KV_MXFP4: "mxfp4 (e2m1, e8m0 per 32)"}[w.kv_dtype]
+                     + " (KV), bf16 (Q/O), f32 accumulate",
             "data": f"synthetic (seeded pa_workloads.{args.workload})",
-            "config": {"workload": WORKLOADS[args.workload], "global_batch": w.batch * world,
+            "config": {"workload": workload_name(args), "global_batch": w.batch * world,
                        "seq_len": SEQ_LEN[args.workload], "query_len": w.query_len,
                        "window": int(w.window), "sinks": w.sinks is not None,
                        "parallelism": "replicas" if world > 1 else "single GPU",

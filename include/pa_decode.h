@@ -35,13 +35,17 @@
  *                 (the plan's q_dtype)
  *   k_cache,
  *   v_cache       [num_pages, num_kv_heads, page_size, head_dim]
- *                 FP8 e4m3fn bytes (OCP) or BF16
+ *                 FP8 e4m3fn bytes (OCP) or BF16; MXFP4:
+ *                 [num_pages, num_kv_heads, page_size, head_dim / 2] bytes,
+ *                 two E2M1 codes each (see PA_KV_MXFP4)
  *   block_table   [batch, max_pages_per_seq]  int32 physical page ids; only
  *                 the entries covering [0, L_b) are ever read
  *   ctx_lens      [batch]  int32, 0 <= L_b <= max_pages_per_seq * page_size
  *   k_scale,
  *   v_scale       float32 [1] (per tensor) or [num_pages, num_kv_heads,
- *                 page_size] (per token); NULL when scale_mode is NONE
+ *                 page_size] (per token); NULL when scale_mode is NONE;
+ *                 MXFP4: uint8 E8M0 [num_pages, num_kv_heads, page_size,
+ *                 head_dim / 32] (passed through the float pointer)
  *   sinks         float32 [num_q_heads] (natural-log units, not multiplied
  *                 by sm_scale) or NULL
  *   topk_idx      int32 [batch, sparse_topk] logical token positions;
@@ -86,13 +90,24 @@ typedef enum pa_status {
   PA_ERR_DEVICE_STATUS = 5 /* a kernel reported a timeout in its status word */
 } pa_status;
 
-enum { PA_KV_FP8_E4M3 = 0, PA_KV_BF16 = 1 };
+/* KV cache element types. MXFP4 (PR "Merge gfx1250 PA decode partitions in
+ * the tile kernel and speed up dense decode", merge-resolution notes, names
+ * MXFP4 K/V; the layout is this library's reading of the OCP Microscaling
+ * (MX) v1.0 format): each K/V token row of head_dim (128) values is
+ * head_dim / 2 bytes of FP4 E2M1 codes, element d in the low nibble of byte
+ * d / 2 when d is even and in the high nibble when odd; its head_dim / 32 E8M0
+ * block scales (value 2^(code - 127)) are the bytes
+ * scale[((page * num_kv_heads + kv_head) * page_size + slot) * head_dim / 32 + d / 32],
+ * passed through the k_scale / v_scale arguments. */
+enum { PA_KV_FP8_E4M3 = 0, PA_KV_BF16 = 1, PA_KV_MXFP4 = 2 };
 /* Element type of the queries and of the output (PR "Extend packed D256 PA
  * decode pipe to page16, transposed V and sliding windows", Validation, and PR
  * "Merge gfx1250 PA decode partitions in the tile kernel and speed up dense
  * decode", Validation, run BF16 and FP16 queries). */
 enum { PA_Q_BF16 = 0, PA_Q_FP16 = 1 };
-enum { PA_SCALE_NONE = 0, PA_SCALE_PER_TENSOR = 1, PA_SCALE_PER_TOKEN = 2 };
+/* PA_SCALE_MX_BLOCK: the E8M0 block scales of MXFP4 caches (required by them,
+ * accepted by no other cache type). */
+enum { PA_SCALE_NONE = 0, PA_SCALE_PER_TENSOR = 1, PA_SCALE_PER_TOKEN = 2, PA_SCALE_MX_BLOCK = 3 };
 
 /* How partitions of one (sequence, KV head) are merged. */
 enum {
@@ -124,14 +139,14 @@ typedef struct pa_plan_desc {
   int batch;
   int num_q_heads;
   int num_kv_heads;      /* num_q_heads % num_kv_heads == 0 */
-  int head_dim;          /* 128 or 256; 64 with BF16 caches (PA_ERR_UNSUPPORTED otherwise) */
+  int head_dim;          /* 128 or 256; 64 with BF16 caches; MXFP4: 128 (PA_ERR_UNSUPPORTED otherwise) */
   int query_len;         /* >= 1 (MTP rows); rows = query_len * group <= 64 (32 at head_dim 256) */
   int page_size;         /* 16, 32, 64, 128 or 256 tokens */
   int max_pages_per_seq; /* block-table row stride (int32 elements) */
   int num_pages;         /* pages in the cache pool */
   int max_context_len;   /* host bound used for automatic choices; 0 = unknown */
   int kv_dtype;          /* PA_KV_* */
-  int scale_mode;        /* PA_SCALE_* (FP8 only; BF16 requires NONE) */
+  int scale_mode;        /* PA_SCALE_* (FP8: NONE/PER_TENSOR/PER_TOKEN; BF16: NONE; MXFP4: MX_BLOCK) */
   int causal;            /* causal mask among the query_len new tokens */
   int has_sinks;
   int sparse_topk;       /* 0 = dense decode; > 0 = index-list decode (query_len 1) */

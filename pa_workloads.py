@@ -303,7 +303,7 @@ def dense(seed: int = 1002, batch: int = 64, lo: int = 1024, hi: int = 8192,
     pool = 40000 * 16 // page_size
     return make_dense("dense", batch=batch, hkv=8, group=8, head_dim=128,
                       query_len=1, page_size=page_size, ctx_lens=lens, kv_dtype=kv_dtype,
-                      scale_mode=SCALE_PER_TENSOR, seed=seed,
+                      scale_mode=SCALE_MX_BLOCK if kv_dtype == KV_MXFP4 else SCALE_PER_TENSOR, seed=seed,
                       pool_pages=max(pool, int(((lens + page_size - 1) // page_size).sum()) + 8),
                       max_pages=hi // page_size)
 
@@ -340,7 +340,7 @@ def mtp4(seed: int = 1005, kv_dtype: int = KV_FP8, batch: int = 32,
     lens = mtp4_lengths(seed, batch, lo, hi)
     return make_dense("mtp4", batch=batch, hkv=4, group=16, head_dim=128,
                       query_len=4, page_size=128, ctx_lens=lens, kv_dtype=kv_dtype,
-                      scale_mode=SCALE_PER_TENSOR, seed=seed, causal=1,
+                      scale_mode=SCALE_MX_BLOCK if kv_dtype == KV_MXFP4 else SCALE_PER_TENSOR, seed=seed, causal=1,
                       max_pages=(hi + 127) // 128)
 
 

@@ -19,8 +19,8 @@ from typing import Optional
 
 __all__ = [
     "PA_OK", "PA_ERR_INVALID_ARG", "PA_ERR_UNSUPPORTED", "PA_ERR_WORKSPACE", "PA_ERR_CUDA",
-    "PA_ERR_DEVICE_STATUS", "PA_KV_FP8_E4M3", "PA_KV_BF16", "PA_SCALE_NONE", "PA_SCALE_PER_TENSOR",
-    "PA_SCALE_PER_TOKEN", "PA_MERGE_AUTO", "PA_MERGE_DIRECT", "PA_MERGE_CLUSTER",
+    "PA_ERR_DEVICE_STATUS", "PA_KV_FP8_E4M3", "PA_KV_BF16", "PA_KV_MXFP4", "PA_SCALE_NONE",
+    "PA_SCALE_PER_TENSOR", "PA_SCALE_PER_TOKEN", "PA_SCALE_MX_BLOCK", "PA_MERGE_AUTO", "PA_MERGE_DIRECT", "PA_MERGE_CLUSTER",
     "PA_MERGE_LAST_ARRIVER", "PA_MERGE_REDUCER", "PA_SCHED_AUTO", "PA_SCHED_BALANCED",
     "PA_SCHED_PER_UNIT", "PA_CONSUMER_AUTO", "PA_CONSUMER_TILE", "PA_CONSUMER_TMEM", "PA_Q_BF16",
     "PA_Q_FP16", "PaError", "PlanDesc", "PlanInfo", "Plan", "library", "library_path",
@@ -30,8 +30,8 @@ __all__ = [
 ]
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA, PA_ERR_DEVICE_STATUS = range(6)
-PA_KV_FP8_E4M3, PA_KV_BF16 = 0, 1
-PA_SCALE_NONE, PA_SCALE_PER_TENSOR, PA_SCALE_PER_TOKEN = 0, 1, 2
+PA_KV_FP8_E4M3, PA_KV_BF16, PA_KV_MXFP4 = 0, 1, 2
+PA_SCALE_NONE, PA_SCALE_PER_TENSOR, PA_SCALE_PER_TOKEN, PA_SCALE_MX_BLOCK = 0, 1, 2, 3
 PA_MERGE_AUTO, PA_MERGE_DIRECT, PA_MERGE_CLUSTER, PA_MERGE_LAST_ARRIVER, PA_MERGE_REDUCER = range(5)
 PA_SCHED_AUTO, PA_SCHED_BALANCED, PA_SCHED_PER_UNIT = 0, 1, 2
 PA_CONSUMER_AUTO, PA_CONSUMER_TILE, PA_CONSUMER_TMEM = 0, 1, 2

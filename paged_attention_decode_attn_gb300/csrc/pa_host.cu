@@ -87,6 +87,7 @@ struct KernelShape {
 // length 2; at head_dim 128 the tile consumer stays ahead up to 16 rows).
 bool umma_supported(const pa_plan_desc& d, int R) {
   if (d.sparse_topk > 0 || R <= (d.head_dim == 256 ? 8 : 16)) return false;
+  if (d.kv_dtype == PA_KV_MXFP4) return false;  // MXFP4: the tile consumer only
   // BF16 caches are read in place by BF16 MMAs, whose other operand (Q) must
   // be BF16 too: FP16 queries there take the tile consumer.
   if (d.kv_dtype == PA_KV_BF16 && d.q_dtype == PA_Q_FP16) return false;
@@ -113,15 +114,18 @@ KernelShape kernel_shape(const pa_plan_desc& d) {
   k.wt = k.wr >= 4 ? 1 : 4 / k.wr;
   k.ncw = k.wr * k.wt;
   k.rpad = k.wr * k.rw;
-  k.elt = d.kv_dtype == PA_KV_FP8_E4M3 ? 1 : 2;
-  k.rb = d.head_dim * k.elt;
-  k.nch = k.rb / 128;
+  const bool mx = d.kv_dtype == PA_KV_MXFP4;
+  // MXFP4 runs the FP8 consumer path on 64-byte rows (head_dim 128, two
+  // elements per byte, one column block).
+  k.elt = (d.kv_dtype == PA_KV_FP8_E4M3 || mx) ? 1 : 2;
+  k.rb = mx ? d.head_dim / 2 : d.head_dim * k.elt;
+  k.nch = mx ? 1 : k.rb / 128;
   // 32 KiB of K+V per ring stage; FP8 head_dim 128 steps two 16-token tiles
   // per warp (128-token stages), every other format one tile.
   int tt = 32768 / (2 * k.rb);
   k.tt = tt < 16 ? 16 : (tt > 128 ? 128 : tt);
-  k.tw = (d.kv_dtype == PA_KV_FP8_E4M3 && d.head_dim == 128) ? 2 : 1;
-  k.vtok = d.kv_dtype == PA_KV_FP8_E4M3 && d.scale_mode == PA_SCALE_PER_TOKEN;
+  k.tw = ((d.kv_dtype == PA_KV_FP8_E4M3 || mx) && d.head_dim == 128) ? 2 : 1;
+  k.vtok = (d.kv_dtype == PA_KV_FP8_E4M3 && d.scale_mode == PA_SCALE_PER_TOKEN) || mx;
   k.umma = use_umma(d, R);
   k.rh = 0;
   k.nwg = 0;
@@ -148,7 +152,10 @@ KernelShape kernel_shape(const pa_plan_desc& d) {
 // Shared-memory layout for `ns` ring stages.
 pa::SmemLayout smem_layout(const pa_plan_desc& d, const KernelShape& k, int ns, bool cluster, int nq) {
   pa::SmemLayout L;
-  L.stage_bytes = 2 * k.tt * k.rb + (d.scale_mode == PA_SCALE_PER_TOKEN ? 1024 : 0);
+  // per-token scales (4 bytes a token row: one binary32, or MXFP4's four E8M0
+  // block scales) for K then V
+  const bool tok_scales = d.scale_mode == PA_SCALE_PER_TOKEN || d.scale_mode == PA_SCALE_MX_BLOCK;
+  L.stage_bytes = 2 * k.tt * k.rb + (tok_scales ? 1024 : 0);
   L.off_scale = 2 * k.tt * k.rb;
   L.off_stage = 0;
   size_t off = (size_t)ns * L.stage_bytes;
@@ -198,6 +205,7 @@ pa::SmemLayout smem_layout(const pa_plan_desc& d, const KernelShape& k, int ns, 
 
 const void* pick_tile_kernel(const pa_plan_desc& d, const KernelShape& k) {
   if (k.umma) return pa::mtp_kernel(d.kv_dtype == PA_KV_FP8_E4M3, d.head_dim, k.vtok, k.rh, k.nwg);
+  if (d.kv_dtype == PA_KV_MXFP4) return pa::tile_kernel_fp4_d128(k.ncw > 4);
   if (d.kv_dtype == PA_KV_FP8_E4M3) {
     if (d.head_dim == 128) return pa::tile_kernel_fp8_d128(k.vtok, k.ncw > 4);
     return k.ncw > 4 ? nullptr : pa::tile_kernel_fp8_d256(k.vtok);
@@ -214,6 +222,8 @@ pa_status validate_desc(const pa_plan_desc& d) {
                 d.num_kv_heads);
   if (d.head_dim != 128 && d.head_dim != 256 && !(d.head_dim == 64 && d.kv_dtype == PA_KV_BF16))
     return fail(PA_ERR_UNSUPPORTED, "head_dim %d unsupported (128 or 256; 64 with BF16 caches)", d.head_dim);
+  if (d.kv_dtype == PA_KV_MXFP4 && d.head_dim != 128)
+    return fail(PA_ERR_UNSUPPORTED, "MXFP4 caches support head_dim 128 (got %d)", d.head_dim);
   if (d.query_len < 1) return fail(PA_ERR_INVALID_ARG, "query_len must be >= 1 (got %d)", d.query_len);
   const long long rows = (long long)(d.num_q_heads / d.num_kv_heads) * d.query_len;
   if (rows > pa::kMaxRows)
@@ -228,10 +238,14 @@ pa_status validate_desc(const pa_plan_desc& d) {
     return fail(PA_ERR_UNSUPPORTED, "cache has 2^31 or more token rows per tensor");
   if ((long long)d.max_pages_per_seq * d.page_size >= (1ll << 30))
     return fail(PA_ERR_UNSUPPORTED, "max_pages_per_seq * page_size too large");
-  if (d.kv_dtype != PA_KV_FP8_E4M3 && d.kv_dtype != PA_KV_BF16)
+  if (d.kv_dtype != PA_KV_FP8_E4M3 && d.kv_dtype != PA_KV_BF16 && d.kv_dtype != PA_KV_MXFP4)
     return fail(PA_ERR_INVALID_ARG, "unknown kv_dtype %d", d.kv_dtype);
-  if (d.scale_mode < PA_SCALE_NONE || d.scale_mode > PA_SCALE_PER_TOKEN)
+  if (d.scale_mode < PA_SCALE_NONE || d.scale_mode > PA_SCALE_MX_BLOCK)
     return fail(PA_ERR_INVALID_ARG, "unknown scale_mode %d", d.scale_mode);
+  if ((d.kv_dtype == PA_KV_MXFP4) != (d.scale_mode == PA_SCALE_MX_BLOCK))
+    return fail(PA_ERR_INVALID_ARG, "MXFP4 caches take PA_SCALE_MX_BLOCK, and only they do");
+  if (d.kv_dtype == PA_KV_MXFP4 && d.sparse_topk > 0)
+    return fail(PA_ERR_UNSUPPORTED, "MXFP4 caches support dense decode only");
   if (d.q_dtype != PA_Q_BF16 && d.q_dtype != PA_Q_FP16)
     return fail(PA_ERR_INVALID_ARG, "unknown q_dtype %d", d.q_dtype);
   if (d.kv_dtype == PA_KV_BF16 && d.scale_mode != PA_SCALE_NONE)
@@ -429,7 +443,10 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
   p.causal = d.causal ? 1 : 0;
   p.topk = d.sparse_topk;
   p.has_sinks = d.has_sinks ? 1 : 0;
-  p.scale_mode = d.kv_dtype == PA_KV_FP8_E4M3 ? d.scale_mode : pa::kScaleNone;
+  // MXFP4 block scales travel like per-token scales (four bytes a token row)
+  p.scale_mode = d.kv_dtype == PA_KV_FP8_E4M3 ? d.scale_mode
+                 : d.kv_dtype == PA_KV_MXFP4 ? pa::kScalePerToken
+                                             : pa::kScaleNone;
   p.q_f16 = d.q_dtype == PA_Q_FP16;
   const float sm_scale = d.sm_scale > 0.f ? d.sm_scale : 1.0f / std::sqrt((float)d.head_dim);
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
@@ -502,14 +519,17 @@ pa_status encode_cache_map(const pa_plan* pl, const void* base, CUtensorMap* tm)
   const pa_plan_desc& d = pl->desc;
   auto fn = encode_fn();
   if (!fn) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
-  const int elt = d.kv_dtype == PA_KV_FP8_E4M3 ? 1 : 2;
-  cuuint64_t dims[2] = {(cuuint64_t)d.head_dim, (cuuint64_t)d.num_pages * d.num_kv_heads * d.page_size};
-  cuuint64_t strides[1] = {(cuuint64_t)d.head_dim * elt};
-  cuuint32_t box[2] = {(cuuint32_t)(128 / elt), (cuuint32_t)pl->base.BH};
+  const bool mx = d.kv_dtype == PA_KV_MXFP4;
+  const int elt = d.kv_dtype == PA_KV_FP8_E4M3 || mx ? 1 : 2;
+  // MXFP4: rows of head_dim / 2 bytes (64), one box per page, 64-byte swizzle
+  const cuuint64_t row_elems = mx ? (cuuint64_t)d.head_dim / 2 : (cuuint64_t)d.head_dim;
+  cuuint64_t dims[2] = {row_elems, (cuuint64_t)d.num_pages * d.num_kv_heads * d.page_size};
+  cuuint64_t strides[1] = {row_elems * elt};
+  cuuint32_t box[2] = {mx ? (cuuint32_t)row_elems : (cuuint32_t)(128 / elt), (cuuint32_t)pl->base.BH};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(tm, elt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  mx ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return PA_OK;
@@ -528,6 +548,8 @@ pa_status launch(const pa_plan* pl, void* ws_ptr, void* out, const void* q, cons
     if (ptr && !aligned16(ptr)) return fail(PA_ERR_INVALID_ARG, "tensor pointer %p is not 16-byte aligned", ptr);
   if (d.kv_dtype == PA_KV_FP8_E4M3 && d.scale_mode != PA_SCALE_NONE && (!k_scale || !v_scale))
     return fail(PA_ERR_INVALID_ARG, "FP8 scales are required by the plan's scale_mode");
+  if (d.kv_dtype == PA_KV_MXFP4 && (!k_scale || !v_scale))
+    return fail(PA_ERR_INVALID_ARG, "MXFP4 caches need their block-scale arrays (k_scale, v_scale)");
   if (d.has_sinks && !sinks) return fail(PA_ERR_INVALID_ARG, "the plan has sinks but sinks is null");
   if (window < 0) return fail(PA_ERR_INVALID_ARG, "window must be >= 0");
   if (window > 0 && !d.causal && d.query_len > 1)

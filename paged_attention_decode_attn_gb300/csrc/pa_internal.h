@@ -78,6 +78,7 @@ using KernelFn = void (*)(PaParams, CUtensorMap, CUtensorMap);
 // Tile-kernel instantiations (defined in the pa_tile_*.cu files).
 // Returns null when the combination is not instantiated.
 const void* tile_kernel_fp8_d128(int vtok, int wide);
+const void* tile_kernel_fp4_d128(int wide);
 const void* tile_kernel_fp8_d256(int vtok);
 const void* tile_kernel_bf16(int d, int wide, int q_f16);
 const void* tile_kernel_bf16_q16(int d, int wide);

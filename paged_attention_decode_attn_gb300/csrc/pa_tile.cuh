@@ -158,6 +158,49 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
   return r;
 }
+// Two OCP FP4 E2M1 codes (the low byte of x, first element in the low
+// nibble) as FP16x2, first element in the low half; every E2M1 value is exact
+// in FP16.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t x) {
+  uint32_t r;
+  asm("{\n .reg .b8 b;\n mov.b32 {b, _, _, _}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b;\n}\n" : "=r"(r) : "r"(x));
+  return r;
+}
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// MX block scales of one head_dim-128 token row: four E8M0 bytes (blocks of
+// 32 dims, first block in the low byte). The row is taken in units of its
+// largest scale: 2^(max - 127) as binary32 (NaN for the NaN code 0xFF) ...
+__device__ __forceinline__ int mx_max_code(uint32_t w) {
+  return max(max((int)(w & 0xFFu), (int)((w >> 8) & 0xFFu)), max((int)((w >> 16) & 0xFFu), (int)(w >> 24)));
+}
+__device__ __forceinline__ float e8m0_to_f32(int x) {
+  if (x == 0xFF) return __uint_as_float(0x7FC00000u);
+  return x == 0 ? __uint_as_float(0x00400000u) : __uint_as_float((uint32_t)x << 23);
+}
+// ... and each block's elements are multiplied in FP16 by 2^(code - max) =
+// 2^-d: exact down to 2^-24 (FP16 subnormals), 0 for d > 24 (a block more than
+// 2^24 below the row's largest).
+__device__ __forceinline__ uint32_t f16x2_pow2_neg(int d) {
+  uint32_t h = d <= 14 ? (uint32_t)(15 - d) << 10 : (d <= 24 ? 1u << (24 - d) : 0u);
+  return h | (h << 16);
+}
+__device__ __forceinline__ uint32_t mx_block_factor(uint32_t w, int blk) {
+  return f16x2_pow2_neg(mx_max_code(w) - (int)((w >> (8 * blk)) & 0xFFu));
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -438,7 +481,9 @@ __device__ __forceinline__ float per_tensor_vscale(const PaParams& p) {
 }
 
 // ================================================================ producer
-template <int ELT, int NCH>
+// ROWB: bytes of one stage row per column block (128; 64 for MXFP4 head_dim
+// 128, whose rows the 64-byte swizzle lays out).
+template <int ELT, int NCH, int ROWB = 128>
 struct Producer {
   const PaParams& p;
   const CUtensorMap* tmK;
@@ -530,7 +575,7 @@ struct Producer {
     int phys = 0;
     if (nbox > 0) phys = staged_pages(h.b, h.L, lp0, S < TT ? TT / S : 1);
     const bool ktok = p.scale_mode == kScalePerToken;
-    const uint32_t bytes = (uint32_t)nbox * BH * 128u * NCH * 2u + (ktok ? (uint32_t)nbox * BH * 8u : 0u);
+    const uint32_t bytes = (uint32_t)nbox * BH * (uint32_t)ROWB * NCH * 2u + (ktok ? (uint32_t)nbox * BH * 8u : 0u);
     if (lane == 0) {
       *sm.hdr(s, p) = h;
       if (bytes)
@@ -547,12 +592,12 @@ struct Producer {
       const int y = (phys * p.Hkv + h.g) * S + yoff;
       const int row = row0 + lane * BH;
       const uint32_t kst = sm.stage(s, p);
-      const uint32_t vst = kst + (uint32_t)TT * 128u * NCH;
+      const uint32_t vst = kst + (uint32_t)TT * (uint32_t)ROWB * NCH;
       const uint32_t bar = sm.full(s, p);
 #pragma unroll
       for (int cb = 0; cb < NCH; ++cb) {
-        tma_load_2d(kst + (uint32_t)(cb * TT + row) * 128u, tmK, cb * (128 / ELT), y, bar);
-        tma_load_2d(vst + (uint32_t)(cb * TT + row) * 128u, tmV, cb * (128 / ELT), y, bar);
+        tma_load_2d(kst + (uint32_t)(cb * TT + row) * (uint32_t)ROWB, tmK, cb * (128 / ELT), y, bar);
+        tma_load_2d(vst + (uint32_t)(cb * TT + row) * (uint32_t)ROWB, tmV, cb * (128 / ELT), y, bar);
       }
       if (ktok) {
         const uint32_t sc = kst + p.off_scale;
@@ -644,7 +689,7 @@ struct Producer {
     if (!acquire_stage(s)) return;
     const int TT = p.TT;
     const uint32_t kst = sm.stage(s, p);
-    const uint32_t vst = kst + (uint32_t)TT * 128u * NCH;
+    const uint32_t vst = kst + (uint32_t)TT * (uint32_t)ROWB * NCH;
     const bool empty = !(h.t1 > h.t0);
     int idx[4], phys[4];
 #pragma unroll
@@ -1005,10 +1050,15 @@ struct StageView {
 // BF16 hi + lo (an FP16 value's 11 significant bits leave at most 4 for lo)
 // and S takes one BF16 MMA per term. FP8 caches convert any query type to
 // FP16 operands at the segment start (a runtime flag).
-template <bool FP8, int D, int NT, bool VTOK, int TW, bool QF16 = false>
+// FP4: MXFP4 caches (head_dim 128, with FP8 = VTOK = true: FP16 queries, P and
+// V; the per-token K and V factors come from the block scales).
+template <bool FP8, int D, int NT, bool VTOK, int TW, bool QF16 = false, bool FP4 = false>
 struct Consumer {
+  static_assert(!FP4 || (FP8 && VTOK && D == 128), "MXFP4 runs the FP8 per-token path at head_dim 128");
   static constexpr int ELT = FP8 ? 1 : 2;
-  static constexpr int NCH = D * ELT / 128;  // 128-byte column blocks per token row
+  static constexpr int NCH = FP4 ? 1 : D * ELT / 128;  // column blocks per token row
+  static constexpr uint32_t ROWB = FP4 ? 64u : 128u;   // bytes of a stage row per block
+  static constexpr uint32_t TILEB = 16u * ROWB;        // bytes of a 16-token tile per block
   static constexpr int KSTEPS = D / 16;
   static constexpr int MT = D / 16;
   static constexpr int KS_BLK = KSTEPS / NCH;
@@ -1022,6 +1072,10 @@ struct Consumer {
   int lane, g4, t4, wr, wt;
   uint32_t koff[NCH][2][2];  // [block][token g4 / g4+8][chunk half], tile-relative
   uint32_t voff[NCH][4];     // [block][token 2t4, 2t4+1, 2t4+8, 2t4+9]
+  // MXFP4: K chunk t4 (32 dims = one MX block) of tokens g4 / g4+8; V bytes
+  // [8 g4, 8 g4 + 8) (dims [16 g4, 16 g4 + 16), MX block g4 / 2) of tokens
+  // 2t4, 2t4+1, 2t4+8, 2t4+9 (64-byte rows, 64-byte swizzle)
+  uint32_t koff4[2], voff4[4];
   float kscale = 1.f, vscale = 1.f;
   // per segment
   uint32_t qf[NT][KSTEPS][2];
@@ -1058,6 +1112,18 @@ struct Consumer {
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         voff[cb][k] = (uint32_t)(cb * p.TT + vr[k]) * 128u + (uint32_t)((g4 ^ (vr[k] & 7)) << 4);
+    }
+    // 64-byte swizzle: row r's 16-byte chunk c sits at chunk c ^ ((r >> 1) & 3)
+#pragma unroll
+    for (int ab = 0; ab < 2; ++ab) {
+      const int row = g4 + 8 * ab;
+      koff4[ab] = (uint32_t)row * 64u + (uint32_t)((t4 ^ ((row >> 1) & 3)) << 4);
+    }
+    {
+      const int vr[4] = {2 * t4, 2 * t4 + 1, 2 * t4 + 8, 2 * t4 + 9};
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        voff4[k] = (uint32_t)vr[k] * 64u + (uint32_t)((((g4 >> 1) ^ ((vr[k] >> 1) & 3)) << 4) | ((g4 & 1) << 3));
     }
   }
 
@@ -1235,14 +1301,38 @@ struct Consumer {
       for (int j = 0; j < NT; ++j)
 #pragma unroll
         for (int e = 0; e < 4; ++e) sacc[u][j][e] = 0.f;
+    float ks4[TW][2];  // MXFP4: the K rows' factors 2^(largest block code - 127)
+    if constexpr (FP4) {
 #pragma unroll
-    for (int cb = 0; cb < NCH; ++cb) {
+      for (int u = 0; u < TW; ++u) {
+        const uint32_t tb = kst + (uint32_t)(tau0 + u) * TILEB;
+        const int rA = 16 * (tau0 + u) + g4;
+        const uint32_t swa = lds32(sst + (uint32_t)rA * 4u), swb = lds32(sst + (uint32_t)(rA + 8) * 4u);
+        ks4[u][0] = e8m0_to_f32(mx_max_code(swa));
+        ks4[u][1] = e8m0_to_f32(mx_max_code(swb));
+        const uint32_t fa = mx_block_factor(swa, t4), fb = mx_block_factor(swb, t4);
+        const uint4 ka = lds128(tb + koff4[0]), kb = lds128(tb + koff4[1]);
+        const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w};
+        const uint32_t wb[4] = {kb.x, kb.y, kb.z, kb.w};
+#pragma unroll
+        for (int s = 0; s < KSTEPS; ++s) {
+          // k-step s: dims 32 t4 + 4 s + {0, 1} (byte 2 s) and + {2, 3} (byte 2 s + 1)
+          const uint32_t xa = wa[s >> 1] >> (16 * (s & 1)), xb = wb[s >> 1] >> (16 * (s & 1));
+          const uint32_t a0 = mul_f16x2(e2m1x2_to_f16x2(xa), fa), a2 = mul_f16x2(e2m1x2_to_f16x2(xa >> 8), fa);
+          const uint32_t a1 = mul_f16x2(e2m1x2_to_f16x2(xb), fb), a3 = mul_f16x2(e2m1x2_to_f16x2(xb >> 8), fb);
+#pragma unroll
+          for (int j = 0; j < NT; ++j) mma16816<true>(sacc[u][j], a0, a1, a2, a3, qf[j][s][0], qf[j][s][1]);
+        }
+      }
+    }
+#pragma unroll
+    for (int cb = 0; cb < (FP4 ? 0 : NCH); ++cb) {
 #pragma unroll
       for (int hl = 0; hl < 2; ++hl) {
         uint4 ka[TW], kb[TW];
 #pragma unroll
         for (int u = 0; u < TW; ++u) {
-          const uint32_t tb = kst + (uint32_t)(tau0 + u) * 2048u;
+          const uint32_t tb = kst + (uint32_t)(tau0 + u) * TILEB;
           ka[u] = lds128(tb + koff[cb][0][hl]);
           kb[u] = lds128(tb + koff[cb][1][hl]);
         }
@@ -1285,11 +1375,16 @@ struct Consumer {
     for (int u = 0; u < TW; ++u) {
       const int rA = 16 * (tau0 + u) + g4;
       ks[u][0] = ks[u][1] = vs[u][0] = vs[u][1] = 1.f;
-      if (ktok) {
+      if constexpr (FP4) {
+        ks[u][0] = ks4[u][0];
+        ks[u][1] = ks4[u][1];
+        vs[u][0] = e8m0_to_f32(mx_max_code(lds32(sst + (uint32_t)(p.TT + rA) * 4u)));
+        vs[u][1] = e8m0_to_f32(mx_max_code(lds32(sst + (uint32_t)(p.TT + rA + 8) * 4u)));
+      } else if (ktok) {
         ks[u][0] = lds_f32(sst + rA * 4);
         ks[u][1] = lds_f32(sst + (rA + 8) * 4);
       }
-      if constexpr (VTOK) {
+      if constexpr (VTOK && !FP4) {
         vs[u][0] = lds_f32(sst + p.TT * 4 + rA * 4);
         vs[u][1] = lds_f32(sst + p.TT * 4 + (rA + 8) * 4);
       }
@@ -1403,10 +1498,40 @@ struct Consumer {
     // ---- O^T += V^T P^T ---------------------------------------------------------
 #pragma unroll
     for (int u = 0; u < TW; ++u) {
+      if constexpr (FP4) {
+        // tokens 2t4, 2t4+1, 2t4+8, 2t4+9: dims [16 g4, 16 g4 + 16), byte i = dims 16 g4 + 2i, +1;
+        // m-tile mt rows g4 / g4+8 = dims 16 g4 + 2 mt / + 1 (the FP8 head_dim-128 order)
+        const uint32_t tb = vst + (uint32_t)(tau0 + u) * TILEB;
+        const int vr0 = 16 * (tau0 + u) + 2 * t4;
+        const int vrow[4] = {vr0, vr0 + 1, vr0 + 8, vr0 + 9};
+        uint2 vv[4];
+        uint32_t fv[4];
 #pragma unroll
-      for (int cb = 0; cb < NCH; ++cb) {
+        for (int k = 0; k < 4; ++k) {
+          vv[k] = lds64(tb + voff4[k]);
+          fv[k] = mx_block_factor(lds32(sst + (uint32_t)(p.TT + vrow[k]) * 4u), g4 >> 1);
+        }
+        if (!interior[u]) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (!token_ok(h, vrow[k])) vv[k] = make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t w[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            w[k] = mul_f16x2(e2m1x2_to_f16x2((mt < 4 ? vv[k].x : vv[k].y) >> (8 * (mt & 3))), fv[k]);
+          const uint32_t r0 = __byte_perm(w[0], w[1], 0x5410u), r1 = __byte_perm(w[0], w[1], 0x7632u);
+          const uint32_t r2 = __byte_perm(w[2], w[3], 0x5410u), r3 = __byte_perm(w[2], w[3], 0x7632u);
+#pragma unroll
+          for (int j = 0; j < NT; ++j) mma16816<true>(o[mt][j], r0, r1, r2, r3, pb[u][j][0], pb[u][j][1]);
+        }
+      }
+#pragma unroll
+      for (int cb = 0; cb < (FP4 ? 0 : NCH); ++cb) {
         uint4 vv[4];
-        const uint32_t tb = vst + (uint32_t)(tau0 + u) * 2048u;
+        const uint32_t tb = vst + (uint32_t)(tau0 + u) * TILEB;
 #pragma unroll
         for (int k = 0; k < 4; ++k) vv[k] = lds128(tb + voff[cb][k]);
         if (!interior[u]) {
@@ -1664,7 +1789,7 @@ struct Consumer {
         break;
       }
       const uint32_t kst = sm.stage(s, p);
-      const uint32_t vst = kst + (uint32_t)p.TT * 128u * NCH;
+      const uint32_t vst = kst + (uint32_t)p.TT * ROWB * NCH;
       const uint32_t sst = kst + p.off_scale;
       const int steps = p.TT / (16 * TW);
       for (int j = wt; j < steps; j += p.Wt) step(h, kst, vst, sst, j * TW);
@@ -1688,7 +1813,7 @@ __device__ __forceinline__ void cluster_sync_all() {
 // MAXW: warps per CTA the instantiation is built for (5: up to 4 consumer
 // warps, two CTAs per SM at head_dim 64/128 and FP8 head_dim 256; 9: up to 8
 // row-slice warps).
-template <bool FP8, int D, int NT, bool VTOK, int TW, int MAXW, bool QF16 = false>
+template <bool FP8, int D, int NT, bool VTOK, int TW, int MAXW, bool QF16 = false, bool FP4 = false>
 __global__ void __launch_bounds__(MAXW * 32, (MAXW == 5 && (D <= 128 || FP8)) ? 2 : 1) pa_tile_kernel(const __grid_constant__ PaParams p,
                                                                       const __grid_constant__ CUtensorMap tmK,
                                                                       const __grid_constant__ CUtensorMap tmV) {
@@ -1717,16 +1842,16 @@ __global__ void __launch_bounds__(MAXW * 32, (MAXW == 5 && (D <= 128 || FP8)) ? 
   }
   __syncthreads();
   constexpr int ELT = FP8 ? 1 : 2;
-  constexpr int NCH = D * ELT / 128;
+  constexpr int NCH = FP4 ? 1 : D * ELT / 128;
   if (warp == p.NCW) {
-    Producer<ELT, NCH> prod(p, &tmK, &tmV, sm);
+    Producer<ELT, NCH, FP4 ? 64 : 128> prod(p, &tmK, &tmV, sm);
     prod.run();
     if (p.merge == kMergeCluster) {
       cluster_sync_all();
       cluster_sync_all();
     }
   } else {
-    Consumer<FP8, D, NT, VTOK, TW, QF16> cons(p, sm);
+    Consumer<FP8, D, NT, VTOK, TW, QF16, FP4> cons(p, sm);
     cons.run();
     if (p.merge == kMergeCluster) {
       cluster_sync_all();

@@ -29,8 +29,9 @@ class DeviceWorkload:
             self.v = t(w.v_cache)
         self.bt = t(w.block_table.astype(np.int32))
         self.ctx = t(w.ctx_lens.astype(np.int32))
-        self.ks = t(w.k_scale.astype(np.float32)) if w.k_scale is not None else None
-        self.vs = t(w.v_scale.astype(np.float32)) if w.v_scale is not None else None
+        sdt = np.uint8 if w.kv_dtype == pw.KV_MXFP4 else np.float32  # MXFP4: E8M0 block-scale bytes
+        self.ks = t(w.k_scale.astype(sdt)) if w.k_scale is not None else None
+        self.vs = t(w.v_scale.astype(sdt)) if w.v_scale is not None else None
         self.sinks = t(w.sinks.astype(np.float32)) if w.sinks is not None else None
         self.idx = t(w.topk_idx.astype(np.int32)) if w.topk_idx is not None else None
         self.out = torch.empty_like(self.q)

@@ -22,16 +22,17 @@ def kernel_shape(d):
     rw = 8 * nt
     wr = -(-R // rw)
     wt = 1 if wr >= 4 else 4 // wr
-    elt = 1 if d["kv_dtype"] == 0 else 2
-    rb = d["head_dim"] * elt
+    mx = d["kv_dtype"] == 2  # MXFP4: 64-byte rows (head_dim 128), the FP8 path
+    elt = 1 if d["kv_dtype"] in (0, 2) else 2
+    rb = d["head_dim"] // 2 if mx else d["head_dim"] * elt
     tt = min(128, max(16, 32768 // (2 * rb)))
-    tw = 2 if (d["kv_dtype"] == 0 and d["head_dim"] == 128) else 1
+    tw = 2 if (d["kv_dtype"] in (0, 2) and d["head_dim"] == 128) else 1
     k = dict(R=R, G=G, nt=nt, rw=rw, wr=wr, wt=wt, ncw=wr * wt, rpad=wr * rw, elt=elt, rb=rb,
              tt=tt, tw=tw, bh=min(d["page_size"], tt), umma=False, rh=0)
     # more than 16 rows on dense decode: the tensor-memory consumer (two
     # softmax warpgroups of rh rows, 128-token stages), taken by AUTO
     # (BF16 caches with FP16 queries stay on the tile consumer)
-    supported = d.get("sparse_topk", 0) == 0 and R > (8 if d["head_dim"] == 256 else 16) and (
+    supported = d.get("sparse_topk", 0) == 0 and not mx and R > (8 if d["head_dim"] == 256 else 16) and (
         d["head_dim"] == 128 or (d["kv_dtype"] == 0 and d["head_dim"] == 256)) and not (
         d["kv_dtype"] == 1 and d.get("q_dtype", 0) == 1)
     consumer = d.get("consumer", 0)
@@ -45,7 +46,7 @@ def kernel_shape(d):
 
 
 def smem_total(d, k, ns, cluster, nq):
-    stage = 2 * k["tt"] * k["rb"] + (1024 if d["scale_mode"] == 2 else 0)
+    stage = 2 * k["tt"] * k["rb"] + (1024 if d["scale_mode"] in (2, 3) else 0)
     off = ns * stage
     if k["umma"]:
         rn = k["nwg"] * k["rh"]

@@ -101,6 +101,12 @@ PLAN_CASES = [
     desc(num_q_heads=64, num_kv_heads=8, kv_dtype=1, scale_mode=0, head_dim=64),
     desc(num_q_heads=64, num_kv_heads=1, kv_dtype=1, scale_mode=0, head_dim=64, q_dtype=pa.PA_Q_FP16),
     desc(batch=8, num_q_heads=32, num_kv_heads=2, query_len=2, scale_mode=2),  # FP8 per-token, 32 rows: auto
+    # MXFP4 (64-byte rows, 16 KiB stages, block scales as per-token scale slots): tile consumer
+    desc(kv_dtype=pa.PA_KV_MXFP4, scale_mode=pa.PA_SCALE_MX_BLOCK),
+    desc(batch=32, num_q_heads=64, num_kv_heads=4, query_len=4, page_size=128, kv_dtype=pa.PA_KV_MXFP4,
+         scale_mode=pa.PA_SCALE_MX_BLOCK),
+    desc(num_q_heads=16, num_kv_heads=8, kv_dtype=pa.PA_KV_MXFP4, scale_mode=pa.PA_SCALE_MX_BLOCK,
+         merge_mode=pa.PA_MERGE_CLUSTER, schedule=pa.PA_SCHED_PER_UNIT, max_partitions=4),
 ]
 
 
@@ -146,6 +152,14 @@ BAD = [
     (dict(consumer=pa.PA_CONSUMER_TMEM, num_q_heads=128, num_kv_heads=1), pa.PA_ERR_UNSUPPORTED),  # > 64 rows
     (dict(consumer=pa.PA_CONSUMER_TMEM, num_q_heads=64, num_kv_heads=1, head_dim=256), pa.PA_ERR_UNSUPPORTED),
     (dict(consumer=-1), pa.PA_ERR_INVALID_ARG),
+    (dict(kv_dtype=pa.PA_KV_MXFP4, scale_mode=pa.PA_SCALE_PER_TOKEN), pa.PA_ERR_INVALID_ARG),  # MX scales only
+    (dict(scale_mode=pa.PA_SCALE_MX_BLOCK), pa.PA_ERR_INVALID_ARG),  # FP8 caches take no MX scales
+    (dict(kv_dtype=pa.PA_KV_MXFP4, scale_mode=pa.PA_SCALE_MX_BLOCK, head_dim=256), pa.PA_ERR_UNSUPPORTED),
+    (dict(kv_dtype=pa.PA_KV_MXFP4, scale_mode=pa.PA_SCALE_MX_BLOCK, sparse_topk=64), pa.PA_ERR_UNSUPPORTED),
+    (dict(kv_dtype=pa.PA_KV_MXFP4, scale_mode=pa.PA_SCALE_MX_BLOCK, consumer=pa.PA_CONSUMER_TMEM,
+          num_q_heads=64, num_kv_heads=4), pa.PA_ERR_UNSUPPORTED),  # tile consumer only
+    (dict(kv_dtype=3), pa.PA_ERR_INVALID_ARG),
+    (dict(scale_mode=4), pa.PA_ERR_INVALID_ARG),
 ]
 
 
