@@ -45,6 +45,7 @@ class Shape(ctypes.Structure):
         ("topk", ctypes.c_int),
         ("sm_scale", ctypes.c_double),
         ("q_dtype", ctypes.c_int),
+        ("v_layout", ctypes.c_int),
     ]
 
 
@@ -132,7 +133,7 @@ class Oracle:
         return Shape(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.query_len,
                      w.page_size, w.max_pages_per_seq, w.num_pages, w.kv_dtype, w.scale_mode,
                      int(w.causal), int(w.window), int(w.sinks is not None), int(w.topk),
-                     sm_scale, int(getattr(w, "q_dtype", 0)))
+                     sm_scale, int(getattr(w, "q_dtype", 0)), int(getattr(w, "v_layout", 0)))
 
     @staticmethod
     def _arrays(w):

@@ -27,6 +27,12 @@
  *       MXFP4 K/V without a layout): the OCP Microscaling (MX) v1.0 format,
  *       blocks of 32 consecutive head dims of one token row, each an E8M0
  *       scale times 32 FP4 E2M1 elements (see kv_element for the layout).
+ *     Transposed V (PR "Extend packed D256 PA decode pipe to page16,
+ *       transposed V and sliding windows", and the D64 note of PR "Merge
+ *       gfx1250 PA decode partitions ..."): a page's BF16 V rows stored as
+ *       chunks of 8 consecutive tokens per head dim, [S/8][D][8], so one
+ *       chunk's dims sit 16 bytes apart and consecutive chunks 16 * D bytes
+ *       apart.
  *     x_t = sm_scale * sum_d q[d] * k[d]  (q widened exactly from BF16 or FP16:
  *       PR "Extend packed D256 PA decode pipe ...", Validation, and PR "Merge
  *       gfx1250 PA decode partitions ...", Validation, run BF16 and FP16
@@ -59,6 +65,8 @@ enum { ORACLE_KV_FP8 = 0, ORACLE_KV_BF16 = 1, ORACLE_KV_MXFP4 = 2 };
 enum { ORACLE_Q_BF16 = 0, ORACLE_Q_FP16 = 1 };
 enum { ORACLE_SCALE_NONE = 0, ORACLE_SCALE_PER_TENSOR = 1, ORACLE_SCALE_PER_TOKEN = 2, ORACLE_SCALE_MX_BLOCK = 3 };
 #define ORACLE_MX_BLOCK 32
+enum { ORACLE_V_PLAIN = 0, ORACLE_V_TRANSPOSED = 1 };
+#define ORACLE_V_CHUNK 8 /* tokens per transposed-V chunk */
 
 typedef struct {
   int batch;
@@ -76,7 +84,8 @@ typedef struct {
   int has_sinks;
   int topk; /* 0 = dense decode; > 0 = sparse index-list decode (QL must be 1) */
   double sm_scale;
-  int q_dtype; /* ORACLE_Q_BF16 or ORACLE_Q_FP16 (the query's element type) */
+  int q_dtype;  /* ORACLE_Q_BF16 or ORACLE_Q_FP16 (the query's element type) */
+  int v_layout; /* ORACLE_V_PLAIN or ORACLE_V_TRANSPOSED (BF16 caches) */
 } pa_oracle_shape;
 
 /* OCP 8-bit floating point, E4M3 ("fn": no infinities, S.1111.111 is NaN):
@@ -194,6 +203,18 @@ static double kv_element(const pa_oracle_shape* sh, const void* cache, const voi
   }
 }
 
+/* Element d of the V row (page, g, slot): the plain layout, or the transposed
+ * one (BF16 only), where the page block of head g is [S/8 chunks][D][8 tokens]. */
+static double v_element(const pa_oracle_shape* sh, const void* cache, const void* scale,
+                        int page, int g, int slot, int d) {
+  if (sh->v_layout == ORACLE_V_TRANSPOSED) {
+    size_t block = ((size_t)page * sh->num_kv_heads + g) * (size_t)(sh->page_size / ORACLE_V_CHUNK);
+    size_t idx = ((block + (size_t)(slot / ORACLE_V_CHUNK)) * sh->head_dim + d) * ORACLE_V_CHUNK + slot % ORACLE_V_CHUNK;
+    return pa_oracle_bf16_to_double(((const uint16_t*)cache)[idx]);
+  }
+  return kv_element(sh, cache, scale, page, g, slot, d);
+}
+
 /* Physical page holding logical token t of sequence b, or -1 if the table
  * entry is out of the pool. */
 static int token_page(const pa_oracle_shape* sh, const int32_t* block_table, int b, int t) {
@@ -258,7 +279,7 @@ int pa_oracle_row_partial(const pa_oracle_shape* sh, const uint16_t* q, const vo
     double w = exp(x[j] - m);
     l += w;
     for (int d = 0; d < D; ++d)
-      o_out[d] += w * kv_element(sh, v_cache, v_scale, page, g, t % sh->page_size, d);
+      o_out[d] += w * v_element(sh, v_cache, v_scale, page, g, t % sh->page_size, d);
   }
   free(x);
   *m_out = m;
@@ -302,6 +323,9 @@ static int check_shape(const pa_oracle_shape* sh) {
     return PA_ORACLE_BAD_ARG;
   if ((sh->kv_dtype == ORACLE_KV_MXFP4) != (sh->scale_mode == ORACLE_SCALE_MX_BLOCK)) return PA_ORACLE_BAD_ARG;
   if (sh->kv_dtype == ORACLE_KV_MXFP4 && sh->head_dim % ORACLE_MX_BLOCK != 0) return PA_ORACLE_BAD_ARG;
+  if (sh->v_layout != ORACLE_V_PLAIN && sh->v_layout != ORACLE_V_TRANSPOSED) return PA_ORACLE_BAD_ARG;
+  if (sh->v_layout == ORACLE_V_TRANSPOSED && (sh->kv_dtype != ORACLE_KV_BF16 || sh->page_size % ORACLE_V_CHUNK != 0))
+    return PA_ORACLE_BAD_ARG;
   return PA_ORACLE_OK;
 }
 

@@ -55,6 +55,9 @@ SCALE_MX_BLOCK = 3
 MX_BLOCK = 32
 Q_BF16 = 0
 Q_FP16 = 1
+V_PLAIN = 0
+V_TRANSPOSED = 1  # BF16 V as [num_pages, num_kv_heads, page_size / 8, head_dim, 8]
+V_CHUNK = 8
 
 FP8_MAX = 448.0
 FP8_NAN = 0x7F
@@ -93,6 +96,7 @@ class Workload:
     topk_idx: Optional[np.ndarray] = None  # int32 [B, topk]
     seed: int = 0
     q_dtype: int = Q_BF16  # element type of q and of the output
+    v_layout: int = V_PLAIN  # V cache layout (V_TRANSPOSED: BF16 only)
 
     @property
     def group(self) -> int:
@@ -157,6 +161,14 @@ def mxfp4_encode(x: np.ndarray):
     code = code.reshape(x.shape[:-1] + (D,))
     packed = (code[..., 0::2] | (code[..., 1::2] << 4)).astype(np.uint8)
     return packed, X.astype(np.uint8)
+
+
+def transpose_v(v_cache: np.ndarray) -> np.ndarray:
+    """A plain [P, Hkv, S, D] BF16 V cache rearranged into the transposed
+    layout [P, Hkv, S/8, D, 8] (chunks of 8 tokens per head dim; the same
+    values, moved)."""
+    P, H, S, D = v_cache.shape
+    return np.ascontiguousarray(v_cache.reshape(P, H, S // V_CHUNK, V_CHUNK, D).transpose(0, 1, 2, 4, 3))
 
 
 def _pool_and_table(rng, ctx_lens, page_size, pool_pages, max_pages):
@@ -239,7 +251,8 @@ def _fill_cache(rng, num_pages, hkv, S, D, used_pages, valid_slots, kv_dtype,
 def make_dense(name, *, batch, hkv, group, head_dim, query_len, page_size,
                ctx_lens, kv_dtype, scale_mode, seed, pool_pages=None,
                causal=1, window=0, with_sinks=False, max_pages=None,
-               v_amplitude=1.0, vfun=None, q_amplitude=1.0, token_sigma=0.0, q_dtype=Q_BF16):
+               v_amplitude=1.0, vfun=None, q_amplitude=1.0, token_sigma=0.0, q_dtype=Q_BF16,
+               v_layout=V_PLAIN):
     """Build a dense paged-decode workload with the given context lengths.
 
     ``q_amplitude`` scales the N(0,1) query values before rounding to the
@@ -272,13 +285,15 @@ def make_dense(name, *, batch, hkv, group, head_dim, query_len, page_size,
     sinks = rng.standard_normal(hq, dtype=np.float32) if with_sinks else None
     if kv_dtype == KV_BF16:
         scale_mode = SCALE_NONE
+    if v_layout == V_TRANSPOSED:
+        vc = transpose_v(vc)
     return Workload(name=name, batch=batch, num_q_heads=hq, num_kv_heads=hkv,
                     head_dim=head_dim, query_len=query_len, page_size=page_size,
                     num_pages=pool_pages, max_pages_per_seq=max_pages,
                     kv_dtype=kv_dtype, scale_mode=scale_mode, q=q, k_cache=kc,
                     v_cache=vc, block_table=table, ctx_lens=ctx_lens, k_scale=ks,
                     v_scale=vs, causal=causal, window=window, sinks=sinks,
-                    seed=seed, q_dtype=q_dtype)
+                    seed=seed, q_dtype=q_dtype, v_layout=v_layout)
 
 
 # --- the five workloads -----------------------------------------------------

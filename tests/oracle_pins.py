@@ -61,6 +61,10 @@ def dequant(w, which: str) -> np.ndarray:
     MXFP4 (float64 [P, Hkv, S, D])."""
     cache = w.k_cache if which == "k" else w.v_cache
     scale = w.k_scale if which == "k" else w.v_scale
+    if which == "v" and getattr(w, "v_layout", pw.V_PLAIN) == pw.V_TRANSPOSED:
+        # [P, Hkv, S/8, D, 8] back to [P, Hkv, S, D]: swap the last two axes, merge chunks
+        P, H, C, D, E = cache.shape
+        cache = np.ascontiguousarray(np.swapaxes(cache, 3, 4)).reshape(P, H, C * E, D)
     if w.kv_dtype == pw.KV_MXFP4:
         e2m1, e8m0 = mx_tables()
         lo = e2m1[cache & 0xF]
@@ -204,6 +208,25 @@ def pin_mx_constant_v(orc):
     w = small(65, kv=pw.KV_MXFP4, scale=pw.SCALE_MX_BLOCK, D=64, QL=2, lens=(3, 40), vfun=vconst)
     out = orc.decode(w)
     assert_close(out, np.full_like(out, 0.75), what="mx constant V")
+
+
+def pin_transposed_v(orc):
+    """Transposed V (BF16 [P, Hkv, S/8, D, 8]): the oracle against the brute
+    force (which undoes the layout with NumPy axis swaps), and equal to the
+    same values in the plain layout."""
+    cases = [
+        dict(seed=71, D=64, S=16, lens=(5, 23, 40)),
+        dict(seed=72, D=32, S=64, QL=3, window=17, lens=(0, 2, 19, 130), group=2, sinks=True),
+        dict(seed=73, D=128, S=32, QL=2, q_dtype=pw.Q_FP16, lens=(1, 70, 99), hkv=2, group=2),
+    ]
+    for c in cases:
+        w = small(kv=pw.KV_BF16, scale=pw.SCALE_NONE, v_layout=pw.V_TRANSPOSED, **c)
+        assert w.v_cache.shape[-1] == pw.V_CHUNK
+        out = orc.decode(w)
+        assert_close(out, brute_force(w), what=f"transposed V brute force {c}")
+        plain = small(kv=pw.KV_BF16, scale=pw.SCALE_NONE, **c)
+        assert np.array_equal(plain.k_cache, w.k_cache)
+        assert_close(out, orc.decode(plain), rtol=0, atol=0, what=f"transposed V = plain {c}")
 
 
 def pin_bf16_widen(orc):
@@ -548,5 +571,5 @@ ALL_PINS = [
     pin_one_token, pin_two_tokens, pin_constant_v, pin_window_one_position, pin_causal_prefix,
     pin_relocation, pin_empty, pin_merge_any_split, pin_sparse, pin_per_token_uniform,
     pin_gqa_heads, pin_poison_unread, pin_logits_brute_force, pin_logits_closed_forms,
-    pin_mx_codes, pin_mx_brute_force, pin_mx_constant_v,
+    pin_mx_codes, pin_mx_brute_force, pin_mx_constant_v, pin_transposed_v,
 ]

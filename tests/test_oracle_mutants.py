@@ -26,7 +26,7 @@ MUTANTS = [
     ("e4m3 bias", "ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
     ("e4m3 subnormal", "ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
     ("per-token scale slot", "v *= (double)((const float*)scale)[row];", "v *= (double)((const float*)scale)[row - slot];"),
-    ("V uses K scale", "kv_element(sh, v_cache, v_scale,", "kv_element(sh, v_cache, k_scale,"),
+    ("V uses K scale", "v_element(sh, v_cache, v_scale,", "v_element(sh, v_cache, k_scale,"),
     ("q operand reversed", "s += q_element(sh, qrow, d) *", "s += q_element(sh, qrow, D - 1 - d) *"),
     ("f16 bias", "ldexp(1024.0 + (double)f, e - 25)", "ldexp(1024.0 + (double)f, e - 24)"),
     ("f16 subnormal", "mag = ldexp((double)f, -24);", "mag = ldexp((double)f, -25);"),
@@ -54,6 +54,13 @@ MUTANTS = [
     ("e2m1 exponent bias", "ldexp(1.0 + 0.5 * (double)m, e - 1)", "ldexp(1.0 + 0.5 * (double)m, e - 2)"),
     ("e2m1 subnormal", "e == 0 ? 0.5 * (double)m", "e == 0 ? 1.0 * (double)m"),
     ("e8m0 bias", "return ldexp(1.0, (int)code - 127);", "return ldexp(1.0, (int)code - 126);"),
+    ("transposed V read as plain", "  if (sh->v_layout == ORACLE_V_TRANSPOSED) {\n    size_t block",
+     "  if (0) {\n    size_t block"),
+    ("transposed V token in chunk", "* sh->head_dim + d) * ORACLE_V_CHUNK + slot % ORACLE_V_CHUNK;",
+     "* sh->head_dim + d) * ORACLE_V_CHUNK + (slot + 1) % ORACLE_V_CHUNK;"),
+    ("transposed V dims and tokens swapped",
+     "size_t idx = ((block + (size_t)(slot / ORACLE_V_CHUNK)) * sh->head_dim + d)",
+     "size_t idx = ((block + (size_t)(slot / ORACLE_V_CHUNK)) * sh->head_dim + (d ^ 1))"),
     ("logits kv row off by one", "pa_oracle_e4m3_to_double(kv[(size_t)j * dim + d]);",
      "pa_oracle_e4m3_to_double(kv[(size_t)(j + 1 < num_kv ? j + 1 : j) * dim + d]);"),
 ]
