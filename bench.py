@@ -67,7 +67,7 @@ def measured_peak_gbs():
 # plus the shared header and the host code that sets its launch.
 KERNEL_SOURCES = {
     "pa_tile": ("pa_tile.cuh", "pa_tile_fp8_d128.cu", "pa_tile_fp8_d256.cu", "pa_tile_bf16.cu",
-                "pa_tile_bf16_q16.cu", "pa_tile_fp4.cu"),
+                "pa_tile_bf16_q16.cu", "pa_tile_fp4.cu", "pa_tile_bf16_tv.cu", "pa_tile_bf16_tv_q16.cu"),
     "pa_mtp": ("pa_tile.cuh", "pa_tc.cuh", "pa_mtp.cuh", "pa_mtp_fp8.cu", "pa_mtp_bf16.cu"),
     "pa_reduce": ("pa_tile.cuh", "pa_reduce.cu"),
     "pa_logits": ("pa_tile.cuh", "pa_tc.cuh", "pa_logits.cu"),
@@ -102,7 +102,7 @@ def profile_name(args, kernel: str) -> Optional[str]:
     name = f"{kernel}_{args.workload}"
     if args.kv == "bf16" and args.workload in ("sparse", "mtp4", "sparse_prefill"):
         name += "_bf16"
-    if args.kv == "bf16" and args.workload == "dense":
+    if (args.kv == "bf16" and args.workload == "dense") or args.v_layout != "plain":
         return None
     if args.kv == "mxfp4":
         name += "_mxfp4"
@@ -288,6 +288,8 @@ def workload_name(args) -> str:
             ", MXFP4 K/V (E2M1 elements, one E8M0 scale per 32 head dims)"
     elif args.kv == "bf16" and args.workload in ("dense", "mtp4"):
         name = name.replace("dense FP8 paged decode", "dense BF16 paged decode") + ", BF16 K/V"
+    if args.v_layout == "transposed":
+        name += ", V transposed ([pages, heads, S/8, D, 8])"
     return name
 
 
@@ -295,8 +297,11 @@ def make_workload(args, rank):
     kv = {"fp8": pw.KV_FP8, "bf16": pw.KV_BF16, "mxfp4": pw.KV_MXFP4}[args.kv]
     if args.kv == "mxfp4" and args.workload not in ("dense", "mtp4"):
         raise SystemExit("--kv mxfp4 applies to the dense and mtp4 workloads")
+    if args.v_layout == "transposed" and not (args.kv == "bf16" and args.workload in ("dense", "mtp4")):
+        raise SystemExit("--v-layout transposed applies to --kv bf16 on the dense and mtp4 workloads")
+    vl = pw.V_TRANSPOSED if args.v_layout == "transposed" else pw.V_PLAIN
     if args.workload == "dense":
-        return pw.dense(seed=1002 + rank, page_size=args.page, batch=args.batch or 64, kv_dtype=kv)
+        return pw.dense(seed=1002 + rank, page_size=args.page, batch=args.batch or 64, kv_dtype=kv, v_layout=vl)
     if args.workload == "tiny":
         return pw.tiny()
     if args.workload == "d256":
@@ -304,7 +309,7 @@ def make_workload(args, rank):
     if args.workload == "sparse":
         return pw.sparse(kv_dtype=kv, rows=args.batch or 64)
     if args.workload == "mtp4":
-        return pw.mtp4(kv_dtype=kv, batch=args.batch or 32)
+        return pw.mtp4(kv_dtype=kv, batch=args.batch or 32, v_layout=vl)
     if args.workload == "sparse_prefill":
         return pw.sparse_prefill(kv_dtype=kv, rows=args.rows)
     raise ValueError(args.workload)
@@ -488,6 +493,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="dense", choices=sorted(WORKLOADS),
                     help="the headline line uses the default dense workload; the others are for profiling")
+    ap.add_argument("--v-layout", default="plain", choices=["plain", "transposed"],
+                    help="V cache layout (transposed: BF16 caches, dense and mtp4 workloads)")
     ap.add_argument("--kv", default="fp8", choices=["fp8", "bf16", "mxfp4"],
                     help="cache format (dense: fp8, bf16, mxfp4; mtp4: all three; sparse workloads: fp8, bf16)")
     ap.add_argument("--rows", type=int, default=1024, help="sparse_prefill: prompt rows")

@@ -37,7 +37,9 @@
  *   v_cache       [num_pages, num_kv_heads, page_size, head_dim]
  *                 FP8 e4m3fn bytes (OCP) or BF16; MXFP4:
  *                 [num_pages, num_kv_heads, page_size, head_dim / 2] bytes,
- *                 two E2M1 codes each (see PA_KV_MXFP4)
+ *                 two E2M1 codes each (see PA_KV_MXFP4); v_cache with
+ *                 PA_V_TRANSPOSED: [num_pages, num_kv_heads, page_size / 8,
+ *                 head_dim, 8] BF16
  *   block_table   [batch, max_pages_per_seq]  int32 physical page ids; only
  *                 the entries covering [0, L_b) are ever read
  *   ctx_lens      [batch]  int32, 0 <= L_b <= max_pages_per_seq * page_size
@@ -105,6 +107,15 @@ enum { PA_KV_FP8_E4M3 = 0, PA_KV_BF16 = 1, PA_KV_MXFP4 = 2 };
  * "Merge gfx1250 PA decode partitions in the tile kernel and speed up dense
  * decode", Validation, run BF16 and FP16 queries). */
 enum { PA_Q_BF16 = 0, PA_Q_FP16 = 1 };
+/* Layout of the V cache (PR "Extend packed D256 PA decode pipe to page16,
+ * transposed V and sliding windows", and PR "Merge gfx1250 PA decode
+ * partitions in the tile kernel and speed up dense decode", where transposed
+ * V "spaces its eight-token chunks 16 * head_dim bytes apart"): PA_V_PLAIN is
+ * [num_pages, num_kv_heads, page_size, head_dim]; PA_V_TRANSPOSED (BF16 caches,
+ * dense decode, the tile consumer) is [num_pages, num_kv_heads, page_size / 8,
+ * head_dim, 8]: for each chunk of 8 consecutive tokens, the 8 values of one
+ * head dim are contiguous. */
+enum { PA_V_PLAIN = 0, PA_V_TRANSPOSED = 1 };
 /* PA_SCALE_MX_BLOCK: the E8M0 block scales of MXFP4 caches (required by them,
  * accepted by no other cache type). */
 enum { PA_SCALE_NONE = 0, PA_SCALE_PER_TENSOR = 1, PA_SCALE_PER_TOKEN = 2, PA_SCALE_MX_BLOCK = 3 };
@@ -159,6 +170,7 @@ typedef struct pa_plan_desc {
   int device;            /* CUDA device ordinal the plan is for */
   int consumer;          /* PA_CONSUMER_*; TMEM on an unsupported shape is PA_ERR_UNSUPPORTED */
   int q_dtype;           /* PA_Q_*: element type of q and out (0 = BF16) */
+  int v_layout;          /* PA_V_*: layout of v_cache (0 = plain) */
 } pa_plan_desc;
 
 typedef struct pa_plan_info {

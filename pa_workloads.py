@@ -311,7 +311,7 @@ def dense_lengths(seed: int, batch: int = 64, lo: int = 1024, hi: int = 8192):
 
 
 def dense(seed: int = 1002, batch: int = 64, lo: int = 1024, hi: int = 8192,
-          kv_dtype: int = KV_FP8, page_size: int = 16) -> Workload:
+          kv_dtype: int = KV_FP8, page_size: int = 16, v_layout: int = V_PLAIN) -> Workload:
     """Batch 64, 8 KV heads, GQA8, D128, page 16, contexts U[1024, 8192], 40k-page pool
     (page_size other than 16 keeps the pool's bytes: 40000 * 16 / page_size pages)."""
     lens = dense_lengths(seed, batch, lo, hi)
@@ -320,7 +320,7 @@ def dense(seed: int = 1002, batch: int = 64, lo: int = 1024, hi: int = 8192,
                       query_len=1, page_size=page_size, ctx_lens=lens, kv_dtype=kv_dtype,
                       scale_mode=SCALE_MX_BLOCK if kv_dtype == KV_MXFP4 else SCALE_PER_TENSOR, seed=seed,
                       pool_pages=max(pool, int(((lens + page_size - 1) // page_size).sum()) + 8),
-                      max_pages=hi // page_size)
+                      max_pages=hi // page_size, v_layout=v_layout)
 
 
 def d256_lengths(seed: int, batch: int = 16, short: int = 8192, long: int = 131072):
@@ -350,13 +350,13 @@ def mtp4_lengths(seed: int, batch: int = 32, lo: int = 4096, hi: int = 65536):
 
 
 def mtp4(seed: int = 1005, kv_dtype: int = KV_FP8, batch: int = 32,
-         lo: int = 4096, hi: int = 65536) -> Workload:
+         lo: int = 4096, hi: int = 65536, v_layout: int = V_PLAIN) -> Workload:
     """Batch 32, 4 KV heads, GQA16, D128, QL4 causal, page 128, contexts U[4096, 65536]."""
     lens = mtp4_lengths(seed, batch, lo, hi)
     return make_dense("mtp4", batch=batch, hkv=4, group=16, head_dim=128,
                       query_len=4, page_size=128, ctx_lens=lens, kv_dtype=kv_dtype,
                       scale_mode=SCALE_MX_BLOCK if kv_dtype == KV_MXFP4 else SCALE_PER_TENSOR, seed=seed, causal=1,
-                      max_pages=(hi + 127) // 128)
+                      max_pages=(hi + 127) // 128, v_layout=v_layout)
 
 
 def sparse(seed: int = 1004, kv_dtype: int = KV_FP8, rows: int = 64,

@@ -23,7 +23,7 @@ __all__ = [
     "PA_SCALE_PER_TENSOR", "PA_SCALE_PER_TOKEN", "PA_SCALE_MX_BLOCK", "PA_MERGE_AUTO", "PA_MERGE_DIRECT", "PA_MERGE_CLUSTER",
     "PA_MERGE_LAST_ARRIVER", "PA_MERGE_REDUCER", "PA_SCHED_AUTO", "PA_SCHED_BALANCED",
     "PA_SCHED_PER_UNIT", "PA_CONSUMER_AUTO", "PA_CONSUMER_TILE", "PA_CONSUMER_TMEM", "PA_Q_BF16",
-    "PA_Q_FP16", "PaError", "PlanDesc", "PlanInfo", "Plan", "library", "library_path",
+    "PA_Q_FP16", "PA_V_PLAIN", "PA_V_TRANSPOSED", "PaError", "PlanDesc", "PlanInfo", "Plan", "library", "library_path",
     "pa_plan_create", "pa_plan_workspace_bytes", "pa_plan_set_workspace", "pa_plan_get_info",
     "pa_plan_destroy", "pa_decode", "pa_decode_sparse", "pa_decode_noalloc", "pa_mqa_logits", "pa_strerror",
     "pa_last_error", "EXPORTED_SYMBOLS",
@@ -36,6 +36,7 @@ PA_MERGE_AUTO, PA_MERGE_DIRECT, PA_MERGE_CLUSTER, PA_MERGE_LAST_ARRIVER, PA_MERG
 PA_SCHED_AUTO, PA_SCHED_BALANCED, PA_SCHED_PER_UNIT = 0, 1, 2
 PA_CONSUMER_AUTO, PA_CONSUMER_TILE, PA_CONSUMER_TMEM = 0, 1, 2
 PA_Q_BF16, PA_Q_FP16 = 0, 1
+PA_V_PLAIN, PA_V_TRANSPOSED = 0, 1
 
 EXPORTED_SYMBOLS = [
     "pa_plan_create", "pa_plan_workspace_bytes", "pa_plan_set_workspace", "pa_plan_get_info",
@@ -60,7 +61,7 @@ class PlanDesc(ctypes.Structure):
         "has_sinks", "sparse_topk")] + [("sm_scale", ctypes.c_float)] + [
         (name, ctypes.c_int) for name in (
             "max_partitions", "merge_mode", "schedule", "sm_count_override",
-            "ctas_per_sm_override", "device", "consumer", "q_dtype")]
+            "ctas_per_sm_override", "device", "consumer", "q_dtype", "v_layout")]
 
 
 class PlanInfo(ctypes.Structure):

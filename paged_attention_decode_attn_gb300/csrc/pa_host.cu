@@ -88,6 +88,7 @@ struct KernelShape {
 bool umma_supported(const pa_plan_desc& d, int R) {
   if (d.sparse_topk > 0 || R <= (d.head_dim == 256 ? 8 : 16)) return false;
   if (d.kv_dtype == PA_KV_MXFP4) return false;  // MXFP4: the tile consumer only
+  if (d.v_layout == PA_V_TRANSPOSED) return false;  // transposed V: the tile consumer only
   // BF16 caches are read in place by BF16 MMAs, whose other operand (Q) must
   // be BF16 too: FP16 queries there take the tile consumer.
   if (d.kv_dtype == PA_KV_BF16 && d.q_dtype == PA_Q_FP16) return false;
@@ -210,6 +211,7 @@ const void* pick_tile_kernel(const pa_plan_desc& d, const KernelShape& k) {
     if (d.head_dim == 128) return pa::tile_kernel_fp8_d128(k.vtok, k.ncw > 4);
     return k.ncw > 4 ? nullptr : pa::tile_kernel_fp8_d256(k.vtok);
   }
+  if (d.v_layout == PA_V_TRANSPOSED) return pa::tile_kernel_bf16_tv(d.head_dim, k.ncw > 4, d.q_dtype == PA_Q_FP16);
   return pa::tile_kernel_bf16(d.head_dim, k.ncw > 4, d.q_dtype == PA_Q_FP16);
 }
 
@@ -246,6 +248,15 @@ pa_status validate_desc(const pa_plan_desc& d) {
     return fail(PA_ERR_INVALID_ARG, "MXFP4 caches take PA_SCALE_MX_BLOCK, and only they do");
   if (d.kv_dtype == PA_KV_MXFP4 && d.sparse_topk > 0)
     return fail(PA_ERR_UNSUPPORTED, "MXFP4 caches support dense decode only");
+  if (d.v_layout != PA_V_PLAIN && d.v_layout != PA_V_TRANSPOSED)
+    return fail(PA_ERR_INVALID_ARG, "unknown v_layout %d", d.v_layout);
+  if (d.v_layout == PA_V_TRANSPOSED) {
+    if (d.kv_dtype != PA_KV_BF16)
+      return fail(PA_ERR_UNSUPPORTED, "the transposed V layout is supported for BF16 caches");
+    if (d.sparse_topk > 0) return fail(PA_ERR_UNSUPPORTED, "the transposed V layout supports dense decode only");
+    if ((long long)d.num_pages * d.num_kv_heads * d.page_size * (d.head_dim / 64) >= (1ll << 31))
+      return fail(PA_ERR_UNSUPPORTED, "transposed V cache has 2^31 or more 128-byte rows");
+  }
   if (d.q_dtype != PA_Q_BF16 && d.q_dtype != PA_Q_FP16)
     return fail(PA_ERR_INVALID_ARG, "unknown q_dtype %d", d.q_dtype);
   if (d.kv_dtype == PA_KV_BF16 && d.scale_mode != PA_SCALE_NONE)
@@ -448,6 +459,7 @@ pa_status compute_plan(pa_plan* pl, int sm_count, int ctas_override) {
                  : d.kv_dtype == PA_KV_MXFP4 ? pa::kScalePerToken
                                              : pa::kScaleNone;
   p.q_f16 = d.q_dtype == PA_Q_FP16;
+  p.v_tr = d.v_layout == PA_V_TRANSPOSED;
   const float sm_scale = d.sm_scale > 0.f ? d.sm_scale : 1.0f / std::sqrt((float)d.head_dim);
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   p.sched = sched;
@@ -515,10 +527,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D view of a paged cache: rows = (page, kv head, slot), columns = head dims.
-pa_status encode_cache_map(const pa_plan* pl, const void* base, CUtensorMap* tm) {
+// A transposed V cache ([page, kv head, slot / 8, dim, slot % 8], BF16) is
+// viewed as 128-byte rows of 8 dims x 8 tokens; a page is BH * D / 64 rows.
+pa_status encode_cache_map(const pa_plan* pl, const void* base, CUtensorMap* tm, bool v) {
   const pa_plan_desc& d = pl->desc;
   auto fn = encode_fn();
   if (!fn) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  if (v && d.v_layout == PA_V_TRANSPOSED) {
+    cuuint64_t dims[2] = {64, (cuuint64_t)d.num_pages * d.num_kv_heads * d.page_size * (d.head_dim / 64)};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {64, (cuuint32_t)(pl->base.BH * (d.head_dim / 64))};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return PA_OK;
+  }
   const bool mx = d.kv_dtype == PA_KV_MXFP4;
   const int elt = d.kv_dtype == PA_KV_FP8_E4M3 || mx ? 1 : 2;
   // MXFP4: rows of head_dim / 2 bytes (64), one box per page, 64-byte swizzle
@@ -562,9 +587,9 @@ pa_status launch(const pa_plan* pl, void* ws_ptr, void* out, const void* q, cons
     if (st != PA_OK) return st;
     if (!pl->tm_valid || pl->tm_k != k_cache || pl->tm_v != v_cache) {
       pl->tm_valid = false;
-      st = encode_cache_map(pl, k_cache, &pl->tmK);
+      st = encode_cache_map(pl, k_cache, &pl->tmK, false);
       if (st != PA_OK) return st;
-      st = encode_cache_map(pl, v_cache, &pl->tmV);
+      st = encode_cache_map(pl, v_cache, &pl->tmV, true);
       if (st != PA_OK) return st;
       pl->tm_k = k_cache;
       pl->tm_v = v_cache;

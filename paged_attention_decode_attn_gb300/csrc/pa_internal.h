@@ -62,6 +62,7 @@ struct PaParams {
   // the two MMA commit barriers, and the tensor-memory address slot
   int off_k16, off_v16, off_q16, off_p16, off_ubar, off_tslot, off_rows;
   int q_f16;  // queries and output are FP16 (else BF16)
+  int v_tr;   // V cache in the transposed layout [pages, Hkv, S/8, D, 8] (BF16)
   // cache bases for the sparse row gathers (dense stages load through the tensor maps)
   const uint8_t* k_cache;
   const uint8_t* v_cache;
@@ -82,6 +83,8 @@ const void* tile_kernel_fp4_d128(int wide);
 const void* tile_kernel_fp8_d256(int vtok);
 const void* tile_kernel_bf16(int d, int wide, int q_f16);
 const void* tile_kernel_bf16_q16(int d, int wide);
+const void* tile_kernel_bf16_tv(int d, int wide, int q_f16);
+const void* tile_kernel_bf16_tv_q16(int d, int wide);
 const void* reduce_kernel(int d);
 // Tensor-memory consumer instantiations (FP8 head_dim 128/256, BF16 head_dim
 // 128; rh = query rows per softmax warpgroup, 16 or 32; nwg = softmax

@@ -595,9 +595,16 @@ struct Producer {
       const uint32_t vst = kst + (uint32_t)TT * (uint32_t)ROWB * NCH;
       const uint32_t bar = sm.full(s, p);
 #pragma unroll
-      for (int cb = 0; cb < NCH; ++cb) {
+      for (int cb = 0; cb < NCH; ++cb)
         tma_load_2d(kst + (uint32_t)(cb * TT + row) * (uint32_t)ROWB, tmK, cb * (128 / ELT), y, bar);
-        tma_load_2d(vst + (uint32_t)(cb * TT + row) * (uint32_t)ROWB, tmV, cb * (128 / ELT), y, bar);
+      if (p.v_tr) {
+        // transposed V: the page's chunks of 8 tokens ([D][8] BF16 each) as
+        // 128-byte rows of 8 dims; the stage holds chunk after chunk
+        tma_load_2d(vst + (uint32_t)row * (uint32_t)(2 * p.D), tmV, 0, y * (p.D / 64), bar);
+      } else {
+#pragma unroll
+        for (int cb = 0; cb < NCH; ++cb)
+          tma_load_2d(vst + (uint32_t)(cb * TT + row) * (uint32_t)ROWB, tmV, cb * (128 / ELT), y, bar);
       }
       if (ktok) {
         const uint32_t sc = kst + p.off_scale;
@@ -1052,9 +1059,11 @@ struct StageView {
 // FP16 operands at the segment start (a runtime flag).
 // FP4: MXFP4 caches (head_dim 128, with FP8 = VTOK = true: FP16 queries, P and
 // V; the per-token K and V factors come from the block scales).
-template <bool FP8, int D, int NT, bool VTOK, int TW, bool QF16 = false, bool FP4 = false>
+// TV: BF16 V in the transposed layout (chunks of 8 tokens per head dim).
+template <bool FP8, int D, int NT, bool VTOK, int TW, bool QF16 = false, bool FP4 = false, bool TV = false>
 struct Consumer {
   static_assert(!FP4 || (FP8 && VTOK && D == 128), "MXFP4 runs the FP8 per-token path at head_dim 128");
+  static_assert(!TV || !FP8, "transposed V: BF16 caches");
   static constexpr int ELT = FP8 ? 1 : 2;
   static constexpr int NCH = FP4 ? 1 : D * ELT / 128;  // column blocks per token row
   static constexpr uint32_t ROWB = FP4 ? 64u : 128u;   // bytes of a stage row per block
@@ -1076,6 +1085,12 @@ struct Consumer {
   // [8 g4, 8 g4 + 8) (dims [16 g4, 16 g4 + 16), MX block g4 / 2) of tokens
   // 2t4, 2t4+1, 2t4+8, 2t4+9 (64-byte rows, 64-byte swizzle)
   uint32_t koff4[2], voff4[4];
+  // transposed V: a stage chunk of 8 tokens is D/8 rows of 128 bytes (8 dims
+  // x 8 tokens) under the 128-byte swizzle; the A fragment of m-tile mt of a
+  // 64-dim block holds dims 8 g4 + 2 mt (row g4) and + 1 (row g4 + 8), the
+  // plain layout's order, read as 4 bytes (tokens 2 t4, 2 t4 + 1) at
+  // row g4, chunk (2 mt + h) ^ g4
+  uint32_t tvoff[4][2];
   float kscale = 1.f, vscale = 1.f;
   // per segment
   uint32_t qf[NT][KSTEPS][2];
@@ -1113,6 +1128,11 @@ struct Consumer {
       for (int k = 0; k < 4; ++k)
         voff[cb][k] = (uint32_t)(cb * p.TT + vr[k]) * 128u + (uint32_t)((g4 ^ (vr[k] & 7)) << 4);
     }
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+        tvoff[mt][hh] = (uint32_t)g4 * 128u + (uint32_t)(((2 * mt + hh) ^ g4) << 4) + 4u * (uint32_t)t4;
     // 64-byte swizzle: row r's 16-byte chunk c sits at chunk c ^ ((r >> 1) & 3)
 #pragma unroll
     for (int ab = 0; ab < 2; ++ab) {
@@ -1528,8 +1548,33 @@ struct Consumer {
           for (int j = 0; j < NT; ++j) mma16816<true>(o[mt][j], r0, r1, r2, r3, pb[u][j][0], pb[u][j][1]);
         }
       }
+      if constexpr (TV) {
+        static_assert(MT_BLK == 4, "64-dim blocks");
+        // tokens 2t4, 2t4+1 (first chunk) and 2t4+8, 2t4+9 (second); those
+        // outside the stage's range are zeroed
+        const uint32_t tb = vst + (uint32_t)(tau0 + u) * (uint32_t)(32 * D);
+        uint32_t m0 = 0xFFFFFFFFu, m1 = 0xFFFFFFFFu;
+        if (!interior[u]) {
+          const int vr0 = 16 * (tau0 + u) + 2 * t4;
+          m0 = (token_ok(h, vr0) ? 0xFFFFu : 0u) | (token_ok(h, vr0 + 1) ? 0xFFFF0000u : 0u);
+          m1 = (token_ok(h, vr0 + 8) ? 0xFFFFu : 0u) | (token_ok(h, vr0 + 9) ? 0xFFFF0000u : 0u);
+        }
 #pragma unroll
-      for (int cb = 0; cb < (FP4 ? 0 : NCH); ++cb) {
+        for (int cb = 0; cb < NCH; ++cb)
+#pragma unroll
+          for (int mt = 0; mt < MT_BLK; ++mt) {
+            const uint32_t base = tb + (uint32_t)cb * 1024u;
+            const uint32_t r0 = lds32(base + tvoff[mt][0]) & m0;
+            const uint32_t r1 = lds32(base + tvoff[mt][1]) & m0;
+            const uint32_t r2 = lds32(base + (uint32_t)(16 * D) + tvoff[mt][0]) & m1;
+            const uint32_t r3 = lds32(base + (uint32_t)(16 * D) + tvoff[mt][1]) & m1;
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+              mma16816<false>(o[cb * MT_BLK + mt][j], r0, r1, r2, r3, pb[u][j][0], pb[u][j][1]);
+          }
+      }
+#pragma unroll
+      for (int cb = 0; cb < ((FP4 || TV) ? 0 : NCH); ++cb) {
         uint4 vv[4];
         const uint32_t tb = vst + (uint32_t)(tau0 + u) * TILEB;
 #pragma unroll
@@ -1813,7 +1858,7 @@ __device__ __forceinline__ void cluster_sync_all() {
 // MAXW: warps per CTA the instantiation is built for (5: up to 4 consumer
 // warps, two CTAs per SM at head_dim 64/128 and FP8 head_dim 256; 9: up to 8
 // row-slice warps).
-template <bool FP8, int D, int NT, bool VTOK, int TW, int MAXW, bool QF16 = false, bool FP4 = false>
+template <bool FP8, int D, int NT, bool VTOK, int TW, int MAXW, bool QF16 = false, bool FP4 = false, bool TV = false>
 __global__ void __launch_bounds__(MAXW * 32, (MAXW == 5 && (D <= 128 || FP8)) ? 2 : 1) pa_tile_kernel(const __grid_constant__ PaParams p,
                                                                       const __grid_constant__ CUtensorMap tmK,
                                                                       const __grid_constant__ CUtensorMap tmV) {
@@ -1851,7 +1896,7 @@ __global__ void __launch_bounds__(MAXW * 32, (MAXW == 5 && (D <= 128 || FP8)) ? 
       cluster_sync_all();
     }
   } else {
-    Consumer<FP8, D, NT, VTOK, TW, QF16, FP4> cons(p, sm);
+    Consumer<FP8, D, NT, VTOK, TW, QF16, FP4, TV> cons(p, sm);
     cons.run();
     if (p.merge == kMergeCluster) {
       cluster_sync_all();

@@ -43,7 +43,7 @@ class DeviceWorkload:
                  max_pages_per_seq=w.max_pages_per_seq, num_pages=w.num_pages,
                  max_context_len=int(w.ctx_lens.max()) if w.batch else 0, kv_dtype=w.kv_dtype,
                  scale_mode=w.scale_mode, causal=int(w.causal), has_sinks=int(w.sinks is not None),
-                 sparse_topk=int(w.topk), q_dtype=int(w.q_dtype))
+                 sparse_topk=int(w.topk), q_dtype=int(w.q_dtype), v_layout=int(w.v_layout))
         f.update(kw)
         return f
 

@@ -32,7 +32,8 @@ def kernel_shape(d):
     # more than 16 rows on dense decode: the tensor-memory consumer (two
     # softmax warpgroups of rh rows, 128-token stages), taken by AUTO
     # (BF16 caches with FP16 queries stay on the tile consumer)
-    supported = d.get("sparse_topk", 0) == 0 and not mx and R > (8 if d["head_dim"] == 256 else 16) and (
+    supported = d.get("sparse_topk", 0) == 0 and not mx and d.get("v_layout", 0) == 0 and R > (
+        8 if d["head_dim"] == 256 else 16) and (
         d["head_dim"] == 128 or (d["kv_dtype"] == 0 and d["head_dim"] == 256)) and not (
         d["kv_dtype"] == 1 and d.get("q_dtype", 0) == 1)
     consumer = d.get("consumer", 0)

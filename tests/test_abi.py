@@ -107,6 +107,12 @@ PLAN_CASES = [
          scale_mode=pa.PA_SCALE_MX_BLOCK),
     desc(num_q_heads=16, num_kv_heads=8, kv_dtype=pa.PA_KV_MXFP4, scale_mode=pa.PA_SCALE_MX_BLOCK,
          merge_mode=pa.PA_MERGE_CLUSTER, schedule=pa.PA_SCHED_PER_UNIT, max_partitions=4),
+    # transposed BF16 V: the tile consumer whatever the row count
+    desc(num_q_heads=64, num_kv_heads=8, kv_dtype=1, scale_mode=0, v_layout=pa.PA_V_TRANSPOSED),
+    desc(batch=32, num_q_heads=64, num_kv_heads=4, query_len=4, page_size=128, kv_dtype=1, scale_mode=0,
+         v_layout=pa.PA_V_TRANSPOSED),
+    desc(num_q_heads=16, num_kv_heads=2, kv_dtype=1, scale_mode=0, head_dim=256, page_size=64,
+         v_layout=pa.PA_V_TRANSPOSED, q_dtype=pa.PA_Q_FP16),
 ]
 
 
@@ -159,6 +165,11 @@ BAD = [
     (dict(kv_dtype=pa.PA_KV_MXFP4, scale_mode=pa.PA_SCALE_MX_BLOCK, consumer=pa.PA_CONSUMER_TMEM,
           num_q_heads=64, num_kv_heads=4), pa.PA_ERR_UNSUPPORTED),  # tile consumer only
     (dict(kv_dtype=3), pa.PA_ERR_INVALID_ARG),
+    (dict(v_layout=pa.PA_V_TRANSPOSED), pa.PA_ERR_UNSUPPORTED),  # FP8 caches: plain V only
+    (dict(kv_dtype=1, scale_mode=0, v_layout=pa.PA_V_TRANSPOSED, sparse_topk=64), pa.PA_ERR_UNSUPPORTED),
+    (dict(kv_dtype=1, scale_mode=0, v_layout=pa.PA_V_TRANSPOSED, consumer=pa.PA_CONSUMER_TMEM, num_q_heads=64,
+          num_kv_heads=4), pa.PA_ERR_UNSUPPORTED),
+    (dict(v_layout=2), pa.PA_ERR_INVALID_ARG),
     (dict(scale_mode=4), pa.PA_ERR_INVALID_ARG),
 ]
 
