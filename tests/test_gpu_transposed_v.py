@@ -66,7 +66,9 @@ def test_transposed_v(orc, case):
     ref = orc.decode(tv)
     dp, dt = DeviceWorkload(plain), DeviceWorkload(tv)
     for m in MODES:
-        out_p, _ = decode(dp, **m)
+        # the plain layout on the same (tile) consumer: AUTO would take the
+        # tensor-memory consumer for more than 16 rows (8 at head_dim 256)
+        out_p, _ = decode(dp, consumer=pa.PA_CONSUMER_TILE, **m)
         out_t, plan = decode(dt, **m)
         assert plan.info["consumer"] == pa.PA_CONSUMER_TILE
         assert_parity(out_t, ref, what=f"transposed V {case} {m}")
@@ -78,6 +80,6 @@ def test_transposed_v_edges(orc, mode):
     lens = [0, 1, 7, 8, 9, 15, 16, 17, 63, 64, 65, 127, 200, 777, 1500, 2049]
     plain, tv = pair((128, 8, 1, 16, 0, False, pw.Q_BF16), 620, lens)
     out_t, _ = decode(DeviceWorkload(tv), **mode)
-    out_p, _ = decode(DeviceWorkload(plain), **mode)
+    out_p, _ = decode(DeviceWorkload(plain), consumer=pa.PA_CONSUMER_TILE, **mode)
     assert_parity(out_t, orc.decode(tv), what=f"transposed V edges {mode}")
     assert np.array_equal(out_t, out_p)
