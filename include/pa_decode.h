@@ -130,13 +130,13 @@ enum {
 };
 
 /* How a stage is consumed. The tile consumer runs mma.sync per 8-row warp
- * (any shape); the tensor-memory consumer issues tcgen05.mma from a dedicated
- * warp with accumulators in TMEM, two softmax warpgroups splitting the rows
- * (dense decode with 17..64 rows per KV head, FP8 head_dim 128/256 or BF16
- * head_dim 128 with BF16 queries; head_dim 256 with 9..32 rows). AUTO takes
- * the tensor-memory
- * consumer wherever it covers the shape (measured faster on every such
- * shape), else the tile consumer. */
+ * (any shape, every cache format and V layout); the tensor-memory consumer
+ * issues tcgen05.mma from a dedicated warp with accumulators in TMEM, two or
+ * four softmax warpgroups splitting the rows (dense decode with 17..64 rows
+ * per KV head, FP8 head_dim 128/256 or BF16 head_dim 128 with BF16 queries
+ * and plain V; head_dim 256 with 9..32 rows; no MXFP4). AUTO takes the
+ * tensor-memory consumer wherever it covers the shape (measured faster on
+ * every such shape), else the tile consumer. */
 enum { PA_CONSUMER_AUTO = 0, PA_CONSUMER_TILE = 1, PA_CONSUMER_TMEM = 2 };
 
 /* How KV chunks are assigned to CTAs. */
