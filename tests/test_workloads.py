@@ -110,3 +110,26 @@ def test_transpose_v_moves_values():
     assert t.shape == (3, 2, 4, 64, 8)
     for p, g, s, d in [(0, 0, 0, 0), (2, 1, 31, 63), (1, 0, 9, 17), (2, 1, 8, 0)]:
         assert t[p, g, s // 8, d, s % 8] == v[p, g, s, d]
+
+
+def test_bench_names_follow_the_options():
+    import argparse
+
+    import bench
+
+    def ns(**kw):
+        d = dict(batch=0, page=16, window=0, sinks=False, partitions=0, merge="auto", consumer="auto",
+                 workload="dense", rows=1024, kv="fp8", ql=1, v_layout="plain")
+        d.update(kw)
+        return argparse.Namespace(**d)
+
+    assert bench.profile_name(ns(), "pa_tile") == "pa_tile_dense"
+    assert bench.profile_name(ns(kv="mxfp4"), "pa_tile") == "pa_tile_dense_mxfp4"
+    assert bench.profile_name(ns(workload="mtp4", kv="bf16"), "pa_mtp") == "pa_mtp_mtp4_bf16"
+    assert bench.profile_name(ns(workload="d256", ql=4), "pa_mtp") == "pa_mtp_d256_ql4"
+    assert bench.profile_name(ns(kv="bf16"), "pa_tile") is None  # no summary covers dense BF16
+    assert bench.profile_name(ns(kv="bf16", v_layout="transposed"), "pa_tile") is None
+    assert bench.profile_name(ns(batch=16), "pa_tile") is None  # a non-default size
+    assert "MXFP4" in bench.workload_name(ns(kv="mxfp4"))
+    assert "transposed" in bench.workload_name(ns(kv="bf16", v_layout="transposed"))
+    assert bench.workload_name(ns()) == bench.WORKLOADS["dense"]
